@@ -1,0 +1,457 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something
+other than itself (hand-worked examples in ``tests/golden/``, brute force with
+exact rational arithmetic, closed forms, and library routines).  The mutation
+tests at the end plant plausible mistakes in the oracle and show that at least
+one pin catches each of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import wq_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# E2M1 magnitudes, sign and magnitude index per code, as the MXFP4 page lists
+# the grid; used only by the brute-force searches below.
+_E2M1_EXACT = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2),
+               Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+
+
+def _e2m1_exact(code):
+    v = _E2M1_EXACT[code & 7]
+    return -v if code & 8 else v
+
+
+def _frac(x):
+    return Fraction(float(x))
+
+
+# ------------------------------------------------------------ weight-only pins
+
+
+def check_w4_worked(gemm=None):
+    gemm = gemm or O.gemm_w4a16
+    g = _load("weight_only_worked.json")["w4a16"]
+    y = gemm(np.array(g["x"], np.float16), np.array(g["w_bytes"], np.uint8), np.array(g["scales"], np.float16))
+    np.testing.assert_array_equal(y, np.array(g["y"]))
+
+
+def check_w8_worked(gemm=None):
+    gemm = gemm or O.gemm_w8a16
+    g = _load("weight_only_worked.json")["w8a16"]
+    y = gemm(np.array(g["x"], np.float16), np.array(g["w"], np.int8), np.array(g["scales"], np.float16))
+    np.testing.assert_array_equal(y, np.array(g["y"]))
+
+
+def test_w4_worked_example():
+    check_w4_worked()
+
+
+def test_w8_worked_example():
+    check_w8_worked()
+
+
+def _brute_w4(x, wq, s):
+    m, k = x.shape
+    n = wq.shape[1]
+    out = np.zeros((m, n))
+    for i in range(m):
+        for j in range(n):
+            acc = Fraction(0)
+            for kk in range(k):
+                byte = int(wq[kk // 2, j])
+                code = (byte >> 4) if kk % 2 else (byte & 15)
+                acc += _frac(x[i, kk]) * (code - 8) * _frac(s[j])
+            out[i, j] = float(acc)
+    return out
+
+
+def check_w4_bruteforce(gemm=None):
+    gemm = gemm or O.gemm_w4a16
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((2, 64)).astype(np.float16)
+    wq = rng.integers(0, 256, (32, 5), dtype=np.uint8)
+    s = rng.uniform(0.005, 0.02, 5).astype(np.float16)
+    np.testing.assert_allclose(gemm(x, wq, s), _brute_w4(x, wq, s), rtol=1e-13, atol=1e-15)
+
+
+def test_w4_bruteforce_exact_rational():
+    check_w4_bruteforce()
+
+
+def test_w8_bruteforce_exact_rational():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((2, 64)).astype(np.float16)
+    w = rng.integers(-128, 128, (64, 5)).astype(np.int8)
+    s = rng.uniform(0.001, 0.01, 5).astype(np.float16)
+    ref = np.zeros((2, 5))
+    for i in range(2):
+        for j in range(5):
+            ref[i, j] = float(sum(_frac(x[i, k]) * int(w[k, j]) * _frac(s[j]) for k in range(64)))
+    np.testing.assert_allclose(O.gemm_w8a16(x, w, s), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_w4_integer_special_case():
+    """Unit scales and integer activations: the result is an exact integer that an
+    integer matmul of the unpacked codes reproduces."""
+    rng = np.random.default_rng(9)
+    xi = rng.integers(-4, 5, (3, 40))
+    codes = rng.integers(0, 16, (40, 6))
+    wq = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+    y = O.gemm_w4a16(xi.astype(np.float16), wq, np.ones(6, np.float16))
+    np.testing.assert_array_equal(y, (xi @ (codes - 8)).astype(np.float64))
+
+
+def test_w8_full_int8_range_and_sign():
+    """-128 and 127 decode to themselves (two's complement, no zero point)."""
+    w = np.array([[-128], [127], [-1]], np.int8)
+    y = O.gemm_w8a16(np.array([[1, 1, 1]], np.float16), w, np.array([1.0], np.float16))
+    assert y[0, 0] == -2.0
+
+
+# ------------------------------------------------------------------ MXFP4 pins
+
+
+@pytest.mark.parametrize("e", [-126, -30, -29, -3, -1, 0, 1, 20, 100, 127])
+def test_ceil_log2_closed_form_around_powers_of_two(e):
+    p = np.float32(2.0) ** np.float32(e) if e > -127 else None
+    above = np.nextafter(p, np.float32(np.inf))
+    below = np.nextafter(p, np.float32(0))
+    got = O.ceil_log2_f32(np.array([p, above, below], np.float32))
+    assert list(got) == [e, e + 1, e]
+
+
+def test_ceil_log2_exact_rational_random():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0x00800000, 0x7F000000, 4000, dtype=np.uint32)
+    q = bits.view(np.float32)
+    got = O.ceil_log2_f32(q)
+    for qi, ei in zip(q[:4000], got):
+        fq = Fraction(float(qi))
+        # ceil(log2 q) = e  <=>  2^(e-1) < q <= 2^e
+        assert Fraction(2) ** (int(ei) - 1) < fq <= Fraction(2) ** int(ei)
+
+
+def check_mx_quantize_golden(quant=None):
+    quant = quant or O.mx_quantize_fp4
+    g = _load("mx_quantize_worked.json")
+    for row in g["rows"]:
+        x = np.array([[float.fromhex(v) for v in row["values"]]], np.float32)
+        data, scales = quant(x)
+        assert list(data[0]) == row["data_bytes"], row["why"]
+        assert int(scales[0, 0]) == row["E"], row["why"]
+
+
+def test_mx_quantize_worked_examples():
+    check_mx_quantize_golden()
+
+
+def _brute_mx_block(vals):
+    """Independent exhaustive quantizer for one 32-element block: the exponent is
+    the smallest integer e with amax/6 <= 2^e (amax clamped at fp32(1e-8)); each
+    element takes the code among all 16 whose value times 2^e is nearest, the
+    smaller magnitude on a tie, and the sign bit of x < 0."""
+    fr = [Fraction(float(v)) for v in vals]
+    amax = max(max(abs(v) for v in fr), Fraction(float(np.float32(1e-8))))
+    e = -200
+    while Fraction(2) ** e < amax / 6:
+        e += 1
+    codes = []
+    for v in fr:
+        best = None
+        for mag in range(8):
+            err = abs(abs(v) - _E2M1_EXACT[mag] * Fraction(2) ** e)
+            if best is None or err < best[0]:
+                best = (err, mag)
+        codes.append((8 if v < 0 else 0) | best[1])
+    return codes, e + 127
+
+
+def check_mx_quantize_bruteforce(quant=None, n_blocks=60):
+    quant = quant or O.mx_quantize_fp4
+    rng = np.random.default_rng(2)
+    rows = []
+    for b in range(n_blocks):
+        scale = np.float32(2.0) ** np.float32(rng.integers(-40, 40))
+        blk = (rng.standard_normal(32) * scale).astype(np.float32)
+        if b % 3 == 0:  # plant exact grid midpoints relative to the block scale
+            amax = np.float32(np.abs(blk).max())
+            e = math.ceil(math.log2(float(amax) / 6.0))
+            mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32) * np.float32(2.0 ** e)
+            blk[:7] = mids * np.where(rng.random(7) < 0.5, -1, 1).astype(np.float32)
+            blk[7] = np.float32(6.0 * 2.0 ** e)
+        rows.append(blk)
+    x = np.stack(rows)
+    data, scales = quant(x)
+    codes = O.mx_unpack_codes(data)
+    for i in range(n_blocks):
+        ref_codes, ref_e = _brute_mx_block(x[i])
+        assert int(scales[i, 0]) == ref_e
+        assert list(codes[i]) == ref_codes
+
+
+def test_mx_quantize_bruteforce_exact_rational():
+    check_mx_quantize_bruteforce()
+
+
+def test_mx_quantize_error_bound_invariant():
+    """Every element lands within half the local grid spacing (times 2^e) of x."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((16, 256)) * 0.5).astype(np.float32)
+    data, scales = O.mx_quantize_fp4(x)
+    xhat = O.mx_dequantize(data, scales)
+    e = np.repeat(scales.astype(np.int64) - 127, 32, axis=1)
+    v = np.abs(x.astype(np.float64)) / np.ldexp(1.0, e)
+    assert v.max() <= 6.0
+    half_gap = np.select([v <= 2, v <= 4], [0.25, 0.5], 1.0)
+    assert np.all(np.abs(x - xhat) <= half_gap * np.ldexp(1.0, e) + 0)
+
+
+def test_mx_e2m1_decode_all_codes():
+    got = O.e2m1_decode(np.arange(16))
+    want = [float(_e2m1_exact(c)) for c in range(16)]
+    assert list(got) == want
+    # each code's value re-quantizes to the same code in a block whose amax is 6
+    blk = np.zeros((1, 32), np.float32)
+    blk[0, :16] = got.astype(np.float32)
+    blk[0, 16] = 6.0
+    data, scales = O.mx_quantize_fp4(blk)
+    codes = O.mx_unpack_codes(data)[0, :16]
+    expect = [c if c != 8 else 0 for c in range(16)]  # -0.0 carries no sign bit
+    assert list(codes) == expect and int(scales[0, 0]) == 127
+
+
+def _one_block(code, e):
+    return np.full((1, 16), code | (code << 4), np.uint8), np.array([[e]], np.uint8)
+
+
+@pytest.mark.parametrize("ea,ew", [(0, 0), (0, 254), (254, 254), (127, 127), (1, 253), (98, 140), (200, 3)])
+def test_mx_gemm_e8m0_exponent_addition(ea, ew):
+    """S_A * S_W = 2^(E_A + E_W - 254): a block of +1.0 codes on both sides gives
+    32 * 2^(E_A + E_W - 254) exactly."""
+    ad, asc = _one_block(2, ea)
+    wd, wsc = _one_block(2, ew)
+    c = O.mx_gemm_fp4(ad, asc, wd, wsc)
+    assert c[0, 0] == math.ldexp(32.0, ea + ew - 254)
+
+
+def test_mx_e8m0_identity_exhaustive():
+    """2^(E_A-127) * 2^(E_W-127) == 2^(E_A+E_W-254) for every E_A, E_W in 0..254."""
+    ea = np.arange(255)[:, None]
+    ew = np.arange(255)[None, :]
+    lhs = np.ldexp(1.0, ea - 127) * np.ldexp(1.0, ew - 127)
+    rhs = np.ldexp(1.0, ea + ew - 254)
+    assert np.array_equal(lhs, rhs)
+
+
+def check_mx_gemm_worked(gemm=None):
+    gemm = gemm or O.mx_gemm_fp4
+    g = _load("mx_gemm_worked.json")
+    c = gemm(np.array(g["a_data"], np.uint8), np.array(g["a_scales"], np.uint8),
+             np.array(g["w_data"], np.uint8), np.array(g["w_scales"], np.uint8))
+    np.testing.assert_array_equal(c, np.array(g["c"]))
+
+
+def test_mx_gemm_worked_example():
+    check_mx_gemm_worked()
+
+
+def check_mx_gemm_bruteforce(gemm=None):
+    """2 x 64 against 2 x 64, the MXFP4 page's own demo shape, in exact rationals."""
+    gemm = gemm or O.mx_gemm_fp4
+    rng = np.random.default_rng(4)
+    ad = rng.integers(0, 256, (2, 32), dtype=np.uint8)
+    wd = rng.integers(0, 256, (3, 32), dtype=np.uint8)
+    asc = rng.integers(110, 140, (2, 2), dtype=np.uint8)
+    wsc = rng.integers(110, 140, (3, 2), dtype=np.uint8)
+    ref = np.zeros((2, 3))
+    for m in range(2):
+        for n in range(3):
+            acc = Fraction(0)
+            for kb in range(2):
+                dot = Fraction(0)
+                for i in range(32):
+                    t = kb * 16 + i // 2
+                    ca = (int(ad[m, t]) >> 4) if i % 2 else (int(ad[m, t]) & 15)
+                    cw = (int(wd[n, t]) >> 4) if i % 2 else (int(wd[n, t]) & 15)
+                    dot += _e2m1_exact(ca) * _e2m1_exact(cw)
+                acc += dot * Fraction(2) ** (int(asc[m, kb]) + int(wsc[n, kb]) - 254)
+            ref[m, n] = float(acc)
+    np.testing.assert_allclose(gemm(ad, asc, wd, wsc), ref, rtol=1e-15, atol=0)
+
+
+def test_mx_gemm_bruteforce_exact_rational():
+    check_mx_gemm_bruteforce()
+
+
+def test_mx_gemm_equals_dequantize_then_matmul():
+    rng = np.random.default_rng(5)
+    a = (rng.standard_normal((4, 128)) * 0.5).astype(np.float32)
+    w = (rng.standard_normal((6, 128)) * 0.5).astype(np.float32)
+    ad, asc = O.mx_quantize_fp4(a)
+    wd, wsc = O.mx_quantize_fp4(w)
+    c = O.mx_gemm_fp4(ad, asc, wd, wsc)
+    np.testing.assert_allclose(c, O.mx_dequantize(ad, asc) @ O.mx_dequantize(wd, wsc).T, rtol=1e-14)
+    sub = O.mx_gemm_fp4(ad, asc, wd, wsc, rows=np.array([3, 1]))
+    np.testing.assert_array_equal(sub, c[[3, 1]])
+
+
+# -------------------------------------------------------------------- FP8 pins
+
+
+def test_e4m3_decode_all_codes_against_torch():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+    got = O.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_e4m3_range_closed_form():
+    v = O.e4m3_decode(np.arange(256))
+    assert np.nanmax(v) == 448.0 and np.nanmin(v) == -448.0
+    assert v[0x01] == 2.0 ** -9 and v[0x38] == 1.0 and v[0x08] == 2.0 ** -6
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.sum(np.isnan(v)) == 2
+
+
+def check_fp8_worked(gemm=None):
+    gemm = gemm or O.fp8_gemm
+    for case in _load("fp8_worked.json")["cases"]:
+        c = gemm(np.array(case["a"], np.uint8), np.array(case["b"], np.uint8), case["scale_a"], case["scale_b"])
+        np.testing.assert_array_equal(c, np.array(case["c"]))
+
+
+def test_fp8_worked_examples():
+    check_fp8_worked()
+
+
+def test_fp8_identity_reproduces_b():
+    rng = np.random.default_rng(6)
+    b = rng.integers(0, 256, (8, 5), dtype=np.uint8)
+    b[(b & 0x7F) == 0x7F] = 0x38
+    eye = np.where(np.eye(8, dtype=bool), 0x38, 0).astype(np.uint8)
+    c = O.fp8_gemm(eye, b, 0.5, 3.0)
+    np.testing.assert_array_equal(c, O.e4m3_decode(b) * 1.5)
+
+
+def test_fp8_bruteforce_exact_rational():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(10)
+    a = rng.integers(0, 256, (2, 64), dtype=np.uint8)
+    b = rng.integers(0, 256, (64, 3), dtype=np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0
+    b[(b & 0x7F) == 0x7F] = 0
+    dec = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    sa, sb = np.float32(0.37), np.float32(1.9)
+    ref = np.zeros((2, 3))
+    for m in range(2):
+        for n in range(3):
+            acc = sum(Fraction(float(dec[a[m, k]])) * Fraction(float(dec[b[k, n]])) for k in range(64))
+            ref[m, n] = float(acc * Fraction(float(sa)) * Fraction(float(sb)))
+    np.testing.assert_allclose(O.fp8_gemm(a, b, sa, sb), ref, rtol=1e-14, atol=0)
+
+
+# ----------------------------------------------------------- tolerance helper
+
+
+def test_ulp_matches_numpy_spacing():
+    for dt, name in ((np.float16, "fp16"), (np.float32, "fp32")):
+        vals = np.array([1.0, 1.5, 1000.0, 3e-3, 0.0, -7.25], dt)
+        np.testing.assert_array_equal(O.ulp(vals, name), np.abs(np.spacing(np.abs(vals))).astype(np.float64))
+    assert O.ulp(np.array([1.0]), "bf16")[0] == 2.0 ** -7
+
+
+# -------------------------------------------------------------- mutation tests
+# Each plants one plausible mistake in the oracle (on the CPU) and checks that
+# the pins above catch it.
+
+
+def _mutant_w4_swapped_nibbles(x, wq, s):
+    q = O.unpack_int4(wq)
+    q2 = q.copy()
+    q2[0::2], q2[1::2] = q[1::2], q[0::2]
+    return x.astype(np.float64) @ ((q2 - 8) * s.astype(np.float64))
+
+
+def _mutant_w4_zero_point_7(x, wq, s):
+    return x.astype(np.float64) @ ((O.unpack_int4(wq) - 7) * s.astype(np.float64))
+
+
+def _mutant_w4_transposed_scale(x, wq, s):
+    return x.astype(np.float64) @ (O.unpack_int4(wq) - 8).astype(np.float64) * float(s.astype(np.float64).mean())
+
+
+def _mutant_mx_ties_up(src):
+    x = np.asarray(src, np.float32)
+    rows, cols = x.shape
+    blocks = x.reshape(rows, cols // 32, 32)
+    amax = np.maximum(np.abs(blocks).max(-1), O.AMAX_FLOOR)
+    e = O.ceil_log2_f32((amax / np.float32(6)).astype(np.float32))
+    v = np.abs(blocks / np.ldexp(np.float32(1), e)[..., None])
+    grid = np.asarray(O.E2M1_GRID, np.float32)
+    dist = np.abs(v[..., None] - grid)
+    j = 7 - np.argmin(dist[..., ::-1], axis=-1)  # last index on ties
+    codes = (((blocks < 0).astype(np.uint8) << 3) | j.astype(np.uint8)).reshape(rows, cols)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), (e + 127).astype(np.uint8)
+
+
+def _mutant_mx_floor_exponent(src):
+    x = np.asarray(src, np.float32)
+    d, s = O.mx_quantize_fp4(x)
+    amax = np.maximum(np.abs(x.reshape(x.shape[0], -1, 32)).max(-1), O.AMAX_FLOOR)
+    e = np.floor(np.log2(amax / 6.0)).astype(np.int64)
+    return d, (e + 127).astype(np.uint8)
+
+
+def _mutant_mx_no_clamp(src):
+    x = np.asarray(src, np.float32)
+    saved = O.AMAX_FLOOR
+    try:
+        O.AMAX_FLOOR = np.float32(1e-38)
+        return O.mx_quantize_fp4(x)
+    finally:
+        O.AMAX_FLOOR = saved
+
+
+def _mutant_mx_gemm_bias_127(ad, asc, wd, wsc, rows=None):
+    return O.mx_gemm_fp4(ad, asc, wd, wsc) * 2.0 ** 127
+
+
+def _mutant_mx_gemm_transposed_blocks(ad, asc, wd, wsc, rows=None):
+    return O.mx_gemm_fp4(ad, asc[:, ::-1], wd, wsc)
+
+
+def _mutant_fp8_no_subnormals(a, b, sa, sb, rows=None):
+    da = O.e4m3_decode(a)
+    da = np.where((np.asarray(a) & 0x78) == 0, 0.0, da)
+    return (da @ O.e4m3_decode(b)) * sa * sb
+
+
+@pytest.mark.parametrize("mutant,checks", [
+    (_mutant_w4_swapped_nibbles, [check_w4_worked, check_w4_bruteforce]),
+    (_mutant_w4_zero_point_7, [check_w4_worked, check_w4_bruteforce]),
+    (_mutant_w4_transposed_scale, [check_w4_worked, check_w4_bruteforce]),
+    (_mutant_mx_ties_up, [check_mx_quantize_golden, check_mx_quantize_bruteforce]),
+    (_mutant_mx_floor_exponent, [check_mx_quantize_golden, check_mx_quantize_bruteforce]),
+    (_mutant_mx_no_clamp, [check_mx_quantize_golden]),
+    (_mutant_mx_gemm_bias_127, [check_mx_gemm_worked, check_mx_gemm_bruteforce]),
+    (_mutant_mx_gemm_transposed_blocks, [check_mx_gemm_worked, check_mx_gemm_bruteforce]),
+    (_mutant_fp8_no_subnormals, [check_fp8_worked]),
+])
+def test_pins_catch_planted_mistakes(mutant, checks):
+    for check in checks:
+        with pytest.raises(AssertionError):
+            check(mutant)
