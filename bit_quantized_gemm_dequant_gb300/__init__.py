@@ -1,0 +1,181 @@
+"""Python binding of libwq, the GB300 fused dequantization GEMM library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libwq.so`` (built in-tree by ``build.py``).  The functions keep
+the C ABI's names and take PyTorch CUDA tensors, which are used for device
+memory and streams; pointers, leading dimensions and the current stream are
+passed through ``ctypes``.  There is no CPU fallback: importing this package
+without a built ``libwq.so`` raises, and every non-zero status raises
+``WqError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwq.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "wq.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libwq.so is not built ({LIB_PATH} missing); run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` first")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+WQ_OK = 0
+WQ_ERR_INVALID_ARG = 1
+WQ_ERR_MISALIGNED = 2
+WQ_ERR_UNSUPPORTED = 3
+WQ_ERR_WORKSPACE = 4
+WQ_ERR_LAUNCH = 5
+WQ_ERR_DEVICE = 6
+
+WQ_OP_W4A16, WQ_OP_W8A16, WQ_OP_MX_QUANTIZE, WQ_OP_MX_GEMM, WQ_OP_FP8_GEMM = range(5)
+
+_i, _i64, _p, _sz, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+_SIGS = {
+    "wq_gemm_w4a16": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
+    "wq_gemm_w8a16": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
+    "mx_quantize_fp4": [_i, _i, _p, _i64, _p, _i64, _p, _i64, _p],
+    "mx_gemm_fp4": [_i, _i, _i, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _sz, _p],
+    "fp8_gemm": [_i, _i, _i, _p, _i64, _p, _i64, _f, _f, _p, _i64, _p, _sz, _p],
+    "wq_workspace_size": [_i, _i, _i, _i],
+    "wq_status_string": [_i],
+    "wq_get_device_error": [_p, ctypes.POINTER(_i)],
+    "wq_version": [],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _i
+lib.wq_workspace_size.restype = _sz
+lib.wq_status_string.restype = ctypes.c_char_p
+
+
+class WqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.wq_status_string(status).decode()}")
+
+
+def header_functions(path: str = HEADER_PATH) -> list[str]:
+    """Names of the functions include/wq.h declares."""
+    with open(path) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def _check(status: int, where: str) -> None:
+    if status != WQ_OK:
+        raise WqError(status, where)
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _ld(t):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise WqError(WQ_ERR_UNSUPPORTED, "matrices must be 2-D with unit inner stride")
+    return t.stride(0)
+
+
+def _ws(workspace):
+    return (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (_p(0), 0)
+
+
+def wq_gemm_w4a16(x, wq, scales, y=None, workspace=None, stream=None):
+    """Y fp16 [M, N] = X fp16 [M, K] * ((unpack(wq [K/2, N]) - 8) * scales[N])."""
+    import torch
+
+    M, K = x.shape
+    N = wq.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    wsp, wsb = _ws(workspace)
+    _check(lib.wq_gemm_w4a16(M, N, K, _ptr(x), _ld(x), _ptr(wq), _ld(wq), _ptr(scales), _ptr(y), _ld(y),
+                             wsp, wsb, _stream(stream)), "wq_gemm_w4a16")
+    return y
+
+
+def wq_gemm_w8a16(x, w, scales, y=None, workspace=None, stream=None):
+    """Y fp16 [M, N] = X fp16 [M, K] * (w int8 [K, N] * scales[N])."""
+    import torch
+
+    M, K = x.shape
+    N = w.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    wsp, wsb = _ws(workspace)
+    _check(lib.wq_gemm_w8a16(M, N, K, _ptr(x), _ld(x), _ptr(w), _ld(w), _ptr(scales), _ptr(y), _ld(y),
+                             wsp, wsb, _stream(stream)), "wq_gemm_w8a16")
+    return y
+
+
+def mx_quantize_fp4(src, data=None, scales=None, stream=None):
+    """fp32 [R, C] -> (uint8 data [R, C/2], uint8 E8M0 scales [R, C/32])."""
+    import torch
+
+    R, C = src.shape
+    if data is None:
+        data = torch.empty((R, C // 2), dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty((R, C // 32), dtype=torch.uint8, device=src.device)
+    _check(lib.mx_quantize_fp4(R, C, _ptr(src), _ld(src), _ptr(data), _ld(data), _ptr(scales), _ld(scales),
+                               _stream(stream)), "mx_quantize_fp4")
+    return data, scales
+
+
+def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
+    """C fp32 [M, N] = A * W^T for MXFP4 operands (data [rows, K/2] + scales [rows, K/32])."""
+    import torch
+
+    M, N, K = a.shape[0], w.shape[0], a.shape[1] * 2
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    wsp, wsb = _ws(workspace)
+    _check(lib.mx_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
+                           _ptr(c), _ld(c), wsp, wsb, _stream(stream)), "mx_gemm_fp4")
+    return c
+
+
+def fp8_gemm(a, b, scale_a, scale_b, c=None, workspace=None, stream=None):
+    """C bf16 [M, N] = (A e4m3 [M, K] * B e4m3 [K, N]) * scale_a * scale_b."""
+    import torch
+
+    M, K = a.shape
+    N = b.shape[1]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    wsp, wsb = _ws(workspace)
+    _check(lib.fp8_gemm(M, N, K, _ptr(a), _ld(a), _ptr(b), _ld(b), float(scale_a), float(scale_b), _ptr(c), _ld(c),
+                        wsp, wsb, _stream(stream)), "fp8_gemm")
+    return c
+
+
+def wq_workspace_size(op: int, M: int, N: int, K: int) -> int:
+    return int(lib.wq_workspace_size(op, M, N, K))
+
+
+def wq_status_string(status: int) -> str:
+    return lib.wq_status_string(status).decode()
+
+
+def wq_get_device_error(stream=None) -> tuple[int, int]:
+    site = _i(0)
+    st = lib.wq_get_device_error(_stream(stream), ctypes.byref(site))
+    return st, site.value
+
+
+def wq_version() -> int:
+    return int(lib.wq_version())

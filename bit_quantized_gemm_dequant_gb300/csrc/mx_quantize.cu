@@ -1,0 +1,99 @@
+// MXFP4 quantizer: FP32 rows -> 32-element E2M1 blocks + E8M0 scales.
+//
+// Defined by "量化推理引擎中的微缩放格式前瞻：MXFP4 矩阵乘法 Kernel 原理", §三
+// (pack_tensor_to_mxfp4_layout): per 32-element block, amax clamped at 1e-8,
+// e = ceil(log2(amax / 6)), v = x / 2^e, nearest E2M1 grid point with the
+// first (smaller) one on a tie.  §一: data and scale segments are separate.
+//
+// HBM-bound: 4 B read + 0.5 B + 1/32 B written per element.  Four threads
+// own one block: each loads 32 contiguous bytes (two 128-bit loads), the
+// block amax is a 4-lane shuffle max, and each thread stores one 32-bit word
+// of packed codes, so a warp reads 1 KB and writes 128 B contiguously.
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 2;  // blocks in flight per thread quad
+
+__device__ __forceinline__ uint32_t e2m1_code(float x, float inv_scale) {
+  // v = x * 2^-e is exact (a power-of-two scaling); the comparisons below
+  // count the grid midpoints strictly below |v|, so a value exactly on a
+  // midpoint takes the smaller grid point — the first index of the argmin.
+  const float a = fabsf(x * inv_scale);
+  uint32_t j = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) +
+               (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
+  return (x < 0.0f ? 8u : 0u) | j;
+}
+
+__global__ void __launch_bounds__(kThreads)
+mx_quantize_kernel(MxQuantArgs p, int64_t n_items) {
+  // A warp owns 8 consecutive blocks (1 KB of source) per step; the loop
+  // bound is warp-uniform so that every lane reaches the quad shuffles.
+  const int lane = threadIdx.x & 31;
+  const int quad_lane = lane & 3;
+  const int64_t blocks_per_row = p.cols / 32;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const int64_t step = n_warps * 8;
+
+  for (int64_t base = warp0 * 8; base < n_items; base += step * kUnroll) {
+    float4 v[kUnroll][2];
+    int64_t item[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      item[u] = base + u * step + (lane >> 2);
+      if (item[u] < n_items) {
+        const int64_t r = item[u] / blocks_per_row;
+        const int64_t b = item[u] - r * blocks_per_row;
+        const float4* src = reinterpret_cast<const float4*>(p.src + r * p.ld_src + b * 32 + quad_lane * 8);
+        v[u][0] = __ldcs(src);
+        v[u][1] = __ldcs(src + 1);
+      } else {
+        v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const float xs[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                           v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xs[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, 1e-8f);
+      // q = amax / 6 rounded to FP32; ceil(log2 q) read off its bits: the
+      // unbiased exponent, plus one unless q is an exact power of two.  q is
+      // normal because amax >= 1e-8.
+      const uint32_t qb = __float_as_uint(__fdiv_rn(amax, 6.0f));
+      const int e = static_cast<int>((qb >> 23) & 0xFF) - 127 + ((qb & 0x7FFFFFu) != 0u);
+      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) word |= e2m1_code(xs[i], inv_scale) << (4 * i);
+      if (item[u] < n_items) {
+        const int64_t r = item[u] / blocks_per_row;
+        const int64_t b = item[u] - r * blocks_per_row;
+        *reinterpret_cast<uint32_t*>(p.data + r * p.ld_data + b * 16 + quad_lane * 4) = word;
+        if (quad_lane == 0) p.scales[r * p.ld_scales + b] = static_cast<uint8_t>(e + 127);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s) {
+  const int64_t n_items = static_cast<int64_t>(a.rows) * (a.cols / 32);
+  if (n_items == 0) return cudaSuccess;
+  const int64_t blocks_per_cta = kThreads / 4;  // one 32-element block per thread quad
+  int64_t ctas = (n_items + blocks_per_cta * kUnroll - 1) / (blocks_per_cta * kUnroll);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // 8 resident CTAs per SM
+  if (ctas > cap) ctas = cap;
+  mx_quantize_kernel<<<static_cast<unsigned>(ctas), kThreads, 0, s>>>(a, n_items);
+  return cudaGetLastError();
+}
+
+}  // namespace wq

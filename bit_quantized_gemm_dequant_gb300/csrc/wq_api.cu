@@ -1,0 +1,175 @@
+// C ABI of libwq: host-side argument validation and shape dispatch.  Every
+// entry point checks its arguments before any CUDA call and returns a WQ_*
+// status; no exception crosses the boundary.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "wq_internal.h"
+
+namespace wq {
+
+namespace {
+__device__ int g_device_error;  // first site code recorded by a bounded wait
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return WQ_OK;
+  cudaGetLastError();  // clear the sticky-free launch error so later calls are unaffected
+  return WQ_ERR_LAUNCH;
+}
+}  // namespace
+
+int* device_error_word() {
+  static int* ptr = nullptr;
+  static int dev = -1;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (ptr == nullptr || cur != dev) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptr = static_cast<int*>(p);
+    dev = cur;
+  }
+  return ptr;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+// Shared validation of the weight-only GEMMs.
+static int check_weight_only(int M, int N, int K, const void* X, int64_t ldx, const void* W, int64_t ldw,
+                             const void* scales, const void* Y, int64_t ldy) {
+  if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQ_OK;
+  if (!Y || !scales || (K > 0 && (!X || !W))) return WQ_ERR_INVALID_ARG;
+  if (K % 2) return WQ_ERR_INVALID_ARG;
+  if (ldy < N || (K > 0 && ldx < K)) return WQ_ERR_INVALID_ARG;
+  if (!aligned(Y, 16) || !aligned(scales, 2) || ldy % 8) return WQ_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(X, 16) || !aligned(W, 16) || ldx % 8 || ldw % 16)) return WQ_ERR_MISALIGNED;
+  return WQ_OK;
+}
+
+static int run_weight_only(int bits, int M, int N, int K, const void* X, int64_t ldx, const void* W, int64_t ldw,
+                           const void* scales, void* Y, int64_t ldy, cudaStream_t s) {
+  if (M == 0 || N == 0) return WQ_OK;
+  WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy};
+  if (M <= wo_skinny_max_m()) return launch_status(launch_wo_skinny(a, bits, s));
+  return launch_status(launch_wo_gemm(a, bits, s));
+}
+
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+int wq_gemm_w4a16(int M, int N, int K, const void* X, int64_t ldx, const uint8_t* Wq, int64_t ldw,
+                  const void* scales, void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                  wq_stream_t stream) {
+  (void)workspace;
+  int st = check_weight_only(M, N, K, X, ldx, Wq, ldw, scales, Y, ldy);
+  if (st != WQ_OK || M == 0 || N == 0) return st;
+  if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
+  if (ws_bytes < wq_workspace_size(WQ_OP_W4A16, M, N, K)) return WQ_ERR_WORKSPACE;
+  return run_weight_only(4, M, N, K, X, ldx, Wq, ldw, scales, Y, ldy, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                  const void* scales, void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                  wq_stream_t stream) {
+  (void)workspace;
+  if (K % 2 && K > 0 && M >= 0 && N >= 0) return WQ_ERR_UNSUPPORTED;
+  int st = check_weight_only(M, N, K, X, ldx, W, ldw, scales, Y, ldy);
+  if (st != WQ_OK || M == 0 || N == 0) return st;
+  if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
+  if (ws_bytes < wq_workspace_size(WQ_OP_W8A16, M, N, K)) return WQ_ERR_WORKSPACE;
+  return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_t* data, int64_t ld_data,
+                    uint8_t* scales, int64_t ld_scales, wq_stream_t stream) {
+  if (rows < 0 || cols < 0 || cols % 32) return WQ_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return WQ_OK;
+  if (!src || !data || !scales) return WQ_ERR_INVALID_ARG;
+  if (ld_src < cols || ld_data < cols / 2 || ld_scales < cols / 32) return WQ_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || ld_src % 4 || !aligned(data, 4) || ld_data % 4) return WQ_ERR_MISALIGNED;
+  MxQuantArgs a{rows, cols, src, ld_src, data, ld_data, scales, ld_scales};
+  return launch_status(launch_mx_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* SA, int64_t ldsa,
+                const uint8_t* W, int64_t ldw, const uint8_t* SW, int64_t ldsw, float* C, int64_t ldc,
+                void* workspace, size_t ws_bytes, wq_stream_t stream) {
+  (void)workspace;
+  if (M < 0 || N < 0 || K < 0 || K % 32) return WQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQ_OK;
+  if (!C || (K > 0 && (!A || !SA || !W || !SW))) return WQ_ERR_INVALID_ARG;
+  if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2 || ldsa < K / 32 || ldsw < K / 32))) return WQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || lda % 16 || ldw % 16 || ldc % 4)
+    return WQ_ERR_MISALIGNED;
+  if (ws_bytes < wq_workspace_size(WQ_OP_MX_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
+  MxGemmArgs a{M, N, K, A, lda, SA, ldsa, W, ldw, SW, ldsw, C, ldc};
+  return launch_status(launch_mx_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb, float scale_a,
+             float scale_b, void* C, int64_t ldc, void* workspace, size_t ws_bytes, wq_stream_t stream) {
+  (void)workspace;
+  if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQ_OK;
+  if (!C || (K > 0 && (!A || !B))) return WQ_ERR_INVALID_ARG;
+  if (ldc < N || (K > 0 && (lda < K || ldb < N))) return WQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || lda % 16 || ldb % 16 || ldc % 8)
+    return WQ_ERR_MISALIGNED;
+  if (ws_bytes < wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
+  Fp8GemmArgs a{M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc};
+  return launch_status(launch_fp8_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t wq_workspace_size(int op, int M, int N, int K) {
+  (void)op; (void)M; (void)N; (void)K;
+  return 0;
+}
+
+const char* wq_status_string(int status) {
+  switch (status) {
+    case WQ_OK: return "WQ_OK";
+    case WQ_ERR_INVALID_ARG: return "WQ_ERR_INVALID_ARG: null pointer, negative size, bad multiple or leading dimension";
+    case WQ_ERR_MISALIGNED: return "WQ_ERR_MISALIGNED: pointer or leading dimension breaks the alignment rule";
+    case WQ_ERR_UNSUPPORTED: return "WQ_ERR_UNSUPPORTED: shape form not served";
+    case WQ_ERR_WORKSPACE: return "WQ_ERR_WORKSPACE: workspace smaller than wq_workspace_size()";
+    case WQ_ERR_LAUNCH: return "WQ_ERR_LAUNCH: CUDA launch error";
+    case WQ_ERR_DEVICE: return "WQ_ERR_DEVICE: a kernel gave up a bounded wait";
+    default: return "WQ_ERR_UNKNOWN";
+  }
+}
+
+int wq_get_device_error(wq_stream_t stream, int* site) {
+  int* word = device_error_word();
+  if (!word) return WQ_ERR_LAUNCH;
+  int host = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&host, word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return WQ_ERR_LAUNCH;
+  if (cudaMemsetAsync(word, 0, sizeof(int), s) != cudaSuccess) return WQ_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return WQ_ERR_LAUNCH;
+  if (site) *site = host;
+  return host ? WQ_ERR_DEVICE : WQ_OK;
+}
+
+int wq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal declarations shared by the libwq translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/wq.h"
+
+namespace wq {
+
+// Device error word written by kernels whose bounded waits give up.  Lives in
+// wq_api.cu; kernels receive its device address as a parameter.
+int* device_error_word();
+
+// Site codes recorded in the device error word.
+enum ErrorSite : int {
+  kSiteNone = 0,
+  kSiteGemmProducer = 1,   // TMA producer waited too long for a free stage
+  kSiteGemmMma = 2,        // MMA issuer waited too long for a full stage
+  kSiteGemmEpilogue = 3,   // epilogue waited too long for the accumulator
+  kSiteGemmTmemFree = 4,   // MMA issuer waited too long for the epilogue
+};
+
+struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
+  int M, N, K;
+  const void* X; int64_t ldx;
+  const void* W; int64_t ldw;
+  const void* scales;
+  void* Y; int64_t ldy;
+};
+
+struct MxQuantArgs {
+  int rows, cols;
+  const float* src; int64_t ld_src;
+  uint8_t* data; int64_t ld_data;
+  uint8_t* scales; int64_t ld_scales;
+};
+
+struct MxGemmArgs {
+  int M, N, K;
+  const uint8_t* A; int64_t lda;
+  const uint8_t* SA; int64_t ldsa;
+  const uint8_t* W; int64_t ldw;
+  const uint8_t* SW; int64_t ldsw;
+  float* C; int64_t ldc;
+};
+
+struct Fp8GemmArgs {
+  int M, N, K;
+  const uint8_t* A; int64_t lda;
+  const uint8_t* B; int64_t ldb;
+  float scale_a, scale_b;
+  void* C; int64_t ldc;
+};
+
+// Launchers (one per kernel family).  Each returns a cudaError_t from the
+// launch; argument validation happened in wq_api.cu.
+cudaError_t launch_wo_skinny(const WoArgs& a, int bits, cudaStream_t s);
+cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s);
+cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s);
+cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s);
+cudaError_t launch_fp8_gemm(const Fp8GemmArgs& a, cudaStream_t s);
+
+// Shape dispatch: the largest M the skinny (split-K, register-dequant) path
+// takes; larger M goes to the tiled tensor-memory GEMM.
+int wo_skinny_max_m();
+
+int sm_count();
+
+}  // namespace wq

@@ -1,0 +1,195 @@
+/*
+ * wq.h — C ABI of libwq, a fused on-the-fly-dequantization GEMM library for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Pages the operations are defined by (cited by title and section):
+ *   [W4A16]  "Triton 工业级融合微算子编写：W4A16 极速切片矩阵乘与 Blackwell NVFP4
+ *            硬件指令实装", §二 fused W4A16 kernel.
+ *   [MXFP4]  "量化推理引擎中的微缩放格式前瞻：MXFP4 矩阵乘法 Kernel 原理", §一
+ *            micro-block layout, §二 tiling equations, §三 simulator.
+ *   [W8A16]  "Triton 量化算子：W8A16 权重量化融合矩阵乘法 (Quantization GEMM)",
+ *            Step 1 formula, Step 3 signature and layout, reference solution.
+ *   [FP8]    "通过 CUTLASS 命名约定在 Triton 中实现 FP8 GEMM 内核", kernel
+ *            listing and the 精度管理 (precision management) bullet.
+ *
+ * Conventions for every entry point below
+ *   - Matrices are row-major.  A leading dimension ("ld*") is the distance in
+ *     ELEMENTS between consecutive rows (bytes for the uint8 arrays); the
+ *     inner stride is always 1.  Non-unit inner strides are not expressible.
+ *   - All array pointers are DEVICE pointers (cudaMalloc'd or otherwise
+ *     device-accessible).  The caller owns every buffer, including the
+ *     optional workspace; the library allocates nothing and keeps no pointer
+ *     after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Inputs must stay valid and outputs untouched until the stream
+ *     work completes.  Outputs must not alias inputs.
+ *   - Every call validates its arguments on the host before launching.  On an
+ *     invalid argument it returns a WQ_ERR_* code and launches nothing.  No
+ *     C++ exception crosses this boundary.
+ *   - M, N or K equal to 0 is a valid empty problem: nothing is launched and
+ *     WQ_OK is returned (for K == 0 with M, N > 0 the GEMMs write zeros).
+ *   - Inputs must be finite; NaN/Inf inputs give unspecified (but in-bounds)
+ *     results.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t / CUstream, so either may be passed. */
+typedef struct CUstream_st* wq_stream_t;
+
+/* Status codes. */
+#define WQ_OK 0
+#define WQ_ERR_INVALID_ARG 1  /* null pointer, negative size, ld < row width, bad K multiple */
+#define WQ_ERR_MISALIGNED 2   /* base pointer or leading dimension breaks the 16-byte rule */
+#define WQ_ERR_UNSUPPORTED 3  /* shape form the kernels do not serve (documented per call) */
+#define WQ_ERR_WORKSPACE 4    /* workspace smaller than wq_workspace_size() */
+#define WQ_ERR_LAUNCH 5       /* CUDA reported an error when launching */
+#define WQ_ERR_DEVICE 6       /* a kernel gave up a bounded wait (see wq_get_device_error) */
+
+/* Operation ids for wq_workspace_size(). */
+#define WQ_OP_W4A16 0
+#define WQ_OP_W8A16 1
+#define WQ_OP_MX_QUANTIZE 2
+#define WQ_OP_MX_GEMM 3
+#define WQ_OP_FP8_GEMM 4
+
+/*
+ * wq_gemm_w4a16 — Y = X * ((q - 8) * s), INT4 weights dequantized on chip.
+ *
+ * [W4A16] §二: the packed INT4 weight byte row k/2 holds the codes of k and
+ * k+1; the code of k is (byte >> ((k % 2) * 4)) & 0xF (even k in the low
+ * nibble); the weight is (q - 8) * s[n]; products accumulate in FP32 and the
+ * result is stored as FP16.  The dequantized weight never leaves the chip.
+ *
+ *   M, N, K  problem size; K must be even (two codes per byte).
+ *   X        fp16 [M, K], row stride ldx (elements, ldx >= K).
+ *   Wq       uint8 [K/2, N], row stride ldw (bytes, ldw >= N).
+ *   scales   fp16 [N], one per output column.
+ *   Y        fp16 [M, N] output, row stride ldy (elements, ldy >= N).
+ *   workspace, ws_bytes  scratch of at least wq_workspace_size(WQ_OP_W4A16,
+ *            M, N, K) bytes (0 for every shape served today: the split-K
+ *            partial sums are reduced inside thread-block clusters).
+ * Alignment: X, Wq, Y 16-byte aligned; ldx and ldy multiples of 8; ldw a
+ * multiple of 16; scales 2-byte aligned.  Otherwise WQ_ERR_MISALIGNED.
+ */
+int wq_gemm_w4a16(int M, int N, int K, const void* X, int64_t ldx,
+                  const uint8_t* Wq, int64_t ldw, const void* scales,
+                  void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                  wq_stream_t stream);
+
+/*
+ * wq_gemm_w8a16 — Y = X * (W_int8 * S), INT8 weights dequantized on chip.
+ *
+ * [W8A16] Step 1 (Y = X x (W_int8 x S)) and Step 3 (X fp16 [M, K], W int8
+ * [K, N], S fp16 [N] one scale per column, Y fp16 [M, N]); symmetric, no zero
+ * point; FP32 accumulation as in the reference solution.
+ *
+ *   M, N, K  problem size; K must be even (the kernels pair K rows).
+ *   X        fp16 [M, K], row stride ldx (elements).
+ *   W        int8 [K, N], row stride ldw (bytes).
+ *   scales   fp16 [N].
+ *   Y        fp16 [M, N], row stride ldy (elements).
+ *   workspace, ws_bytes  as for wq_gemm_w4a16.
+ * Alignment: as for wq_gemm_w4a16.  Odd K returns WQ_ERR_UNSUPPORTED.
+ */
+int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx,
+                  const int8_t* W, int64_t ldw, const void* scales,
+                  void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                  wq_stream_t stream);
+
+/*
+ * mx_quantize_fp4 — quantize FP32 rows to MXFP4 (E2M1 elements, E8M0 scales).
+ *
+ * [MXFP4] §三 simulator, per 32-element block of each row:
+ *   amax = max(max|x|, 1e-8); e = ceil(log2(amax / 6)) (exact, amax/6 in
+ *   FP32); E = e + 127; v = x / 2^e; magnitude index j = nearest point of
+ *   {0, .5, 1, 1.5, 2, 3, 4, 6} to |v|, the smaller one on a tie; sign bit set
+ *   when x < 0; code = sign << 3 | j.
+ * [MXFP4] §一: data and scale segments are separate arrays.
+ *
+ *   rows, cols  source size; cols must be a multiple of 32.
+ *   src         fp32 [rows, cols], row stride ld_src (elements).
+ *   data        uint8 [rows, cols/2] output: element 2t in the low nibble and
+ *               2t+1 in the high nibble of byte t; row stride ld_data (bytes).
+ *   scales      uint8 [rows, cols/32] output E8M0 bytes; row stride ld_scales.
+ * Alignment: src 16-byte aligned and ld_src a multiple of 4; data 4-byte
+ * aligned and ld_data a multiple of 4.  The output is bit-exact with the
+ * definition above.
+ */
+int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
+                    uint8_t* data, int64_t ld_data, uint8_t* scales,
+                    int64_t ld_scales, wq_stream_t stream);
+
+/*
+ * mx_gemm_fp4 — C = A * W^T for MXFP4 operands, FP32 output.
+ *
+ * [MXFP4] §二.1 and §二.2: for every output (m, n) and 32-element K block k,
+ *   dC = 2^(E_A[m,k] + E_W[n,k] - 254) * sum_{i<32} a[m,k,i] * w[n,k,i],
+ * summed over the blocks in FP32 (§三: C = A @ W^T with A [M, K], W [N, K]).
+ *
+ *   M, N, K  problem size; K must be a multiple of 32.
+ *   A, SA    A's data uint8 [M, K/2] (row stride lda bytes) and E8M0 scales
+ *            uint8 [M, K/32] (row stride ldsa bytes), as mx_quantize_fp4
+ *            writes them.
+ *   W, SW    the same for W [N, K] (row strides ldw, ldsw).
+ *   C        fp32 [M, N] output, row stride ldc (elements).
+ *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_MX_GEMM, M, N, K).
+ * Alignment: A, W 16-byte aligned with lda, ldw multiples of 16; C 16-byte
+ * aligned with ldc a multiple of 4.
+ */
+int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
+                const uint8_t* SA, int64_t ldsa, const uint8_t* W,
+                int64_t ldw, const uint8_t* SW, int64_t ldsw, float* C,
+                int64_t ldc, void* workspace, size_t ws_bytes,
+                wq_stream_t stream);
+
+/*
+ * fp8_gemm — C = bf16((A * B) * scale_a * scale_b) for e4m3 operands.
+ *
+ * [FP8] kernel listing and 精度管理 bullet: e4m3fn inputs, FP32 accumulation,
+ * the per-tensor scales applied once to the accumulator, BF16 output
+ * (round to nearest even).
+ *
+ *   M, N, K  problem size; K must be a multiple of 16.
+ *   A        e4m3fn bytes [M, K], row stride lda (bytes).
+ *   B        e4m3fn bytes [K, N], row stride ldb (bytes).
+ *   scale_a, scale_b  per-tensor FP32 scales, passed by value.
+ *   C        bf16 [M, N] output, row stride ldc (elements).
+ *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K).
+ * Alignment: A, B, C 16-byte aligned; lda, ldb multiples of 16; ldc a
+ * multiple of 8.
+ */
+int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda,
+             const uint8_t* B, int64_t ldb, float scale_a, float scale_b,
+             void* C, int64_t ldc, void* workspace, size_t ws_bytes,
+             wq_stream_t stream);
+
+/* Scratch bytes an operation needs for this shape (0 when none). */
+size_t wq_workspace_size(int op, int M, int N, int K);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* wq_status_string(int status);
+
+/*
+ * Read and clear the device error word that kernels set when a bounded
+ * wait (an mbarrier or cluster handshake) gives up instead of hanging.
+ * Synchronizes `stream`.  Returns WQ_OK when no kernel gave up, otherwise
+ * WQ_ERR_DEVICE and stores the recorded site code in *site (if non-NULL).
+ */
+int wq_get_device_error(wq_stream_t stream, int* site);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int wq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

@@ -1,0 +1,93 @@
+"""The C ABI library builds, loads, exports every function include/wq.h
+declares, and rejects bad arguments on the host before any launch.  Nothing
+here touches a GPU: the validation paths return before the first CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def wq():
+    from bit_quantized_gemm_dequant_gb300 import build
+
+    build.build()
+    import bit_quantized_gemm_dequant_gb300 as mod
+
+    return mod
+
+
+def test_header_declares_the_five_entry_points(wq):
+    names = wq.header_functions()
+    for n in ("wq_gemm_w4a16", "wq_gemm_w8a16", "mx_quantize_fp4", "mx_gemm_fp4", "fp8_gemm",
+              "wq_workspace_size", "wq_status_string", "wq_get_device_error", "wq_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(wq):
+    out = subprocess.run(["nm", "-D", "--defined-only", wq.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in wq.header_functions():
+        assert name in exported, name
+        assert getattr(wq.lib, name) is not None
+
+
+def test_status_strings(wq):
+    for code in range(7):
+        assert wq.wq_status_string(code).startswith("WQ_")
+    assert wq.wq_status_string(99) == "WQ_ERR_UNKNOWN"
+    assert wq.wq_version() >= 100
+
+
+FAKE = 0x10000  # never dereferenced: validation returns first
+
+
+def _w4(wq, M=4, N=64, K=64, X=FAKE, ldx=64, W=FAKE, ldw=64, S=FAKE, Y=FAKE, ldy=64):
+    return wq.lib.wq_gemm_w4a16(M, N, K, X, ldx, W, ldw, S, Y, ldy, None, 0, None)
+
+
+def test_weight_only_validation(wq):
+    assert _w4(wq, M=-1) == wq.WQ_ERR_INVALID_ARG
+    assert _w4(wq, K=63) == wq.WQ_ERR_INVALID_ARG          # INT4 packs two codes per byte
+    assert _w4(wq, X=0) == wq.WQ_ERR_INVALID_ARG
+    assert _w4(wq, ldx=32) == wq.WQ_ERR_INVALID_ARG        # ldx < K
+    assert _w4(wq, ldy=32) == wq.WQ_ERR_INVALID_ARG
+    assert _w4(wq, ldw=32) == wq.WQ_ERR_INVALID_ARG        # ldw < N
+    assert _w4(wq, X=FAKE + 2) == wq.WQ_ERR_MISALIGNED
+    assert _w4(wq, ldw=72) == wq.WQ_ERR_MISALIGNED
+    assert _w4(wq, ldx=68) == wq.WQ_ERR_MISALIGNED
+    assert _w4(wq, M=0) == wq.WQ_OK and _w4(wq, N=0) == wq.WQ_OK   # empty: no launch
+    assert wq.lib.wq_gemm_w8a16(4, 64, 63, FAKE, 64, FAKE, 64, FAKE, FAKE, 64, None, 0, None) == wq.WQ_ERR_UNSUPPORTED
+
+
+def test_mx_and_fp8_validation(wq):
+    L = wq.lib
+    assert L.mx_quantize_fp4(4, 48, FAKE, 48, FAKE, 24, FAKE, 2, None) == wq.WQ_ERR_INVALID_ARG  # cols % 32
+    assert L.mx_quantize_fp4(4, 64, FAKE + 4, 64, FAKE, 32, FAKE, 2, None) == wq.WQ_ERR_MISALIGNED
+    assert L.mx_quantize_fp4(0, 64, 0, 64, 0, 32, 0, 2, None) == wq.WQ_OK
+    assert L.mx_gemm_fp4(8, 8, 48, FAKE, 32, FAKE, 2, FAKE, 32, FAKE, 2, FAKE, 8, None, 0, None) == wq.WQ_ERR_INVALID_ARG
+    assert L.mx_gemm_fp4(8, 8, 64, FAKE, 40, FAKE, 2, FAKE, 32, FAKE, 2, FAKE, 8, None, 0, None) == wq.WQ_ERR_MISALIGNED
+    assert L.fp8_gemm(8, 8, 32, 0, 32, FAKE, 16, ctypes.c_float(1), ctypes.c_float(1), FAKE, 8, None, 0, None) \
+        == wq.WQ_ERR_INVALID_ARG
+    assert L.fp8_gemm(8, 8, 32, FAKE, 40, FAKE, 16, ctypes.c_float(1), ctypes.c_float(1), FAKE, 8, None, 0, None) \
+        == wq.WQ_ERR_MISALIGNED
+    assert L.fp8_gemm(0, 8, 32, 0, 32, 0, 16, ctypes.c_float(1), ctypes.c_float(1), 0, 8, None, 0, None) == wq.WQ_OK
+
+
+def test_workspace_query(wq):
+    for op in range(5):
+        assert wq.wq_workspace_size(op, 16, 4096, 4096) >= 0
+
+
+def test_product_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "bit_quantized_gemm_dequant_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh")):
+                with open(os.path.join(dirpath, f)) as fh:
+                    text = fh.read()
+                assert not re.search(r"(^|\s)(import|from)\s+oracle", text), f

@@ -1,0 +1,119 @@
+"""GPU parity of wq_gemm_w4a16 / wq_gemm_w8a16 against the CPU oracle.
+
+Tolerance: |y - y_ref| <= 5e-3 * max|y_ref| + 1 fp16 ulp at y_ref, per element.
+Small cases span several 128-column tiles, ragged N/K/M tails and padded leading
+dimensions; the decode workloads run at full size with every output checked;
+large M is checked on sampled rows."""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import wq_oracle as O
+from tests.gpu_util import assert_gemm_close, dev_empty, dev_matrix
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def wq():
+    import bit_quantized_gemm_dequant_gb300 as mod
+
+    return mod
+
+
+def _run(wq, bits, case, ldx=None, ldw=None, ldy=None):
+    M, K = case.x.shape
+    N = case.w.shape[1]
+    x = dev_matrix(torch, case.x, ldx)
+    w = dev_matrix(torch, case.w, ldw)
+    s = torch.from_numpy(case.scales).cuda()
+    y = dev_empty(torch, M, N, torch.float16, ldy, fill=float("nan"))
+    fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+    fn(x, w, s, y=y)
+    torch.cuda.synchronize()
+    return y
+
+
+def _ref(bits, case, rows=None):
+    x = case.x if rows is None else case.x[rows]
+    return O.gemm_w4a16(x, case.w, case.scales) if bits == 4 else O.gemm_w8a16(x, case.w, case.scales)
+
+
+def _case(bits, M, K, N, seed):
+    return workloads.w4a16_case(M, K, N, seed) if bits == 4 else workloads.w8a16_case(M, K, N, seed)
+
+
+SMALL = [  # (M, K, N, ldx, ldw, ldy)
+    (16, 512, 512, None, None, None),     # the tiny W4A16 workload
+    (1, 64, 128, None, None, None),
+    (3, 96, 257, None, 272, 264),         # ragged N inside the last 16-column vector
+    (8, 50, 384, 56, 400, 392),           # K not a multiple of 16, padded strides
+    (9, 1024, 200, None, 208, 200),       # second MMA column block, ragged N
+    (16, 2048, 1000, 2056, 1008, 1000),
+    (5, 4096, 4096, None, None, None),
+    (12, 11008, 640, None, None, None),   # down-projection K
+]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N,ldx,ldw,ldy", SMALL)
+def test_small_cases(wq, bits, M, K, N, ldx, ldw, ldy):
+    case = _case(bits, M, K, N, seed=M + K + N)
+    y = _run(wq, bits, case, ldx, ldw, ldy)
+    assert_gemm_close(y, _ref(bits, case), "fp16")
+
+
+@pytest.mark.parametrize("M,K,N", workloads.WORKLOADS["w8a16_decode"]["shapes"])
+def test_w8a16_decode_full_size(wq, M, K, N):
+    case = workloads.w8a16_case(M, K, N, seed=0)
+    assert_gemm_close(_run(wq, 8, case), _ref(8, case), "fp16")
+
+
+@pytest.mark.parametrize("M,K,N", [s for s in workloads.WORKLOADS["w4a16_llama7b"]["shapes"]])
+def test_w4a16_llama_shapes(wq, M, K, N):
+    case = workloads.w4a16_case(M, K, N, seed=0)
+    y = _run(wq, 4, case)
+    if M <= 64:
+        assert_gemm_close(y, _ref(4, case), "fp16")
+    else:
+        rows = np.random.default_rng(M).choice(M, 48, replace=False)
+        rows[:2] = [0, M - 1]
+        # the bound's max|y_ref| term is taken over the sampled rows only
+        assert_gemm_close(y[torch.from_numpy(rows).cuda()], _ref(4, case, rows), "fp16")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_k_zero_writes_zeros(wq, bits):
+    x = torch.empty((3, 0), dtype=torch.float16, device="cuda")
+    w = torch.empty((0, 64), dtype=torch.uint8 if bits == 4 else torch.int8, device="cuda")
+    s = torch.ones(64, dtype=torch.float16, device="cuda")
+    y = torch.full((3, 64), float("nan"), dtype=torch.float16, device="cuda")
+    (wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16)(x, w, s, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+
+
+def test_int8_extremes(wq):
+    """-128 and 127 codes, scales near the fp16 subnormal edge and large."""
+    rng = np.random.default_rng(11)
+    K, N = 256, 256
+    w = rng.choice(np.array([-128, 127, -1, 0, 1], np.int8), size=(K, N))
+    x = rng.standard_normal((7, K)).astype(np.float16)
+    s = np.concatenate([np.full(128, 6.1e-5, np.float16), np.full(128, 3.0, np.float16)])
+    case = workloads.WeightOnlyCase(x, w, s, 8)
+    assert_gemm_close(_run(wq, 8, case), _ref(8, case), "fp16")
+
+
+def test_out_of_tile_columns_untouched(wq):
+    """Padding columns of Y beyond N keep their contents (the kernel writes only [M, N])."""
+    case = workloads.w4a16_case(4, 128, 100, seed=3)
+    x = dev_matrix(torch, case.x)
+    w = dev_matrix(torch, case.w, 112)
+    s = torch.from_numpy(case.scales).cuda()
+    buf = torch.full((4, 128), 7.0, dtype=torch.float16, device="cuda")
+    wq.wq_gemm_w4a16(x, w, s, y=buf[:, :100])
+    torch.cuda.synchronize()
+    assert torch.all(buf[:, 100:] == 7.0)
+    assert_gemm_close(buf[:, :100], _ref(4, case), "fp16")
