@@ -115,30 +115,42 @@ class WeightOnly:
 def _sample_clocks():
     """Start nvidia-smi sampling clocks and throttle reasons every 200 ms."""
     try:
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        q = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         return subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "200"],
-                                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
     except (OSError, ValueError):
         return None
 
 
-def _finish_clocks(proc, gpu_index):
+def _pci_bus_id(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+def _finish_clocks(proc, pci):
     if proc is None:
         return None
     proc.terminate()
     try:
-        out, _ = proc.communicate(timeout=5)
+        out, err = proc.communicate(timeout=5)
     except subprocess.TimeoutExpired:
         proc.kill()
-        out, _ = proc.communicate()
+        out, err = proc.communicate()
+    rows = [[x.strip() for x in line.split(",")] for line in out.splitlines()]
+    rows = [r for r in rows if len(r) >= 9]
+    ids = {r[0] for r in rows}
+    if pci is not None and any(i.upper().endswith(pci[-12:].upper()) for i in ids):
+        rows = [r for r in rows if r[0].upper().endswith(pci[-12:].upper())]
+    elif len(ids) > 1:
+        return {"error": f"could not match the GPU among {sorted(ids)}"}
     sm, mx, reasons = [], None, set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-    for line in out.splitlines():
-        f = [x.strip() for x in line.split(",")]
-        if len(f) < 9 or f[0] != str(gpu_index):
-            continue
+    for f in rows:
         try:
             sm.append(float(f[1]))
             mx = float(f[2])
@@ -148,7 +160,7 @@ def _finish_clocks(proc, gpu_index):
             if v.lower() == "active":
                 reasons.add(n)
     if not sm:
-        return None
+        return {"error": (err or "no samples").strip()[:200]}
     return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -169,13 +181,22 @@ def _barrier_max(torch, value, ws):
     return float(t.item())
 
 
+def _hold_stream(torch, seconds):
+    """Keep the stream busy for about `seconds` (a device-side spin) so that the
+    host can enqueue the whole timed region before the GPU reaches it: the
+    events then measure device time only, not Python / launch latency."""
+    torch.cuda._sleep(int(seconds * 2.2e9))  # cycles at or above the maximum SM clock
+
+
 def time_workload(torch, wl, steps, warmup, replicas, ws):
     """Time `steps` passes over wl.calls; per-launch CUDA events on the launching stream."""
     stream = torch.cuda.current_stream()
     n_calls = len(wl.calls)
+    t_host = time.perf_counter()
     for s in range(warmup):
         for (_, i, _, _) in wl.calls:
             wl.run(s % replicas, i)
+    host_per_step = (time.perf_counter() - t_host) / max(1, warmup)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -183,6 +204,7 @@ def time_workload(torch, wl, steps, warmup, replicas, ws):
           for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    _hold_stream(torch, 2.0 * host_per_step * steps + 2e-3)
     t0.record(stream)
     for s in range(steps):
         for j, (_, i, _, _) in enumerate(wl.calls):
@@ -234,7 +256,7 @@ def run_ours(args):
 
     clock_proc = _sample_clocks() if rank == 0 else None
     total_ms, per_call = time_workload(torch, wl, args.steps, args.warmup, replicas, ws)
-    clocks = _finish_clocks(clock_proc, local) if rank == 0 else None
+    clocks = _finish_clocks(clock_proc, _pci_bus_id(torch, local)) if rank == 0 else None
 
     value = ws * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
     dominant = max(per_call, key=lambda c: c["ms"])
@@ -293,18 +315,86 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def time_calls(torch, calls, steps, warmup, flush_bytes=2 * L2_BYTES):
+    """Per-call CUDA-event times (ms) on the launching stream.  Before every
+    call an L2-sized buffer is overwritten (outside the events), so no call
+    starts with its operands in L2."""
+    stream = torch.cuda.current_stream()
+    scratch = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        for c in calls:
+            c["run"]()
+    torch.cuda.synchronize()
+    ev = {c["call"]: [] for c in calls}
+    _hold_stream(torch, 60e-6 * steps * len(calls) + 2e-3)
+    for _ in range(steps):
+        for c in calls:
+            scratch.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            c["run"]()
+            e1.record(stream)
+            ev[c["call"]].append((e0, e1))
+    torch.cuda.synchronize()
+    out = []
+    for c in calls:
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev[c["call"]])
+        out.append({"call": c["call"], "ms": ms, "bytes": c["bytes"], "flops": c["flops"]})
+    del scratch
+    return out
+
+
 def run_breakdown(torch, wq, peaks, args):
     """Other workloads, each timed over a few steps with its own roofline."""
     out = []
     steps, warm = 5, 3
+
     spec = workloads.WORKLOADS["w4a16_llama7b"]
-    wl = WeightOnly(wq, torch, 4, spec["shapes"], 2)
-    _, per_call = time_workload(torch, wl, steps, warm, 2, 1)
-    for c in per_call:
+    wl = WeightOnly(wq, torch, 4, spec["shapes"], 1)
+    calls = [{"call": name, "run": (lambda i=i: wl.run(0, i)), "bytes": nb, "flops": fl}
+             for (name, i, nb, fl) in wl.calls]
+    for c in time_calls(torch, calls, steps, warm):
         M = int(c["call"].split("_")[1].split("x")[0])
         bound = "hbm" if M <= 64 else "tensor"
         out.append({"workload": "w4a16_llama7b", **c, "roofline": roofline_for(c, peaks, bound, "fp16")})
-    del wl
+    del wl, calls
+    torch.cuda.empty_cache()
+
+    # MXFP4: quantize both fp32 operands on the device, then the GEMM.
+    K = N = 8192
+    w_src = torch.from_numpy(workloads.mx_source(N, K, seed=0, stream=1)).cuda()
+    wd, ws = wq.mx_quantize_fp4(w_src)
+    calls = [{"call": f"mx_quantize_{N}x{K}", "run": (lambda: wq.mx_quantize_fp4(w_src, wd, ws)),
+              "bytes": N * K * 4 + N * K // 2 + N * K // 32, "flops": 0, "bound": "hbm"}]
+    keep = []
+    for M in (128, 2048, 8192):
+        a_src = torch.from_numpy(workloads.mx_source(M, K, seed=0, stream=0)).cuda()
+        ad, asc = wq.mx_quantize_fp4(a_src)
+        c_out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        keep.append((a_src, ad, asc, c_out))
+        calls.append({"call": f"mx_gemm_{M}x{K}x{N}",
+                      "run": (lambda ad=ad, asc=asc, c_out=c_out: wq.mx_gemm_fp4(ad, asc, wd, ws, c=c_out)),
+                      "bytes": (M + N) * (K // 2 + K // 32) + 4 * M * N, "flops": 2 * M * N * K,
+                      "bound": "hbm" if M <= 128 else "tensor"})
+    for c, spec_c in zip(time_calls(torch, calls, steps, warm), calls):
+        out.append({"workload": "mxfp4", **c, "roofline": roofline_for(c, peaks, spec_c["bound"], "fp4")})
+    del keep, calls, w_src, wd, ws
+    torch.cuda.empty_cache()
+
+    calls, keep = [], []
+    for (M, K, N) in workloads.WORKLOADS["fp8"]["shapes"]:
+        case = workloads.fp8_case(M, K, N, seed=0)
+        a = torch.from_numpy(case.a8).cuda()
+        b = torch.from_numpy(case.b8).cuda()
+        cc = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        keep.append((a, b, cc))
+        calls.append({"call": f"fp8_{M}x{K}x{N}",
+                      "run": (lambda a=a, b=b, cc=cc, sa=case.scale_a, sb=case.scale_b: wq.fp8_gemm(a, b, sa, sb, c=cc)),
+                      "bytes": M * K + K * N + 2 * M * N, "flops": 2 * M * N * K,
+                      "bound": "hbm" if M <= 16 else "tensor"})
+    for c, spec_c in zip(time_calls(torch, calls, steps, warm), calls):
+        out.append({"workload": "fp8", **c, "roofline": roofline_for(c, peaks, spec_c["bound"], "fp8")})
+    del keep, calls
     torch.cuda.empty_cache()
     return out
 

@@ -1,0 +1,226 @@
+// MXFP4 GEMM C = A * W^T on the block-scaled 5th-generation tensor cores.
+//
+// Defined by "量化推理引擎中的微缩放格式前瞻：MXFP4 矩阵乘法 Kernel 原理": §二.1
+// (block dot product dC = S_A S_W sum_{i<32} a w over each 32-element K block)
+// and §二.2 (S_A S_W = 2^(E_A + E_W - 254)); §三: C = A @ W^T, A [M, K],
+// W [N, K], both split along K into 32-element E2M1 blocks with one E8M0
+// exponent each.
+//
+// The page's CPU simulator adds exponents and shifts in software; here the
+// exponent addition happens inside tcgen05.mma.kind::mxf4.block_scale: the
+// E2M1 operands stay packed (two per byte) from HBM to the tensor core, and
+// the UE8M0 block scales ride along in tensor memory.
+//
+// Design: one 128 x 128 output tile per CTA, K in 256-element (128-byte)
+// steps through a 6-stage ring.
+//   warp 0      producer.  Lane 0 issues the TMA loads of the A and W data
+//               tiles (128 rows x 128 bytes, 128-byte swizzle).  All lanes
+//               gather the stage's 8 E8M0 bytes of each of the 256 rows and
+//               write them in the 128-row x 4-block chunk layout the scale
+//               copy expects (byte 16*(r%32) + 4*(r/32) + kb of a 512-byte
+//               chunk), then arrive on the stage's barrier.
+//   warp 1      TMEM allocator and MMA issuer: per stage, four tcgen05.cp
+//               32x128b.warpx4 (scale chunks -> TMEM) and four
+//               tcgen05.mma 128 x 128 x 64 with scale_vec::2X, the scale
+//               byte pair chosen by the descriptor's scale-factor ids.
+//   warps 2-5   epilogue: tcgen05.ld and FP32 stores.
+#include "tc_common.cuh"
+#include "tma_host.h"
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int BKB = 128;                    // K bytes per stage (256 E2M1 elements)
+constexpr int kBlocksPerStage = BKB * 2 / 32;  // 8 scale blocks
+constexpr int kStages = 6;
+constexpr int kABytes = BM * BKB;           // 16 KB
+constexpr int kBBytes = BN * BKB;           // 16 KB
+constexpr int kSfChunk = 512;               // 128 rows x 4 blocks
+constexpr int kSfBytes = 4 * kSfChunk;      // A: 2 chunks, W: 2 chunks
+constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // 34 KB (multiple of 1024)
+constexpr int kAccCols = BN;                // FP32 accumulator columns
+constexpr int kSfColsPerStage = 16;         // 4 chunks x 4 columns
+constexpr int kTmemCols = 256;              // accumulator + 6 x 16 scale columns, rounded up
+constexpr int kThreads = 192;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+
+static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+static_assert(kStageBytes % 1024 == 0, "stage alignment");
+
+// Gather 8 scale bytes (blocks kb0 .. kb0+7) of one row; rows or blocks
+// outside the matrix read as 127 (2^0) so that zero-filled data stays zero.
+__device__ __forceinline__ void load_sf8(const uint8_t* S, int64_t ld, int row, int rows, int kb0, int nkb,
+                                         bool aligned4, uint32_t& lo, uint32_t& hi) {
+  if (row < rows && kb0 + 8 <= nkb && aligned4) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(S + static_cast<int64_t>(row) * ld + kb0);
+    lo = __ldg(p);
+    hi = __ldg(p + 1);
+    return;
+  }
+  uint32_t w[2] = {0x7F7F7F7Fu, 0x7F7F7F7Fu};
+  if (row < rows) {
+    const uint8_t* p = S + static_cast<int64_t>(row) * ld;
+    for (int i = 0; i < 8; ++i)
+      if (kb0 + i < nkb) {
+        w[i >> 2] &= ~(0xFFu << (8 * (i & 3)));
+        w[i >> 2] |= static_cast<uint32_t>(__ldg(p + kb0 + i)) << (8 * (i & 3));
+      }
+  }
+  lo = w[0];
+  hi = w[1];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
+               int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* accum = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nkb = p.K / 32;
+  const int KT = (p.K / 2 + BKB - 1) / BKB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 2);  // TMA transaction arrival + scale gather arrival
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(accum, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tmA);
+      tc::tma_prefetch_desc(&tmW);
+    }
+    const bool a4 = ((reinterpret_cast<uintptr_t>(p.SA) | static_cast<uintptr_t>(p.ldsa)) & 3) == 0;
+    const bool w4 = ((reinterpret_cast<uintptr_t>(p.SW) | static_cast<uintptr_t>(p.ldsw)) & 3) == 0;
+    int issued = 0;
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % kStages;
+      const bool free_slot = tc::mbar_wait(&empty[s], ((kt / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
+      if (!__all_sync(0xffffffffu, free_slot)) break;  // warp-uniform exit
+      uint8_t* st = smem + s * kStageBytes;
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+        tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
+        tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
+      }
+      // Scale chunks: [A blocks 0-3][A blocks 4-7][W blocks 0-3][W blocks 4-7].
+      uint8_t* sf = st + kABytes + kBBytes;
+      const int kb0 = kt * kBlocksPerStage;
+#pragma unroll
+      for (int side = 0; side < 2; ++side) {
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane + 32 * i;
+          if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0, nkb, a4, lo[i], hi[i]);
+          else load_sf8(p.SW, p.ldsw, n0 + r, p.N, kb0, nkb, w4, lo[i], hi[i]);
+        }
+        uint8_t* c0 = sf + side * 2 * kSfChunk;
+        *reinterpret_cast<uint4*>(c0 + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(c0 + kSfChunk + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+      tc::fence_proxy_async_smem();  // scale bytes -> visible to tcgen05.cp
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&full[s]);
+      issued = kt + 1;
+    }
+    if (*abort && lane == 0) {
+      for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
+        tc::mbar_wait_drain(&full[kt % kStages], (kt / kStages) & 1);
+    }
+  } else if (warp == 1 && lane == 0) {
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % kStages;
+      if (!tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmMma)) break;
+      tc::tc_fence_after();
+      const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
+      const uint32_t b = a + kABytes;
+      const uint32_t sf = b + kBBytes;
+      const uint32_t sf_col = tmem + kAccCols + s * kSfColsPerStage;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)  // A chunk 0, A chunk 1, W chunk 0, W chunk 1
+        tc::tmem_cp_32x128b_warpx4(sf_col + 4 * c, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // 64 elements = 32 bytes per MMA
+        const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
+        const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
+        const uint32_t id = 2 * (j & 1);
+        const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
+        tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 4 * (j >> 1), (kt | j) != 0);
+      }
+      tc::tc_commit(&empty[s]);
+    }
+    tc::tc_commit(accum);
+  } else if (warp >= 2) {
+    const bool ok = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
+    tc::tc_fence_after();
+    const int q = warp & 3;
+    const int row = m0 + 32 * q + lane;
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
+      tc::tmem_ld_wait();
+      if (!ok || row >= p.M) continue;
+      const int col0 = n0 + 32 * c;
+      float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+      if (col0 + 32 <= p.N) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          *reinterpret_cast<uint4*>(dst + 4 * v) = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+      } else {
+        for (int t = 0; t < 32 && col0 + t < p.N; ++t) dst[t] = __uint_as_float(r[t]);
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
+  if (a.K == 0)
+    return cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
+  CUtensorMap tA, tW;
+  cudaError_t e = make_tmap_2d(&tA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.lda, BKB, BM,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.N, a.ldw, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  static bool configured = false;
+  if (!configured) {
+    e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
+  mx_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tA, tW, a, device_error_word());
+  return cudaGetLastError();
+}
+
+}  // namespace wq

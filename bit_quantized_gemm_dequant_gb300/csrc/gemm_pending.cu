@@ -3,7 +3,5 @@
 #include "wq_internal.h"
 
 namespace wq {
-cudaError_t launch_mx_gemm(const MxGemmArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_fp8_gemm(const Fp8GemmArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s) { return launch_wo_skinny(a, bits, s); }
 }  // namespace wq

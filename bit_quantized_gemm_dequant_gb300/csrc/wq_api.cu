@@ -119,8 +119,8 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_
   if (M == 0 || N == 0) return WQ_OK;
   if (!C || (K > 0 && (!A || !SA || !W || !SW))) return WQ_ERR_INVALID_ARG;
   if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2 || ldsa < K / 32 || ldsw < K / 32))) return WQ_ERR_INVALID_ARG;
-  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || lda % 16 || ldw % 16 || ldc % 4)
-    return WQ_ERR_MISALIGNED;
+  if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(A, 16) || !aligned(W, 16) || lda % 16 || ldw % 16)) return WQ_ERR_MISALIGNED;
   if (ws_bytes < wq_workspace_size(WQ_OP_MX_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
   MxGemmArgs a{M, N, K, A, lda, SA, ldsa, W, ldw, SW, ldsw, C, ldc};
   return launch_status(launch_mx_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -133,8 +133,8 @@ int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* 
   if (M == 0 || N == 0) return WQ_OK;
   if (!C || (K > 0 && (!A || !B))) return WQ_ERR_INVALID_ARG;
   if (ldc < N || (K > 0 && (lda < K || ldb < N))) return WQ_ERR_INVALID_ARG;
-  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || lda % 16 || ldb % 16 || ldc % 8)
-    return WQ_ERR_MISALIGNED;
+  if (!aligned(C, 16) || ldc % 8) return WQ_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(A, 16) || !aligned(B, 16) || lda % 16 || ldb % 16)) return WQ_ERR_MISALIGNED;
   if (ws_bytes < wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
   Fp8GemmArgs a{M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc};
   return launch_status(launch_fp8_gemm(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -1,0 +1,107 @@
+"""GPU mx_gemm_fp4 against the CPU oracle.
+
+Tolerance: |c - c_ref| <= 5e-3 * max|c_ref| + 1 fp32 ulp at c_ref, per element.
+Structured cases (one non-trivial scale per row / per block) come first: a
+wrong scale-factor placement shows up there as a clean pattern."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import wq_oracle as O
+from tests.gpu_util import assert_gemm_close, dev_empty, dev_matrix
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def wq():
+    import bit_quantized_gemm_dequant_gb300 as mod
+
+    return mod
+
+
+def _gemm(wq, ad, asc, wd, wsc, lda=None, ldsa=None, ldw=None, ldsw=None, ldc=None):
+    M, N = ad.shape[0], wd.shape[0]
+    c = dev_empty(torch, M, N, torch.float32, ldc, fill=float("nan"))
+    wq.mx_gemm_fp4(dev_matrix(torch, ad, lda), dev_matrix(torch, asc, ldsa), dev_matrix(torch, wd, ldw),
+                   dev_matrix(torch, wsc, ldsw), c=c)
+    torch.cuda.synchronize()
+    return c
+
+
+def test_worked_example(wq):
+    with open(os.path.join(os.path.dirname(__file__), "golden", "mx_gemm_worked.json")) as f:
+        g = json.load(f)
+    ad, asc = np.array(g["a_data"], np.uint8), np.array(g["a_scales"], np.uint8)
+    wd, wsc = np.array(g["w_data"], np.uint8), np.array(g["w_scales"], np.uint8)
+    c = _gemm(wq, ad, asc, wd, wsc, lda=32, ldw=32, ldc=4)
+    np.testing.assert_array_equal(c.cpu().numpy().astype(np.float64), np.array(g["c"]))
+
+
+def test_per_row_and_per_block_scales(wq):
+    """All data +1.0 (code 2); A row m gets exponent 127 + (m % 7) - 3 in block
+    kb % 3 == 0 and 127 elsewhere, W row n gets 127 + (n % 5) - 2 in blocks
+    kb % 4 == 1: every scale position is distinguishable in the result."""
+    M, N, K = 256, 256, 1024
+    nkb = K // 32
+    ad = np.full((M, K // 2), 0x22, np.uint8)
+    wd = np.full((N, K // 2), 0x22, np.uint8)
+    asc = np.full((M, nkb), 127, np.uint8)
+    wsc = np.full((N, nkb), 127, np.uint8)
+    for kb in range(nkb):
+        if kb % 3 == 0:
+            asc[:, kb] = 127 + (np.arange(M) % 7) - 3
+        if kb % 4 == 1:
+            wsc[:, kb] = 127 + (np.arange(N) % 5) - 2
+    c = _gemm(wq, ad, asc, wd, wsc)
+    assert_gemm_close(c, O.mx_gemm_fp4(ad, asc, wd, wsc), "fp32", rel=1e-6)
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldsa,ldw,ldsw,ldc", [
+    (128, 128, 256, None, None, None, None, None),
+    (1, 16, 32, 16, None, 16, None, None),          # a single scale block
+    (200, 300, 800, 400, 25, 400, 27, 304),         # ragged M/N/K, odd scale strides
+    (130, 256, 8192, None, None, None, None, None),
+    (384, 128, 4096, 2064, 130, 2048, 128, 132),
+])
+def test_random_quantized(wq, M, N, K, lda, ldsa, ldw, ldsw, ldc):
+    a = workloads.mx_source(M, K, seed=M + K, stream=0)
+    w = workloads.mx_source(N, K, seed=N + K, stream=1)
+    ad, asc = O.mx_quantize_fp4(a)
+    wd, wsc = O.mx_quantize_fp4(w)
+    c = _gemm(wq, ad, asc, wd, wsc, lda, ldsa, ldw, ldsw, ldc)
+    assert_gemm_close(c, O.mx_gemm_fp4(ad, asc, wd, wsc), "fp32")
+
+
+@pytest.mark.parametrize("M", [128, 2048, 8192])
+def test_mxfp4_workload_quantize_then_gemm(wq, M):
+    """The MXFP4 workload end to end on the device: both fp32 operands quantized
+    by mx_quantize_fp4, then mx_gemm_fp4; checked on sampled rows."""
+    K = N = 8192
+    a = workloads.mx_source(M, K, seed=0, stream=0)
+    w = workloads.mx_source(N, K, seed=0, stream=1)
+    ad, asc = wq.mx_quantize_fp4(torch.from_numpy(a).cuda())
+    wd, wsc = wq.mx_quantize_fp4(torch.from_numpy(w).cuda())
+    c = wq.mx_gemm_fp4(ad, asc, wd, wsc)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(M).choice(M, 24, replace=False)
+    rows[:2] = [0, M - 1]
+    rad, ras = O.mx_quantize_fp4(a[rows])
+    rwd, rws = O.mx_quantize_fp4(w)
+    assert np.array_equal(ad.cpu().numpy()[rows], rad) and np.array_equal(asc.cpu().numpy()[rows], ras)
+    ref = O.mx_gemm_fp4(rad, ras, rwd, rws)
+    assert_gemm_close(c[torch.from_numpy(rows).cuda()], ref, "fp32")
+
+
+def test_k_zero(wq):
+    c = dev_empty(torch, 3, 20, torch.float32, 20, fill=float("nan"))
+    e = torch.empty((3, 0), dtype=torch.uint8, device="cuda")
+    f = torch.empty((20, 0), dtype=torch.uint8, device="cuda")
+    wq.mx_gemm_fp4(e, e, f, f, c=c)
+    torch.cuda.synchronize()
+    assert torch.all(c == 0)

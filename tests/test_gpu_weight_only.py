@@ -117,3 +117,29 @@ def test_out_of_tile_columns_untouched(wq):
     torch.cuda.synchronize()
     assert torch.all(buf[:, 100:] == 7.0)
     assert_gemm_close(buf[:, :100], _ref(4, case), "fp16")
+
+
+LARGE_M = [  # (M, K, N, ldx, ldw, ldy): the tensor-memory path (M > 64)
+    (65, 64, 128, None, None, None),
+    (100, 256, 384, None, None, None),
+    (257, 1000, 200, 1008, 208, 200),   # ragged M, N, K (K not a multiple of 64)
+    (300, 4096, 640, None, None, None),
+    (512, 2048, 1024, None, None, None),
+]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N,ldx,ldw,ldy", LARGE_M)
+def test_large_m_cases(wq, bits, M, K, N, ldx, ldw, ldy):
+    case = _case(bits, M, K, N, seed=M * 7 + K + N)
+    y = _run(wq, bits, case, ldx, ldw, ldy)
+    assert_gemm_close(y, _ref(bits, case), "fp16")
+
+
+@pytest.mark.parametrize("M,K,N", [(4096, 4096, 4096), (4096, 4096, 14336)])
+def test_w8a16_large_m_sampled(wq, M, K, N):
+    case = workloads.w8a16_case(M, K, N, seed=1)
+    y = _run(wq, 8, case)
+    rows = np.random.default_rng(N).choice(M, 32, replace=False)
+    rows[:2] = [0, M - 1]
+    assert_gemm_close(y[torch.from_numpy(rows).cuda()], _ref(8, case, rows), "fp16")
