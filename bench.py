@@ -1,21 +1,23 @@
 """Benchmark of the fused dequantization GEMM library on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-breakdown]
+                    [--workload NAME] [--only SUBSTRING] [--no-breakdown] [--no-e2e]
 
 A step is one pass over the workload's calls with inputs resident in HBM.
 The default workload is the INT8 weight-only decode sweep
 (M in {1, 4, 16} x K = 4096 x N in {4096, 14336}); its value is the whole-job
 HBM throughput on algorithmic bytes (packed weights + scales + activations +
-outputs) in GB/s.  Every step reads a different replica of all inputs, and one
-step's inputs are larger than the 129 MB L2, so no step starts with its
-weights in L2.  Rank 0 prints one JSON line.
+outputs) in GB/s.  Steps rotate over replicas of all inputs and one step reads
+more than the 129 MB L2, so no call starts with its weights in L2.
 
-The `breakdown` key carries the other workloads (INT4 Llama-7B linears, the
-MXFP4 quantize + GEMM and the FP8 GEMM) measured in the same run, each with
-its own roofline.  `--impl reference` times the CPU oracle on a bounded
-sample of the same workload instead (the oracle is the only place this
-script runs oracle code besides the cpu_baseline leg).
+Before the timed region the stream is held by a device-side spin long enough
+for the host to enqueue every timed launch, so CUDA events measure device time
+and not Python / launch latency.  Rank 0 prints one JSON line.
+
+`breakdown` carries the other workloads (INT4 Llama-7B linears, MXFP4 quantize
++ GEMM, FP8 GEMM), each call timed after an L2 flush, with its own roofline.
+`--impl reference` times the CPU oracle on a bounded sample of the workload;
+the oracle runs nowhere else in this script except the cpu_baseline leg.
 """
 from __future__ import annotations
 
@@ -35,6 +37,9 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+METRIC = "W4A16/W8A16 GEMV HBM GB/s (% peak); MXFP4/FP8 GEMM TFLOPS (% peak)"
+# Nominal dense tensor rates relative to bf16 (2.25 PF): fp8 4.5 PF, fp4 13.5 PF.
+NOMINAL_RATIO = {"bf16": 1.0, "fp16": 1.0, "fp8": 2.0, "fp4": 6.0}
 
 
 def load_peaks():
@@ -47,69 +52,243 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-# Nominal dense tensor rates relative to bf16 (2.25 PF): fp8 4.5 PF, fp4 13.5 PF.
-NOMINAL_RATIO = {"bf16": 1.0, "fp16": 1.0, "fp8": 2.0, "fp4": 6.0}
-
-
 # ----------------------------------------------------------------- workloads
-# Each workload builds its inputs on the device (R replicas) and returns a
-# list of calls; a call is (name, fn(replica), alg_bytes, flops, dtype_for_peak).
+# A workload owns device inputs (several replicas) and a list of calls.  Each
+# call is a dict: name, index, bytes, flops, bound ("hbm"/"tensor"), dtype
+# (for the tensor peak).  The main line's unit is GB/s when every call is
+# HBM-bound, TFLOP/s otherwise.
 
 
 def _wo_bytes(bits, M, K, N):
-    wbytes = K * N // 2 if bits == 4 else K * N
-    return wbytes + 2 * N + 2 * M * K + 2 * M * N
+    return (K * N // 2 if bits == 4 else K * N) + 2 * N + 2 * M * K + 2 * M * N
 
 
 class WeightOnly:
-    def __init__(self, wq, torch, bits, shapes, replicas, seed=0):
-        self.wq, self.torch, self.bits, self.shapes = wq, torch, bits, shapes
-        self.cases = []
-        for (M, K, N) in shapes:
-            c = workloads.w4a16_case(M, K, N, seed) if bits == 4 else workloads.w8a16_case(M, K, N, seed)
-            self.cases.append(c)
+    def __init__(self, torch, wq, bits, shapes, replicas, seed=0):
+        self.torch, self.bits = torch, bits
+        self.cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, seed)
+                      for (M, K, N) in shapes]
+        self.fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
         self.dev = []
         for _ in range(replicas):
             reps = []
             for c in self.cases:
-                x = torch.from_numpy(c.x).cuda()
-                w = torch.from_numpy(c.w).cuda()
-                s = torch.from_numpy(c.scales).cuda()
-                y = torch.empty((c.x.shape[0], c.w.shape[1]), dtype=torch.float16, device="cuda")
-                reps.append((x, w, s, y))
+                reps.append((torch.from_numpy(c.x).cuda(), torch.from_numpy(c.w).cuda(),
+                             torch.from_numpy(c.scales).cuda(),
+                             torch.empty((c.x.shape[0], c.w.shape[1]), dtype=torch.float16, device="cuda")))
             self.dev.append(reps)
-        self.fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+        # One zero-filled workspace serves every call: they run one after the
+        # other on one stream and each leaves it zero-filled.
+        op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
+        need = max(wq.wq_workspace_size(op, M, N, K) for (M, K, N) in shapes)
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
         tag = "w4a16" if bits == 4 else "w8a16"
         self.calls = []
         for i, (M, K, N) in enumerate(shapes):
-            self.calls.append((f"{tag}_{M}x{K}x{N}", i, _wo_bytes(bits, M, K, N), 2 * M * N * K))
+            self.calls.append({"call": f"{tag}_{M}x{K}x{N}", "index": i, "bytes": _wo_bytes(bits, M, K, N),
+                               "flops": 2 * M * N * K, "bound": "hbm" if M <= 64 else "tensor", "dtype": "fp16"})
 
     def run(self, r, i):
         x, w, s, y = self.dev[r][i]
-        self.fn(x, w, s, y=y)
+        self.fn(x, w, s, y=y, workspace=self.ws)
 
     def host_inputs(self):
-        t = self.torch
-        out = []
-        for c in self.cases:
-            out.append(tuple(t.from_numpy(a).pin_memory() for a in (c.x, c.w, c.scales)))
-        return out
+        return [tuple(self.torch.from_numpy(a).pin_memory() for a in (c.x, c.w, c.scales)) for c in self.cases]
 
-    def e2e_step(self, host, i, stream):
-        t = self.torch
+    def e2e_call(self, host, i):
         hx, hw, hs = host[i]
-        x = hx.to("cuda", non_blocking=True)
-        w = hw.to("cuda", non_blocking=True)
-        s = hs.to("cuda", non_blocking=True)
-        y = self.fn(x, w, s)
-        return y.to("cpu", non_blocking=True), sum(a.numel() * a.element_size() for a in (hx, hw, hs)), \
-            y.numel() * y.element_size()
+        y = self.fn(hx.to("cuda", non_blocking=True), hw.to("cuda", non_blocking=True),
+                    hs.to("cuda", non_blocking=True))
+        y.to("cpu", non_blocking=True)
+        return sum(a.numel() * a.element_size() for a in (hx, hw, hs)), y.numel() * y.element_size()
 
     def oracle_call(self, i):
         from oracle import wq_oracle as O
 
         c = self.cases[i]
-        return (O.gemm_w4a16 if self.bits == 4 else O.gemm_w8a16)(c.x, c.w, c.scales)
+        (O.gemm_w4a16 if self.bits == 4 else O.gemm_w8a16)(c.x, c.w, c.scales)
+        return self.calls[i]["bytes"], self.calls[i]["flops"]
+
+
+class MxFp4:
+    """Per M: quantize A [M, K] and W [N, K] on the device, then C = A W^T."""
+
+    def __init__(self, torch, wq, shapes, replicas, seed=0):
+        self.torch, self.wq = torch, wq
+        K, N = shapes[0][1], shapes[0][2]
+        self.w_src = workloads.mx_source(N, K, seed=seed, stream=1)
+        self.a_srcs = [workloads.mx_source(M, K, seed=seed, stream=0) for (M, _, _) in shapes]
+        self.dev = []
+        for _ in range(replicas):
+            w = torch.from_numpy(self.w_src).cuda()
+            wd, wsc = wq.mx_quantize_fp4(w)
+            reps = {"w": (w, wd, wsc), "a": []}
+            for a_src in self.a_srcs:
+                a = torch.from_numpy(a_src).cuda()
+                ad, asc = wq.mx_quantize_fp4(a)
+                c = torch.empty((a.shape[0], N), dtype=torch.float32, device="cuda")
+                reps["a"].append((a, ad, asc, c))
+            self.dev.append(reps)
+        self.calls = [{"call": f"mx_quantize_{N}x{K}", "index": ("qw", 0),
+                       "bytes": N * K * 4 + N * K // 2 + N * K // 32, "flops": 0, "bound": "hbm", "dtype": "fp4"}]
+        for i, (M, _, _) in enumerate(shapes):
+            self.calls.append({"call": f"mx_quantize_{M}x{K}", "index": ("qa", i),
+                               "bytes": M * K * 4 + M * K // 2 + M * K // 32, "flops": 0, "bound": "hbm",
+                               "dtype": "fp4"})
+            self.calls.append({"call": f"mx_gemm_{M}x{K}x{N}", "index": ("g", i),
+                               "bytes": (M + N) * (K // 2 + K // 32) + 4 * M * N, "flops": 2 * M * N * K,
+                               "bound": "hbm" if M <= 128 else "tensor", "dtype": "fp4"})
+
+    def run(self, r, idx):
+        kind, i = idx
+        d = self.dev[r]
+        w, wd, wsc = d["w"]
+        if kind == "qw":
+            self.wq.mx_quantize_fp4(w, wd, wsc)
+            return
+        a, ad, asc, c = d["a"][i]
+        if kind == "qa":
+            self.wq.mx_quantize_fp4(a, ad, asc)
+        else:
+            self.wq.mx_gemm_fp4(ad, asc, wd, wsc, c=c)
+
+
+class Fp8:
+    def __init__(self, torch, wq, shapes, replicas, seed=0):
+        self.torch, self.wq = torch, wq
+        self.cases = [workloads.fp8_case(M, K, N, seed) for (M, K, N) in shapes]
+        self.dev = []
+        for _ in range(replicas):
+            self.dev.append([(torch.from_numpy(c.a8).cuda(), torch.from_numpy(c.b8).cuda(),
+                              torch.empty((c.a8.shape[0], c.b8.shape[1]), dtype=torch.bfloat16, device="cuda"))
+                             for c in self.cases])
+        self.calls = [{"call": f"fp8_{M}x{K}x{N}", "index": i, "bytes": M * K + K * N + 2 * M * N,
+                       "flops": 2 * M * N * K, "bound": "hbm" if M <= 16 else "tensor", "dtype": "fp8"}
+                      for i, (M, K, N) in enumerate(shapes)]
+
+    def run(self, r, i):
+        a, b, c = self.dev[r][i]
+        self.wq.fp8_gemm(a, b, self.cases[i].scale_a, self.cases[i].scale_b, c=c)
+
+
+def make_workload(torch, wq, name, replicas, only=None):
+    spec = workloads.WORKLOADS[name]
+    shapes = spec["shapes"]
+    if spec["op"] in ("w4a16", "w8a16"):
+        wl = WeightOnly(torch, wq, 4 if spec["op"] == "w4a16" else 8, shapes, replicas)
+    elif spec["op"] == "mxfp4":
+        wl = MxFp4(torch, wq, shapes, replicas)
+    else:
+        wl = Fp8(torch, wq, shapes, replicas)
+    if only:
+        wl.calls = [c for c in wl.calls if only in c["call"]]
+        if not wl.calls:
+            raise SystemExit(f"--only {only!r} matches no call of {name}")
+    return wl
+
+
+def replicas_for(step_bytes):
+    """Enough replicas that the inputs touched between two uses of one replica exceed 2x L2."""
+    return max(2, min(8, int(np.ceil(2 * L2_BYTES / max(1, step_bytes))) + 1))
+
+
+# ------------------------------------------------------------------- timing
+
+
+def _hold_stream(torch, seconds):
+    """Keep the stream busy for about `seconds` with a device-side spin, so that
+    the host enqueues the whole timed region before the GPU reaches it: the
+    events then measure device time, not Python / launch latency."""
+    seconds = min(seconds, 0.05)  # under a profiler host launches are slow: cap the hold
+    torch.cuda._sleep(int(seconds * 2.2e9))  # cycles at (or above) the maximum SM clock
+
+
+def _barrier_max(torch, value, ws):
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _summary(c, ms):
+    return {k: c[k] for k in ("call", "bytes", "flops", "bound", "dtype")} | {"ms": ms}
+
+
+def time_steps(torch, wl, steps, warmup, replicas, ws):
+    """K steps over wl.calls, per-call CUDA events on the launching stream."""
+    stream = torch.cuda.current_stream()
+    t_host = time.perf_counter()
+    for s in range(warmup):
+        for c in wl.calls:
+            wl.run(s % replicas, c["index"])
+    host_per_step = (time.perf_counter() - t_host) / max(1, warmup)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wl.calls]
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    _hold_stream(torch, 2.0 * host_per_step * steps + 2e-3)
+    t0.record(stream)
+    for s in range(steps):
+        for j, c in enumerate(wl.calls):
+            ev[s][j][0].record(stream)
+            wl.run(s % replicas, c["index"])
+            ev[s][j][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = _barrier_max(torch, t0.elapsed_time(t1), ws)
+    per_call = [_summary(c, statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(steps)))
+                for j, c in enumerate(wl.calls)]
+    return total_ms, per_call
+
+
+def time_calls_flushed(torch, wl, steps, warmup):
+    """Per-call device times (median ms), each call preceded by an L2 flush
+    (a 2 x L2 buffer overwritten outside the events)."""
+    stream = torch.cuda.current_stream()
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        for c in wl.calls:
+            wl.run(0, c["index"])
+    torch.cuda.synchronize()
+    ev = {c["call"]: [] for c in wl.calls}
+    _hold_stream(torch, 80e-6 * steps * len(wl.calls) + 2e-3)
+    for _ in range(steps):
+        for c in wl.calls:
+            scratch.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            wl.run(0, c["index"])
+            e1.record(stream)
+            ev[c["call"]].append((e0, e1))
+    torch.cuda.synchronize()
+    out = [_summary(c, statistics.median(a.elapsed_time(b) for a, b in ev[c["call"]])) for c in wl.calls]
+    del scratch
+    return out
+
+
+def roofline_for(call, peaks, traffic=None):
+    if call["bound"] == "hbm":
+        achieved = call["bytes"] / (call["ms"] * 1e-3) / 1e9
+        peak, unit, src = peaks["hbm_gbs"], "GB/s", peaks["source"] + " HBM copy"
+    else:
+        ratio = NOMINAL_RATIO[call["dtype"]]
+        achieved = call["flops"] / (call["ms"] * 1e-3) / 1e12
+        peak, unit = peaks["bf16_tflops"] * ratio, "TFLOP/s"
+        src = peaks["source"] + (f" bf16 burst x {ratio:g} (nominal {call['dtype']}/bf16 ratio)" if ratio != 1
+                                 else " bf16 burst")
+    return {"bound": call["bound"], "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel_call": call["call"], "peak_source": src}
+
+
+# ------------------------------------------------------------------- clocks
 
 
 def _sample_clocks():
@@ -164,76 +343,28 @@ def _finish_clocks(proc, pci):
     return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------- the arms
+
+
 def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def _barrier_max(torch, value, ws):
-    if ws == 1:
-        return value
-    import torch.distributed as dist
-
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+def _unit_of(calls):
+    return "GB/s" if all(c["bound"] == "hbm" for c in calls) else "TFLOP/s"
 
 
-def _hold_stream(torch, seconds):
-    """Keep the stream busy for about `seconds` (a device-side spin) so that the
-    host can enqueue the whole timed region before the GPU reaches it: the
-    events then measure device time only, not Python / launch latency."""
-    torch.cuda._sleep(int(seconds * 2.2e9))  # cycles at or above the maximum SM clock
+def _throughput(calls, unit, seconds, factor=1):
+    if unit == "GB/s":
+        return factor * sum(c["bytes"] for c in calls) / seconds / 1e9
+    return factor * sum(c["flops"] for c in calls) / seconds / 1e12
 
 
-def time_workload(torch, wl, steps, warmup, replicas, ws):
-    """Time `steps` passes over wl.calls; per-launch CUDA events on the launching stream."""
-    stream = torch.cuda.current_stream()
-    n_calls = len(wl.calls)
-    t_host = time.perf_counter()
-    for s in range(warmup):
-        for (_, i, _, _) in wl.calls:
-            wl.run(s % replicas, i)
-    host_per_step = (time.perf_counter() - t_host) / max(1, warmup)
-    torch.cuda.synchronize()
-    if ws > 1:
-        torch.distributed.barrier()
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
-          for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    _hold_stream(torch, 2.0 * host_per_step * steps + 2e-3)
-    t0.record(stream)
-    for s in range(steps):
-        for j, (_, i, _, _) in enumerate(wl.calls):
-            ev[s][j][0].record(stream)
-            wl.run(s % replicas, i)
-            ev[s][j][1].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if ws > 1:
-        torch.distributed.barrier()
-    total_ms = _barrier_max(torch, t0.elapsed_time(t1), ws)
-    per_call = []
-    for j, (name, _, nbytes, flops) in enumerate(wl.calls):
-        ms = [ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(steps)]
-        per_call.append({"call": name, "ms": statistics.mean(ms), "bytes": nbytes, "flops": flops})
-    return total_ms, per_call
-
-
-def roofline_for(call, peaks, bound, dtype="fp16", traffic=None):
-    if bound == "hbm":
-        achieved = call["bytes"] / (call["ms"] * 1e-3) / 1e9
-        peak, unit = peaks["hbm_gbs"], "GB/s"
-    else:
-        achieved = call["flops"] / (call["ms"] * 1e-3) / 1e12
-        peak, unit = peaks["bf16_tflops"] * NOMINAL_RATIO[dtype], "TFLOP/s"
-    return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel_call": call["call"],
-            "peak_source": peaks["source"] + (f" (bf16 x {NOMINAL_RATIO[dtype]} nominal ratio)" if bound == "tensor"
-                                              and dtype != "bf16" else "")}
+DTYPES = {"w8a16": "int8 weights x fp16 activations, fp32 accumulate",
+          "w4a16": "int4 weights x fp16 activations, fp32 accumulate",
+          "mxfp4": "e2m1 x e2m1 with e8m0 block scales, fp32 accumulate",
+          "fp8": "e4m3 x e4m3, fp32 accumulate, bf16 out"}
 
 
 def run_ours(args):
@@ -248,63 +379,72 @@ def run_ours(args):
     import bit_quantized_gemm_dequant_gb300 as wq
 
     peaks = load_peaks()
-    replicas = 3
-    spec = workloads.WORKLOADS[args.workload]
-    bits = 4 if spec["op"] == "w4a16" else 8
-    wl = WeightOnly(wq, torch, bits, spec["shapes"], replicas)
-    step_bytes = sum(c[2] for c in wl.calls)
+    probe = make_workload(torch, wq, args.workload, 1, args.only)
+    step_bytes = sum(c["bytes"] for c in probe.calls)
+    del probe
+    torch.cuda.empty_cache()
+    replicas = replicas_for(step_bytes)
+    wl = make_workload(torch, wq, args.workload, replicas, args.only)
+    unit = _unit_of(wl.calls)
 
     clock_proc = _sample_clocks() if rank == 0 else None
-    total_ms, per_call = time_workload(torch, wl, args.steps, args.warmup, replicas, ws)
+    total_ms, per_call = time_steps(torch, wl, args.steps, args.warmup, replicas, ws)
     clocks = _finish_clocks(clock_proc, _pci_bus_id(torch, local)) if rank == 0 else None
 
-    value = ws * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    value = _throughput(wl.calls, unit, total_ms * 1e-3 / args.steps, factor=ws)
     dominant = max(per_call, key=lambda c: c["ms"])
-    roof = roofline_for(dominant, peaks, "hbm", traffic=args.traffic)
+    roof = roofline_for(dominant, peaks, traffic=args.traffic)
 
-    # End to end through the public API with pinned host buffers: H2D of the
-    # step's inputs, the call, D2H of the result, every step.
-    host = wl.host_inputs()
-    stream = torch.cuda.current_stream()
-    for _ in range(2):
-        for (_, i, _, _) in wl.calls:
-            wl.e2e_step(host, i, stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
-    h2d = d2h = 0
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    e2e = None
+    if not args.no_e2e and hasattr(wl, "e2e_call"):
+        host = wl.host_inputs()
+        for c in wl.calls:
+            wl.e2e_call(host, c["index"])
+        torch.cuda.synchronize()
+        n = max(1, min(args.steps, 10))
         h2d = d2h = 0
-        for (_, i, _, _) in wl.calls:
-            _, bi, bo = wl.e2e_step(host, i, stream)
-            h2d += bi
-            d2h += bo
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = _barrier_max(torch, e0.elapsed_time(e1), ws)
-    e2e_val = ws * step_bytes * e2e_steps / (e2e_ms * 1e-3) / 1e9
+        t0 = time.perf_counter()
+        for _ in range(n):
+            h2d = d2h = 0
+            for c in wl.calls:
+                bi, bo = wl.e2e_call(host, c["index"])
+                h2d += bi
+                d2h += bo
+        torch.cuda.synchronize()
+        e2e_s = _barrier_max(torch, time.perf_counter() - t0, ws)
+        e2e = {"value": round(_throughput(wl.calls, unit, e2e_s / n, factor=ws), 3), "unit": unit,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "how": "wall clock over steps of: pinned-host -> device copies of X, W and scales, the C-ABI call, "
+                      "device -> pinned-host copy of Y; one synchronize at the end"}
 
     breakdown = []
     if not args.no_breakdown and rank == 0:
-        breakdown = run_breakdown(torch, wq, peaks, args)
+        for name in ("w4a16_llama7b", "mxfp4", "fp8"):
+            if name == args.workload:
+                continue
+            other = make_workload(torch, wq, name, 1)
+            for c in time_calls_flushed(torch, other, 5, 3):
+                breakdown.append({"workload": name, **c, "roofline": roofline_for(c, peaks)})
+            del other
+            torch.cuda.empty_cache()
 
-    cpu = cpu_baseline(wl, step_bytes, budget_s=args.cpu_budget) if (rank == 0 and ws == 1) else None
+    cpu = cpu_baseline(wl, unit, args.cpu_budget) if (rank == 0 and ws == 1 and args.cpu_budget > 0) else None
 
     if rank == 0:
+        op = workloads.WORKLOADS[args.workload]["op"]
         line = {
-            "metric": "W4A16/W8A16 GEMV HBM GB/s (% peak); MXFP4/FP8 GEMM TFLOPS (% peak)",
-            "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8/int4 weights x fp16 activations, fp32 accumulate", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: " + ", ".join(f"{m}x{k}x{n}" for (m, k, n) in spec["shapes"]),
-                       "shapes_MxKxN": spec["shapes"], "seed": 0, "replicas": replicas,
-                       "l2": f"inputs rotate over {replicas} replicas; one step reads "
-                             f"{step_bytes / 1e6:.0f} MB (> {L2_BYTES / 1e6:.0f} MB L2)",
+            "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPES[op],
+            "data": "synthetic (seeded numpy; shapes and distributions of the workload)",
+            "config": {"workload": f"{args.workload}: " + ", ".join(c["call"] for c in wl.calls), "seed": 0,
+                       "replicas": replicas,
+                       "l2": f"inputs rotate over {replicas} replicas of {step_bytes / 1e6:.0f} MB per step "
+                             f"(> 2 x {L2_BYTES / 1e6:.0f} MB L2 between reuses)",
                        "parallelism": f"replicas x{ws}"},
             "roofline": roof,
-            "per_call": [{**c, "GBps": round(c["bytes"] / (c["ms"] * 1e-3) / 1e9, 1)} for c in per_call],
-            "e2e": {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "per_call": [{**c, "achieved": roofline_for(c, peaks)["achieved"]} for c in per_call],
+            "e2e": e2e,
             "gpu_launches": len(wl.calls) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -315,104 +455,24 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def time_calls(torch, calls, steps, warmup, flush_bytes=2 * L2_BYTES):
-    """Per-call CUDA-event times (ms) on the launching stream.  Before every
-    call an L2-sized buffer is overwritten (outside the events), so no call
-    starts with its operands in L2."""
-    stream = torch.cuda.current_stream()
-    scratch = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda")
-    for _ in range(warmup):
-        for c in calls:
-            c["run"]()
-    torch.cuda.synchronize()
-    ev = {c["call"]: [] for c in calls}
-    _hold_stream(torch, 60e-6 * steps * len(calls) + 2e-3)
-    for _ in range(steps):
-        for c in calls:
-            scratch.fill_(1.0)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            c["run"]()
-            e1.record(stream)
-            ev[c["call"]].append((e0, e1))
-    torch.cuda.synchronize()
-    out = []
-    for c in calls:
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev[c["call"]])
-        out.append({"call": c["call"], "ms": ms, "bytes": c["bytes"], "flops": c["flops"]})
-    del scratch
-    return out
-
-
-def run_breakdown(torch, wq, peaks, args):
-    """Other workloads, each timed over a few steps with its own roofline."""
-    out = []
-    steps, warm = 5, 3
-
-    spec = workloads.WORKLOADS["w4a16_llama7b"]
-    wl = WeightOnly(wq, torch, 4, spec["shapes"], 1)
-    calls = [{"call": name, "run": (lambda i=i: wl.run(0, i)), "bytes": nb, "flops": fl}
-             for (name, i, nb, fl) in wl.calls]
-    for c in time_calls(torch, calls, steps, warm):
-        M = int(c["call"].split("_")[1].split("x")[0])
-        bound = "hbm" if M <= 64 else "tensor"
-        out.append({"workload": "w4a16_llama7b", **c, "roofline": roofline_for(c, peaks, bound, "fp16")})
-    del wl, calls
-    torch.cuda.empty_cache()
-
-    # MXFP4: quantize both fp32 operands on the device, then the GEMM.
-    K = N = 8192
-    w_src = torch.from_numpy(workloads.mx_source(N, K, seed=0, stream=1)).cuda()
-    wd, ws = wq.mx_quantize_fp4(w_src)
-    calls = [{"call": f"mx_quantize_{N}x{K}", "run": (lambda: wq.mx_quantize_fp4(w_src, wd, ws)),
-              "bytes": N * K * 4 + N * K // 2 + N * K // 32, "flops": 0, "bound": "hbm"}]
-    keep = []
-    for M in (128, 2048, 8192):
-        a_src = torch.from_numpy(workloads.mx_source(M, K, seed=0, stream=0)).cuda()
-        ad, asc = wq.mx_quantize_fp4(a_src)
-        c_out = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        keep.append((a_src, ad, asc, c_out))
-        calls.append({"call": f"mx_gemm_{M}x{K}x{N}",
-                      "run": (lambda ad=ad, asc=asc, c_out=c_out: wq.mx_gemm_fp4(ad, asc, wd, ws, c=c_out)),
-                      "bytes": (M + N) * (K // 2 + K // 32) + 4 * M * N, "flops": 2 * M * N * K,
-                      "bound": "hbm" if M <= 128 else "tensor"})
-    for c, spec_c in zip(time_calls(torch, calls, steps, warm), calls):
-        out.append({"workload": "mxfp4", **c, "roofline": roofline_for(c, peaks, spec_c["bound"], "fp4")})
-    del keep, calls, w_src, wd, ws
-    torch.cuda.empty_cache()
-
-    calls, keep = [], []
-    for (M, K, N) in workloads.WORKLOADS["fp8"]["shapes"]:
-        case = workloads.fp8_case(M, K, N, seed=0)
-        a = torch.from_numpy(case.a8).cuda()
-        b = torch.from_numpy(case.b8).cuda()
-        cc = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        keep.append((a, b, cc))
-        calls.append({"call": f"fp8_{M}x{K}x{N}",
-                      "run": (lambda a=a, b=b, cc=cc, sa=case.scale_a, sb=case.scale_b: wq.fp8_gemm(a, b, sa, sb, c=cc)),
-                      "bytes": M * K + K * N + 2 * M * N, "flops": 2 * M * N * K,
-                      "bound": "hbm" if M <= 16 else "tensor"})
-    for c, spec_c in zip(time_calls(torch, calls, steps, warm), calls):
-        out.append({"workload": "fp8", **c, "roofline": roofline_for(c, peaks, spec_c["bound"], "fp8")})
-    del keep, calls
-    torch.cuda.empty_cache()
-    return out
-
-
-def cpu_baseline(wl, step_bytes, budget_s=15.0):
-    """The oracle as it stands on this host, over whole steps until ~budget_s."""
+def cpu_baseline(wl, unit, budget_s):
+    """The oracle as it stands on this host: whole calls of the workload, in
+    order, until about budget_s seconds have passed."""
+    if not hasattr(wl, "oracle_call"):
+        return None
     t0 = time.perf_counter()
-    n = 0
-    while True:
-        for (_, i, _, _) in wl.calls:
-            wl.oracle_call(i)
-        n += 1
-        if time.perf_counter() - t0 >= budget_s or n >= 20:
-            break
+    nbytes = nflops = ncalls = 0
+    while time.perf_counter() - t0 < budget_s and ncalls < 200:
+        c = wl.calls[ncalls % len(wl.calls)]
+        b, f = wl.oracle_call(c["index"])
+        nbytes += b
+        nflops += f
+        ncalls += 1
     dt = time.perf_counter() - t0
-    return {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{n} full step(s) of the workload on the CPU oracle (numpy float64, BLAS threads = cores)"}
+    value = nbytes / dt / 1e9 if unit == "GB/s" else nflops / dt / 1e12
+    return {"value": round(value, 5), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{ncalls} oracle call(s) of the workload in order ({dt:.1f} s; numpy float64, "
+                      f"BLAS threads = cores)"}
 
 
 def run_reference(args):
@@ -420,14 +480,18 @@ def run_reference(args):
     if rank != 0:
         return
     spec = workloads.WORKLOADS[args.workload]
+    if spec["op"] not in ("w4a16", "w8a16"):
+        print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the weight-only workloads"}))
+        return
     from oracle import wq_oracle as O
 
     bits = 4 if spec["op"] == "w4a16" else 8
-    cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, 0) for (M, K, N) in spec["shapes"]]
+    shapes = spec["shapes"]
+    cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, 0) for (M, K, N) in shapes]
     fn = O.gemm_w4a16 if bits == 4 else O.gemm_w8a16
     # A bounded sample of the workload per step: the first `per_step` calls.
-    per_step = 2 if args.steps + args.warmup > 4 else len(cases)
-    sample_bytes = sum(_wo_bytes(bits, *spec["shapes"][i]) for i in range(per_step))
+    per_step = len(cases) if args.steps + args.warmup <= 4 else 2
+    sample_bytes = sum(_wo_bytes(bits, *shapes[i]) for i in range(per_step))
     for _ in range(args.warmup):
         for c in cases[:per_step]:
             fn(c.x, c.w, c.scales)
@@ -438,13 +502,12 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     value = sample_bytes * args.steps / dt / 1e9
     sample = f"first {per_step} call(s) of the workload per step: " + ", ".join(
-        f"{m}x{k}x{n}" for (m, k, n) in spec["shapes"][:per_step])
+        f"{m}x{k}x{n}" for (m, k, n) in shapes[:per_step])
     print(json.dumps({
-        "impl": "reference", "metric": "W4A16/W8A16 GEMV HBM GB/s (% peak); MXFP4/FP8 GEMM TFLOPS (% peak)",
-        "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: " + ", ".join(f"{m}x{k}x{n}" for (m, k, n) in spec["shapes"]),
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: " + ", ".join(f"{m}x{k}x{n}" for (m, k, n) in shapes),
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
@@ -458,14 +521,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="w8a16_decode", choices=["w8a16_decode", "w4a16_llama7b", "w4a16_tiny"])
+    ap.add_argument("--workload", default="w8a16_decode", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--only", default=None, help="keep only the calls whose name contains this string")
     ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
-                    help="dram bytes per launch of the dominant kernel from an ncu capture of this build")
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture of this build")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
+    args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args)
     else:

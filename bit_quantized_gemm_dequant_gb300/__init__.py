@@ -94,6 +94,28 @@ def _ws(workspace):
     return (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (_p(0), 0)
 
 
+_WS_CACHE: dict = {}
+
+
+def auto_workspace(op: int, M: int, N: int, K: int, device):
+    """A device workspace of at least wq_workspace_size(op, M, N, K) bytes,
+    zero-filled when created, cached per (device, stream) and grown on demand.
+    Every successful call leaves its counter area zero again, so the cached
+    buffer is reused as is; calls that share one must not overlap on the GPU
+    (one cache entry per stream)."""
+    import torch
+
+    need = wq_workspace_size(op, M, N, K)
+    if need == 0:
+        return None
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _WS_CACHE.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=device)
+        _WS_CACHE[key] = buf
+    return buf
+
+
 def wq_gemm_w4a16(x, wq, scales, y=None, workspace=None, stream=None):
     """Y fp16 [M, N] = X fp16 [M, K] * ((unpack(wq [K/2, N]) - 8) * scales[N])."""
     import torch
@@ -102,6 +124,8 @@ def wq_gemm_w4a16(x, wq, scales, y=None, workspace=None, stream=None):
     N = wq.shape[1]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = auto_workspace(WQ_OP_W4A16, M, N, K, x.device)
     wsp, wsb = _ws(workspace)
     _check(lib.wq_gemm_w4a16(M, N, K, _ptr(x), _ld(x), _ptr(wq), _ld(wq), _ptr(scales), _ptr(y), _ld(y),
                              wsp, wsb, _stream(stream)), "wq_gemm_w4a16")
@@ -116,6 +140,8 @@ def wq_gemm_w8a16(x, w, scales, y=None, workspace=None, stream=None):
     N = w.shape[1]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = auto_workspace(WQ_OP_W8A16, M, N, K, x.device)
     wsp, wsb = _ws(workspace)
     _check(lib.wq_gemm_w8a16(M, N, K, _ptr(x), _ld(x), _ptr(w), _ld(w), _ptr(scales), _ptr(y), _ld(y),
                              wsp, wsb, _stream(stream)), "wq_gemm_w8a16")

@@ -11,19 +11,27 @@
 // E2M1 operands stay packed (two per byte) from HBM to the tensor core, and
 // the UE8M0 block scales ride along in tensor memory.
 //
-// Design: one 128 x 128 output tile per CTA, K in 256-element (128-byte)
-// steps through a 6-stage ring.
+// Design: one 128 x 256 output tile per CTA, K in 256-element (128-byte)
+// steps through a 4-stage ring.
 //   warp 0      producer.  Lane 0 issues the TMA loads of the A and W data
-//               tiles (128 rows x 128 bytes, 128-byte swizzle).  All lanes
-//               gather the stage's 8 E8M0 bytes of each of the 256 rows and
-//               write them in the 128-row x 4-block chunk layout the scale
-//               copy expects (byte 16*(r%32) + 4*(r/32) + kb of a 512-byte
-//               chunk), then arrive on the stage's barrier.
-//   warp 1      TMEM allocator and MMA issuer: per stage, four tcgen05.cp
-//               32x128b.warpx4 (scale chunks -> TMEM) and four
-//               tcgen05.mma 128 x 128 x 64 with scale_vec::2X, the scale
-//               byte pair chosen by the descriptor's scale-factor ids.
+//               tiles (A 128 rows, W 256 rows, x 128 bytes, 128-byte swizzle)
+//               and of the stage's E8M0 bytes: a 16-byte box per row (the 16
+//               blocks of two stages; the box must start on a 16-byte column).
+//   warp 2      scale-layout warp during the main loop: rewrites the stage's
+//               8 scale bytes per row, in place, into the 128-row x 4-block
+//               chunk layout tcgen05.cp expects (byte 16*(r%32) + 4*(r/32) + kb
+//               of a 512-byte chunk).  Each lane reads exactly the rows whose
+//               bytes it then overwrites, so no lane waits on another.
+//   warp 1      TMEM allocator and MMA issuer: per stage, six tcgen05.cp
+//               32x128b.warpx4 (scale chunks -> TMEM) and eight
+//               tcgen05.mma 128 x 128 x 64 with scale_vec::2X (four K steps
+//               x two 128-column halves sharing the A tile and its scales),
+//               the scale byte pair chosen by the descriptor's scale-factor
+//               ids.
 //   warps 2-5   epilogue: tcgen05.ld and FP32 stores.
+// Scale arrays whose row stride is not a multiple of 16 bytes cannot be
+// described to TMA; for them the producer warp gathers the bytes with plain
+// loads and writes the chunk layout itself (slower, same result).
 #include "tc_common.cuh"
 #include "tma_host.h"
 #include "wq_internal.h"
@@ -31,18 +39,19 @@
 namespace wq {
 namespace {
 
-constexpr int BM = 128, BN = 128;
+constexpr int BM = 128, BN = 256;
 constexpr int BKB = 128;                    // K bytes per stage (256 E2M1 elements)
 constexpr int kBlocksPerStage = BKB * 2 / 32;  // 8 scale blocks
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kABytes = BM * BKB;           // 16 KB
 constexpr int kBBytes = BN * BKB;           // 16 KB
 constexpr int kSfChunk = 512;               // 128 rows x 4 blocks
-constexpr int kSfBytes = 4 * kSfChunk;      // A: 2 chunks, W: 2 chunks
-constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // 34 KB (multiple of 1024)
+constexpr int kSfRowBytes = 16;             // scale bytes per row and TMA box (two stages)
+constexpr int kSfBytes = (BM + BN) * kSfRowBytes;  // 6 KB: raw boxes, rewritten into 6 chunks in place
+constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // 54 KB (multiple of 1024)
 constexpr int kAccCols = BN;                // FP32 accumulator columns
-constexpr int kSfColsPerStage = 16;         // 4 chunks x 4 columns
-constexpr int kTmemCols = 256;              // accumulator + 6 x 16 scale columns, rounded up
+constexpr int kSfColsPerStage = 24;         // 6 chunks x 4 columns
+constexpr int kTmemCols = 512;              // accumulator + 4 x 24 scale columns, rounded up
 constexpr int kThreads = 192;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 
@@ -72,14 +81,40 @@ __device__ __forceinline__ void load_sf8(const uint8_t* S, int64_t ld, int row, 
   hi = w[1];
 }
 
+// Rewrite the stage's raw scale boxes (A: 128 rows, W: 256 rows, 16 bytes
+// each; the stage uses bytes 8h .. 8h+7) into six chunks at the start of the
+// same area: [A kb 0-3][A kb 4-7][W 0-127 kb 0-3][W 0-127 kb 4-7][W 128-255
+// kb 0-3][W 128-255 kb 4-7].  Lane l reads rows l + 32q of each 128-row
+// group and writes line l of each chunk, which lies in bytes it read.
+__device__ __forceinline__ void sf_to_chunks(uint8_t* sf, int h, int lane) {
+  uint32_t v[3][2][4];
+#pragma unroll
+  for (int grp = 0; grp < 3; ++grp)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* row = sf + (grp * 128 + lane + 32 * q) * kSfRowBytes + 8 * h;
+      v[grp][0][q] = *reinterpret_cast<const uint32_t*>(row);
+      v[grp][1][q] = *reinterpret_cast<const uint32_t*>(row + 4);
+    }
+#pragma unroll
+  for (int grp = 0; grp < 3; ++grp)
+#pragma unroll
+    for (int half = 0; half < 2; ++half)
+      *reinterpret_cast<uint4*>(sf + (2 * grp + half) * kSfChunk + 16 * lane) =
+          make_uint4(v[grp][half][0], v[grp][half][1], v[grp][half][2], v[grp][half][3]);
+}
+
+template <bool kSfTma>
 __global__ void __launch_bounds__(kThreads, 1)
-mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
+mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW, MxGemmArgs p,
                int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* accum = empty + kStages;
+  uint64_t* sf_ready = empty + kStages;
+  uint64_t* accum = sf_ready + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -90,8 +125,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], 2);  // TMA transaction arrival + scale gather arrival
+      // TMA mode: the transaction bytes alone complete a stage.  Gather mode:
+      // the TMA arrival plus the producer warp's scale arrival.
+      tc::mbar_init(&full[s], kSfTma ? 1 : 2);
       tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&sf_ready[s], 1);
     }
     tc::mbar_init(accum, 1);
     *abort = 0;
@@ -110,6 +148,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmA);
       tc::tma_prefetch_desc(&tmW);
+      if (kSfTma) {
+        tc::tma_prefetch_desc(&tmSA);
+        tc::tma_prefetch_desc(&tmSW);
+      }
     }
     const bool a4 = ((reinterpret_cast<uintptr_t>(p.SA) | static_cast<uintptr_t>(p.ldsa)) & 3) == 0;
     const bool w4 = ((reinterpret_cast<uintptr_t>(p.SW) | static_cast<uintptr_t>(p.ldsw)) & 3) == 0;
@@ -119,30 +161,37 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool free_slot = tc::mbar_wait(&empty[s], ((kt / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
       if (!__all_sync(0xffffffffu, free_slot)) break;  // warp-uniform exit
       uint8_t* st = smem + s * kStageBytes;
+      uint8_t* sf = st + kABytes + kBBytes;
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+        tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + (kSfTma ? kSfBytes : 0));
         tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
         tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
-      }
-      // Scale chunks: [A blocks 0-3][A blocks 4-7][W blocks 0-3][W blocks 4-7].
-      uint8_t* sf = st + kABytes + kBBytes;
-      const int kb0 = kt * kBlocksPerStage;
-#pragma unroll
-      for (int side = 0; side < 2; ++side) {
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = lane + 32 * i;
-          if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0, nkb, a4, lo[i], hi[i]);
-          else load_sf8(p.SW, p.ldsw, n0 + r, p.N, kb0, nkb, w4, lo[i], hi[i]);
+        if (kSfTma) {
+          const int x = kSfRowBytes * (kt / 2);  // 16-byte aligned column of the scale arrays
+          tc::tma_load_2d(sf, &tmSA, x, m0, &full[s]);
+          tc::tma_load_2d(sf + BM * kSfRowBytes, &tmSW, x, n0, &full[s]);
         }
-        uint8_t* c0 = sf + side * 2 * kSfChunk;
-        *reinterpret_cast<uint4*>(c0 + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(c0 + kSfChunk + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
-      tc::fence_proxy_async_smem();  // scale bytes -> visible to tcgen05.cp
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&full[s]);
+      if (!kSfTma) {
+        // Gather: chunks [A 0-3][A 4-7][W 0-127: 0-3][4-7][W 128-255: 0-3][4-7].
+        const int kb0 = kt * kBlocksPerStage;
+#pragma unroll
+        for (int side = 0; side < 3; ++side) {
+          uint32_t lo[4], hi[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0, nkb, a4, lo[i], hi[i]);
+            else load_sf8(p.SW, p.ldsw, n0 + 128 * (side - 1) + r, p.N, kb0, nkb, w4, lo[i], hi[i]);
+          }
+          uint8_t* c0 = sf + side * 2 * kSfChunk;
+          *reinterpret_cast<uint4*>(c0 + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(c0 + kSfChunk + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
+        tc::fence_proxy_async_smem();  // scale bytes -> visible to tcgen05.cp
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&full[s]);
+      }
       issued = kt + 1;
     }
     if (*abort && lane == 0) {
@@ -152,27 +201,44 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1 && lane == 0) {
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % kStages;
-      if (!tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmMma)) break;
+      uint64_t* ready = kSfTma ? &sf_ready[s] : &full[s];
+      if (!tc::mbar_wait(ready, (kt / kStages) & 1, abort, err, kSiteGemmMma)) break;
       tc::tc_fence_after();
       const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
       const uint32_t b = a + kABytes;
       const uint32_t sf = b + kBBytes;
       const uint32_t sf_col = tmem + kAccCols + s * kSfColsPerStage;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)  // A chunk 0, A chunk 1, W chunk 0, W chunk 1
+      for (int c = 0; c < 6; ++c)  // A chunks 0-1, W rows 0-127 chunks 0-1, W rows 128-255 chunks 0-1
         tc::tmem_cp_32x128b_warpx4(sf_col + 4 * c, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // 64 elements = 32 bytes per MMA
         const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
-        const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
         const uint32_t id = 2 * (j & 1);
-        const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
-        tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 4 * (j >> 1), (kt | j) != 0);
+        const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, 128, id, id);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t bdesc = tc::smem_desc(b + h * 128 * BKB + 32 * j, 1024, 1024, tc::kSwizzle128B);
+          tc::mma_mxf4(tmem + 128 * h, adesc, bdesc, idesc, sf_col + 4 * (j >> 1),
+                       sf_col + 8 + 8 * h + 4 * (j >> 1), (kt | j) != 0);
+        }
       }
       tc::tc_commit(&empty[s]);
     }
     tc::tc_commit(accum);
   } else if (warp >= 2) {
+    if (kSfTma && warp == 2) {
+      // Scale-layout duty during the main loop.
+      for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % kStages;
+        const bool ok = tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmMma);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        sf_to_chunks(smem + s * kStageBytes + kABytes + kBBytes, kt & 1, lane);
+        tc::fence_proxy_async_smem();  // chunk bytes -> visible to tcgen05.cp
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sf_ready[s]);
+      }
+    }
     const bool ok = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
     const int q = warp & 3;
@@ -206,20 +272,35 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
   if (a.K == 0)
     return cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
-  CUtensorMap tA, tW;
+  CUtensorMap tA, tW, tSA, tSW;
   cudaError_t e = make_tmap_2d(&tA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.lda, BKB, BM,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.N, a.ldw, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // Scale arrays go through TMA when their rows start on 16-byte boundaries.
+  const bool sf_tma = ((reinterpret_cast<uintptr_t>(a.SA) | reinterpret_cast<uintptr_t>(a.SW) |
+                        static_cast<uintptr_t>(a.ldsa) | static_cast<uintptr_t>(a.ldsw)) & 15) == 0;
+  if (sf_tma) {
+    e = make_tmap_2d(&tSA, a.SA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 32, a.M, a.ldsa, kSfRowBytes, BM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
-    configured = true;
+    e = make_tmap_2d(&tSW, a.SW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 32, a.N, a.ldsw, kSfRowBytes, BN,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  } else {
+    tSA = tA;  // unused by the gather variant
+    tSW = tW;
+  }
+  auto kern = sf_tma ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
+  static bool configured[2] = {false, false};
+  if (!configured[sf_tma]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[sf_tma] = true;
   }
   dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
-  mx_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tA, tW, a, device_error_word());
+  kern<<<grid, kThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
   return cudaGetLastError();
 }
 

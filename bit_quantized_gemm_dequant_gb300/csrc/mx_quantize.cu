@@ -15,7 +15,7 @@ namespace wq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;  // blocks in flight per thread quad
+constexpr int kUnroll = 4;  // blocks in flight per thread quad
 
 __device__ __forceinline__ uint32_t e2m1_code(float x, float inv_scale) {
   // v = x * 2^-e is exact (a power-of-two scaling); the comparisons below
@@ -27,7 +27,7 @@ __device__ __forceinline__ uint32_t e2m1_code(float x, float inv_scale) {
   return (x < 0.0f ? 8u : 0u) | j;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 mx_quantize_kernel(MxQuantArgs p, int64_t n_items) {
   // A warp owns 8 consecutive blocks (1 KB of source) per step; the loop
   // bound is warp-uniform so that every lane reaches the quad shuffles.
@@ -90,7 +90,7 @@ cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s) {
   if (n_items == 0) return cudaSuccess;
   const int64_t blocks_per_cta = kThreads / 4;  // one 32-element block per thread quad
   int64_t ctas = (n_items + blocks_per_cta * kUnroll - 1) / (blocks_per_cta * kUnroll);
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // 8 resident CTAs per SM
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 3;  // resident CTAs per SM (<= 85 registers)
   if (ctas > cap) ctas = cap;
   mx_quantize_kernel<<<static_cast<unsigned>(ctas), kThreads, 0, s>>>(a, n_items);
   return cudaGetLastError();

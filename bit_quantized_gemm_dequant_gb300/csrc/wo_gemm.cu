@@ -185,6 +185,7 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           r[c] = h2_sub((b ^ 0x00800080u) | 0x64006400u, 0x64806480u);  // minus 1152
         }
       }
+      tc::fence_proxy_async_smem();  // generic reads of the tile before its TMA refill
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&empty[s]);  // this warp is done with the packed tile
       tc::tc_fence_after();
@@ -245,7 +246,6 @@ cudaError_t launch_tc(const WoArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s) {
-  if (a.M <= 64) return launch_wo_skinny(a, bits, s);  // HBM-bound: the split-K register path
   if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
   return bits == 4 ? launch_tc<4, 256>(a, s) : launch_tc<8, 256>(a, s);
 }

@@ -5,62 +5,85 @@
 // (q - 8) * s[n], FP32 accumulation, FP16 output) and "Triton 量化算子：W8A16
 // 权重量化融合矩阵乘法" Step 1 / Step 3 (INT8: Y = X (W_int8 S), W [K, N]).
 //
-// Design (HBM-bound; the packed weights are read exactly once):
-//   * A warp owns 128 output columns and a slice of K.  Each thread streams
-//     16-byte vectors of packed weights with non-allocating 128-bit loads
-//     (a warp covers 128 contiguous bytes per weight row), a whole slice of
-//     loads in flight before any math.
-//   * The weights are dequantized in registers straight into the A operand
-//     of mma.sync.m16n8k16 (Y^T = W^T X^T: weight columns are the MMA rows,
-//     the M <= 16 activation rows the MMA columns).  The dequantized weight
-//     never touches shared or global memory.  INT4 codes become exact fp16
-//     (q - 8) with one LOP3 (0x6400 | nibble = 1024 + nibble) and one
-//     HSUB2/HFMA2 per two weights; INT8 with one LOP3 (byte ^ 0x80 | 0x6400)
-//     and one HSUB2.  The per-column scale factors out of the K sum and is
-//     applied once in the epilogue (exact reordering: it is per column).
-//   * Split-K: the warps of a CTA take different K slices and reduce through
-//     shared memory; the CTAs of a thread-block cluster (up to 8) take
-//     further slices and reduce through distributed shared memory, each CTA
-//     finishing a 1/C share of the columns.  No workspace, one launch.
+// Design (HBM-bound; the packed weights are read from HBM exactly once):
+//   * A CTA owns 128 output columns and a slice of K.  One producer thread
+//     streams the packed weight tile of every 64-k chunk (INT8: 64 rows x 128
+//     bytes, INT4: 32 rows x 128 bytes) with TMA into a 64 KB shared-memory
+//     ring, so up to 64 KB per CTA (three CTAs per SM) is in flight no matter
+//     what the consumers are doing.
+//   * Consumer warps take the chunks round-robin.  Each thread reads 16-byte
+//     vectors of packed weights from shared memory and dequantizes them in
+//     registers straight into the A operand of mma.sync.m16n8k16
+//     (Y^T = W^T X^T: weight columns are the MMA rows, the M <= 16 activation
+//     rows the MMA columns).  INT4 codes become exact fp16 (q - 8) with one
+//     LOP3 (0x6400 | nibble = 1024 + nibble) and one HSUB2/HFMA2 per two
+//     weights; INT8 with one LOP3 (byte ^ 0x80 | 0x6400) and one HSUB2.  The
+//     per-column scale factors out of the K sum and is applied once in the
+//     epilogue (exact reordering: it is per column).
 //   * INT4 MMA k-order: a register of the A fragment holds the low (or high)
 //     nibbles of the same byte column from K-pair rows c and c + 4, so one
 //     PRMT serves four weights; the activation fragment is permuted to the
 //     same k order (k0+2c, k0+2c+8 | k0+2c+1, k0+2c+9).
-#include <cooperative_groups.h>
+//   * Stream-K split: the grid is exactly the number of CTAs the GPU holds at
+//     once (three per SM), and the (M tile, 128-column tile, 64-k chunk) work
+//     units are dealt out as equal contiguous runs, so every SM streams the
+//     same number of bytes and the launch is a single wave.  Consumer warps
+//     reduce a tile's partial sums through shared memory; when a tile is
+//     split between CTAs, each writes its partial tile to the caller's
+//     workspace and the last one to arrive (per-tile counter) adds them in a
+//     fixed order, so the result is deterministic, and resets the counter.
 #include <cuda_fp16.h>
 
+#include "tc_common.cuh"
+#include "tma_host.h"
 #include "wq_internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace wq {
 namespace {
 
-constexpr int kTileN = 128;       // output columns per warp (and per CTA)
-constexpr int kRedPad = 4;        // shared-memory row padding (floats)
+constexpr int kTileN = 128;       // output columns per CTA
+constexpr int kChunkK = 64;       // k per pipeline stage
+constexpr int kRingBytes = 64 * 1024;
+constexpr int kConsumers = 4;     // consumer warps (plus one producer warp)
+constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kCtasPerSm = 3;
+// Workspace layout: a fixed counter area first (one int per tile, at most
+// kMaxSplitTiles tiles), so that the counters of any shape sit in bytes that
+// every call leaves zero; the partial tiles follow.
+constexpr int kMaxSplitTiles = 16384;
+constexpr size_t kCounterBytes = kMaxSplitTiles * sizeof(int);
 
-__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
+template <int BITS>
+struct Ring {
+  static constexpr int kRows = BITS == 4 ? kChunkK / 2 : kChunkK;  // rows of the packed tile
+  static constexpr int kStageBytes = kRows * kTileN;
+  static constexpr int kStages = kRingBytes / kStageBytes;
+};
+
+template <int MT>
+constexpr size_t skinny_smem_bytes() {
+  return kRingBytes + sizeof(float) * 8 * MT * kTileN + 512 + 128;
 }
 
-// 16 bytes at p, of which only the first `valid` (0..16) are read.
-__device__ __forceinline__ uint4 ldg_vec16(const uint8_t* p, int valid) {
-  if (valid >= 16) return ldg_stream16(p);
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  for (int i = 0; i < valid; ++i) w[i >> 2] |= static_cast<uint32_t>(p[i]) << (8 * (i & 3));
-  return make_uint4(w[0], w[1], w[2], w[3]);
+// Stream-K plan: U = tiles * chunks units over G CTAs; CTA b owns units
+// [b*U/G, (b+1)*U/G).
+struct Plan {
+  int n_tiles, tiles, chunks, grid, slots;
+  int64_t units;
+};
+
+__host__ __device__ __forceinline__ int64_t unit_lo(int b, int64_t U, int G) { return (int64_t)b * U / G; }
+// The CTA whose run contains unit u.
+__host__ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
 }
 
 __device__ __forceinline__ uint32_t ldg_x2(const __half* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
@@ -87,26 +110,14 @@ __device__ __forceinline__ uint32_t int8_pair(uint32_t u) {
   return h2_bits(__hsub2(bits_h2(t), bits_h2(0x64806480u)));  // 1152 = 1024 + 128
 }
 
-template <int BITS>
-struct WoTraits;
-template <>
-struct WoTraits<4> {
-  static constexpr int kVecs = 2;    // 16-byte weight vectors per thread per 16-k step
-  static constexpr int kDepth = 8;   // steps whose loads are in flight together
-};
-template <>
-struct WoTraits<8> {
-  static constexpr int kVecs = 4;
-  static constexpr int kDepth = 4;
-};
-
 // One 16-k step: dequantize the thread's weight vectors and issue the MMAs.
+// INT4: wv[0] = K-pair row c, wv[1] = row c + 4 of the step's 8 K-pair rows.
+// INT8: wv[0..3] = rows 2c, 2c + 1, 2c + 8, 2c + 9 of the step's 16 rows.
 template <int BITS, int MT>
-__device__ __forceinline__ void wo_step(float (&acc)[MT][8][4], const uint4 (&wv)[WoTraits<BITS>::kVecs],
-                                        const uint32_t (&xb)[MT][2]) {
+__device__ __forceinline__ void wo_step(float (&acc)[MT][8][4], const uint4* wv, const uint32_t (&xb)[MT][2]) {
   if constexpr (BITS == 4) {
-    const uint32_t wa[4] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w};  // K-pair row c
-    const uint32_t wb[4] = {wv[1].x, wv[1].y, wv[1].z, wv[1].w};  // K-pair row c + 4
+    const uint32_t wa[4] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w};
+    const uint32_t wb[4] = {wv[1].x, wv[1].y, wv[1].z, wv[1].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -119,10 +130,10 @@ __device__ __forceinline__ void wo_step(float (&acc)[MT][8][4], const uint4 (&wv
       }
     }
   } else {
-    const uint32_t w0[4] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w};  // row k0 + 2c
-    const uint32_t w1[4] = {wv[1].x, wv[1].y, wv[1].z, wv[1].w};  // row k0 + 2c + 1
-    const uint32_t w2[4] = {wv[2].x, wv[2].y, wv[2].z, wv[2].w};  // row k0 + 2c + 8
-    const uint32_t w3[4] = {wv[3].x, wv[3].y, wv[3].z, wv[3].w};  // row k0 + 2c + 9
+    const uint32_t w0[4] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w};
+    const uint32_t w1[4] = {wv[1].x, wv[1].y, wv[1].z, wv[1].w};
+    const uint32_t w2[4] = {wv[2].x, wv[2].y, wv[2].z, wv[2].w};
+    const uint32_t w3[4] = {wv[3].x, wv[3].y, wv[3].z, wv[3].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -139,174 +150,298 @@ __device__ __forceinline__ void wo_step(float (&acc)[MT][8][4], const uint4 (&wv
   }
 }
 
-// grid.x = n_tiles * C (cluster of C CTAs per 128-column tile), grid.y = M tiles
-// of 8 * MT rows.  Dynamic shared memory: partial tiles of every warp plus
-// the CTA's reduced tile.
-template <int BITS, int MT, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
-wo_skinny_kernel(WoArgs p) {
-  using T = WoTraits<BITS>;
-  constexpr int kRows = 8 * MT;
-  constexpr int kLd = kTileN + kRedPad;
-  extern __shared__ float smem[];
-  float* red = smem;                              // [WARPS][kRows][kLd]
-  float* part = smem + WARPS * kRows * kLd;       // [kRows][kTileN]
-
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = static_cast<int>(cluster.num_blocks());
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int tile = blockIdx.x / C;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int n_base = tile * kTileN;
-  const int m_base = blockIdx.y * kRows;
-
-  const int steps = (p.K + 15) / 16;
-  const int slices = C * WARPS;
-  const int slice = rank * WARPS + warp;
-  const int s_begin = static_cast<int>((static_cast<int64_t>(steps) * slice) / slices);
-  const int s_end = static_cast<int>((static_cast<int64_t>(steps) * (slice + 1)) / slices);
-
-  const uint8_t* W = static_cast<const uint8_t*>(p.W);
+// Activation fragments of the 4 steps of one chunk (rows 8mt + g of this M tile).
+template <int BITS, int MT>
+__device__ __forceinline__ void load_x_chunk(uint32_t (&xb)[4][MT][2], const WoArgs& p, int m_base, int k_chunk,
+                                             int g, int c) {
   const __half* X = static_cast<const __half*>(p.X);
-  const int col = n_base + 16 * g;
-  const int col_valid = min(16, max(0, p.N - col));
-  const int w_rows = BITS == 4 ? p.K / 2 : p.K;
-
-  float acc[MT][8][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
+  for (int j = 0; j < 4; ++j) {
+    const int ka = k_chunk + 16 * j + 2 * c, kb = ka + 8;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[mt][i][r] = 0.0f;
-
-  for (int s0 = s_begin; s0 < s_end; s0 += T::kDepth) {
-    uint4 wv[T::kDepth][T::kVecs];
-    uint32_t xb[T::kDepth][MT][2];
-#pragma unroll
-    for (int d = 0; d < T::kDepth; ++d) {
-      const int st = s0 + d;
-      const bool live = st < s_end;
-      const int k0 = st * 16;
-#pragma unroll
-      for (int v = 0; v < T::kVecs; ++v) {
-        int row;
-        if constexpr (BITS == 4) row = k0 / 2 + c + 4 * v;
-        else row = k0 + 2 * c + (v & 1) + 8 * (v >> 1);
-        const bool ok = live && row < w_rows && col_valid > 0;
-        wv[d][v] = ok ? ldg_vec16(W + static_cast<int64_t>(row) * p.ldw + col, col_valid) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int m = m_base + 8 * mt + g;
-        const bool mok = live && m < p.M;
-        const __half* xr = X + static_cast<int64_t>(m) * p.ldx;
-        const int ka = k0 + 2 * c, kb = k0 + 2 * c + 8;
-        const uint32_t pa = (mok && ka < p.K) ? ldg_x2(xr + ka) : 0u;
-        const uint32_t pb = (mok && kb < p.K) ? ldg_x2(xr + kb) : 0u;
-        if constexpr (BITS == 4) {
-          xb[d][mt][0] = __byte_perm(pa, pb, 0x5410);  // {x[k0+2c], x[k0+2c+8]}
-          xb[d][mt][1] = __byte_perm(pa, pb, 0x7632);  // {x[k0+2c+1], x[k0+2c+9]}
-        } else {
-          xb[d][mt][0] = pa;
-          xb[d][mt][1] = pb;
-        }
+    for (int mt = 0; mt < MT; ++mt) {
+      const int m = m_base + 8 * mt + g;
+      const bool mok = m < p.M;
+      const __half* xr = X + static_cast<int64_t>(m) * p.ldx;
+      const uint32_t pa = (mok && ka < p.K) ? ldg_x2(xr + ka) : 0u;
+      const uint32_t pb = (mok && kb < p.K) ? ldg_x2(xr + kb) : 0u;
+      if constexpr (BITS == 4) {
+        xb[j][mt][0] = __byte_perm(pa, pb, 0x5410);  // {x[k0+2c], x[k0+2c+8]}
+        xb[j][mt][1] = __byte_perm(pa, pb, 0x7632);  // {x[k0+2c+1], x[k0+2c+9]}
+      } else {
+        xb[j][mt][0] = pa;
+        xb[j][mt][1] = pb;
       }
     }
-#pragma unroll
-    for (int d = 0; d < T::kDepth; ++d) wo_step<BITS, MT>(acc, wv[d], xb[d]);
   }
-
-  // Per-warp partial tiles -> shared memory.  acc[mt][i] covers MMA rows
-  // (weight columns) 16g + 2i and 16g + 2i + 1, MMA columns (rows of X)
-  // 8mt + 2c and 8mt + 2c + 1.
-  float* rw = red + warp * kRows * kLd;
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int n = 16 * g + 2 * i;
-      const int m = 8 * mt + 2 * c;
-      *reinterpret_cast<float2*>(rw + m * kLd + n) = make_float2(acc[mt][i][0], acc[mt][i][2]);
-      *reinterpret_cast<float2*>(rw + (m + 1) * kLd + n) = make_float2(acc[mt][i][1], acc[mt][i][3]);
-    }
-  __syncthreads();
-  for (int o = threadIdx.x; o < kRows * kTileN; o += WARPS * 32) {
-    const int m = o / kTileN, n = o % kTileN;
-    float sum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) sum += red[(w * kRows + m) * kLd + n];
-    part[o] = sum;
-  }
-  // Cluster-wide reduction: CTA `rank` finishes columns [lo, hi) of the tile
-  // from every CTA's reduced tile (distributed shared memory).
-  cluster.sync();
-  const int span = kTileN / C;
-  const int lo = rank * span, hi = (rank == C - 1) ? kTileN : lo + span;
-  const __half* S = static_cast<const __half*>(p.scales);
-  __half* Y = static_cast<__half*>(p.Y);
-  for (int o = threadIdx.x; o < kRows * (hi - lo); o += WARPS * 32) {
-    const int m = o / (hi - lo), n = lo + o % (hi - lo);
-    float sum = 0.0f;
-    for (int q = 0; q < C; ++q) sum += cluster.map_shared_rank(part, q)[m * kTileN + n];
-    const int gm = m_base + m, gn = n_base + n;
-    if (gm < p.M && gn < p.N)
-      Y[static_cast<int64_t>(gm) * p.ldy + gn] = __float2half_rn(__half2float(S[gn]) * sum);
-  }
-  cluster.sync();  // keep every CTA's shared memory alive until all reads are done
 }
 
-template <int BITS, int MT, int WARPS>
-cudaError_t launch_variant(const WoArgs& a, int C, cudaStream_t s) {
+// Barrier over the consumer warps only (the producer keeps streaming).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+}
+
+template <int BITS, int MT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, WoArgs p, Plan pl, int* err) {
+  using R = Ring<BITS>;
   constexpr int kRows = 8 * MT;
-  const size_t smem = sizeof(float) * (WARPS * kRows * (kTileN + kRedPad) + kRows * kTileN);
-  auto kern = wo_skinny_kernel<BITS, MT, WARPS>;
-  static bool configured = false;  // per instantiation; a benign race sets it twice
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
+  constexpr int kOut = kRows * kTileN;  // outputs per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128 - (tc::smem_u32(smem_raw) & 127)) & 127);
+  uint8_t* ring = smem;
+  float* part = reinterpret_cast<float*>(smem + kRingBytes);  // [kRows][kTileN]
+  uint64_t* full = reinterpret_cast<uint64_t*>(part + kOut);
+  uint64_t* empty = full + R::kStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(empty + R::kStages);
+  volatile int* last_flag = abort + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int b = blockIdx.x, G = gridDim.x;
+  const int64_t U = pl.units;
+  const int ch = pl.chunks;
+  const int64_t lo = unit_lo(b, U, G);
+  const int n_local = static_cast<int>(unit_lo(b + 1, U, G) - lo);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < R::kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    *abort = 0;
+    tc::fence_mbar_init();
   }
-  const int n_tiles = (a.N + kTileN - 1) / kTileN;
-  const int m_tiles = (a.M + kRows - 1) / kRows;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * C), static_cast<unsigned>(m_tiles), 1);
-  cfg.blockDim = dim3(WARPS * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  __syncthreads();
+
+  if (warp == kConsumers) {
+    // Producer: one elected thread keeps the ring full across the CTA's run.
+    if (lane == 0 && n_local > 0) {
+      tc::tma_prefetch_desc(&tmW);
+      int issued = 0;
+      for (int i = 0; i < n_local; ++i) {
+        const int64_t u = lo + i;
+        const int T = static_cast<int>(u / ch), chunk = static_cast<int>(u % ch);
+        const int s = i % R::kStages;
+        if (!tc::mbar_wait(&empty[s], ((i / R::kStages) & 1) ^ 1, abort, err, kSiteGemmProducer)) break;
+        tc::mbar_arrive_expect_tx(&full[s], R::kStageBytes);
+        tc::tma_load_2d(ring + s * R::kStageBytes, &tmW, (T % pl.n_tiles) * kTileN, chunk * R::kRows, &full[s]);
+        issued = i + 1;
+      }
+      if (*abort)
+        for (int i = issued > R::kStages ? issued - R::kStages : 0; i < issued; ++i)
+          tc::mbar_wait_drain(&full[i % R::kStages], (i / R::kStages) & 1);
+    }
+    return;
+  }
+
+  // Consumers: one segment per tile the run touches.
+  int* ws_count = static_cast<int*>(p.ws);
+  float* ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(p.ws) + kCounterBytes);
+  const __half* S = static_cast<const __half*>(p.scales);
+  __half* Y = static_cast<__half*>(p.Y);
+  uint32_t xb[4][MT][2];
+  for (int i = 0; i < n_local;) {
+    const int64_t u0 = lo + i;
+    const int T = static_cast<int>(u0 / ch);
+    const int64_t seg_end = static_cast<int64_t>(T + 1) * ch < lo + n_local ? static_cast<int64_t>(T + 1) * ch
+                                                                             : lo + n_local;
+    const int seg = static_cast<int>(seg_end - u0);
+    const int m_base = (T / pl.n_tiles) * kRows, n_base = (T % pl.n_tiles) * kTileN;
+    const int chunk0 = static_cast<int>(u0 - static_cast<int64_t>(T) * ch);
+
+    float acc[MT][8][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[mt][q][r] = 0.0f;
+
+    for (int j = warp; j < seg; j += kConsumers) {
+      const int li = i + j;
+      const int s = li % R::kStages;
+      load_x_chunk<BITS, MT>(xb, p, m_base, (chunk0 + j) * kChunkK, g, c);
+      const bool ok = tc::mbar_wait(&full[s], (li / R::kStages) & 1, abort, err, kSiteGemmMma);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint8_t* st = ring + s * R::kStageBytes + 16 * g;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 wv[BITS == 4 ? 2 : 4];
+        if constexpr (BITS == 4) {
+          wv[0] = *reinterpret_cast<const uint4*>(st + (8 * q + c) * kTileN);
+          wv[1] = *reinterpret_cast<const uint4*>(st + (8 * q + c + 4) * kTileN);
+        } else {
+          wv[0] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c) * kTileN);
+          wv[1] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c + 1) * kTileN);
+          wv[2] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c + 8) * kTileN);
+          wv[3] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c + 9) * kTileN);
+        }
+        wo_step<BITS, MT>(acc, wv, xb[q]);
+      }
+      // The slot's next contents arrive through TMA (async proxy): order this
+      // thread's generic-proxy reads of the slot before releasing it.
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[s]);
+    }
+
+    // Sum the consumer warps' partial tiles in a fixed order.  acc[mt][q]
+    // covers MMA rows (weight columns) 16g + 2q and 16g + 2q + 1, MMA columns
+    // (rows of X) 8mt + 2c and 8mt + 2c + 1.
+    for (int r = 0; r < kConsumers; ++r) {
+      if (warp == r) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int n = 16 * g + 2 * q, m = 8 * mt + 2 * c;
+            float2* p0 = reinterpret_cast<float2*>(part + m * kTileN + n);
+            float2* p1 = reinterpret_cast<float2*>(part + (m + 1) * kTileN + n);
+            float2 v0 = make_float2(acc[mt][q][0], acc[mt][q][2]);
+            float2 v1 = make_float2(acc[mt][q][1], acc[mt][q][3]);
+            if (r > 0) {
+              const float2 o0 = *p0, o1 = *p1;
+              v0.x += o0.x; v0.y += o0.y; v1.x += o1.x; v1.y += o1.y;
+            }
+            *p0 = v0;
+            *p1 = v1;
+          }
+      }
+      consumer_sync();
+    }
+
+    // Finish the tile, or hand this CTA's share to the last contributor.
+    const int f0 = unit_owner(static_cast<int64_t>(T) * ch, U, G);
+    const int f1 = unit_owner(static_cast<int64_t>(T + 1) * ch - 1, U, G);
+    const int contributors = f1 - f0 + 1;
+    const int t = threadIdx.x;  // 0 .. 127 across the consumer warps
+    bool finish = true;
+    const float* src = part;
+    if (contributors > 1) {
+      float* mine = ws_part + (static_cast<size_t>(T) * pl.slots + (b - f0)) * kOut;
+      for (int o = 4 * t; o < kOut; o += 4 * kConsumers * 32)
+        __stcg(reinterpret_cast<float4*>(mine + o), *reinterpret_cast<const float4*>(part + o));
+      __threadfence();
+      consumer_sync();
+      if (t == 0) *last_flag = (atomicAdd(&ws_count[T], 1) == contributors - 1);
+      consumer_sync();
+      finish = *last_flag != 0;
+      if (finish) __threadfence();
+      src = ws_part + static_cast<size_t>(T) * pl.slots * kOut;
+    }
+    if (finish) {
+      for (int o = 4 * t; o < kOut; o += 4 * kConsumers * 32) {
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (contributors > 1) {
+          for (int q = 0; q < contributors; ++q) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(q) * kOut + o));
+            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+          }
+        } else {
+          sum = *reinterpret_cast<const float4*>(src + o);
+        }
+        const int m = o / kTileN, n = o % kTileN;
+        const int gm = m_base + m;
+        const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+        if (gm < p.M)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int gn = n_base + n + e;
+            if (gn < p.N) Y[static_cast<int64_t>(gm) * p.ldy + gn] = __float2half_rn(__half2float(S[gn]) * v[e]);
+          }
+      }
+      if (contributors > 1 && t == 0) ws_count[T] = 0;  // ready for the next call
+    }
+    consumer_sync();  // `part` is rewritten by the next segment
+    i += seg;
+  }
+}
+
+// Opt the kernel into its dynamic shared memory (above the 48 KB default);
+// must precede both the occupancy query and the first launch.
+template <int BITS, int MT>
+cudaError_t configure_kernel() {
+  static cudaError_t status = cudaFuncSetAttribute(wo_skinny_kernel<BITS, MT>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(skinny_smem_bytes<MT>()));
+  return status;
+}
+
+template <int BITS, int MT>
+int ctas_per_sm() {
+  static int cached = 0;
+  if (cached == 0) {
+    int n = 0;
+    if (configure_kernel<BITS, MT>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wo_skinny_kernel<BITS, MT>, kThreads,
+                                                      skinny_smem_bytes<MT>()) != cudaSuccess || n < 1)
+      return 1;  // not cached: a later call may succeed
+    cached = n;
+  }
+  return cached;
+}
+
+template <int BITS, int MT>
+Plan make_plan(int M, int N, int K) {
+  Plan pl;
+  pl.n_tiles = (N + kTileN - 1) / kTileN;
+  pl.tiles = pl.n_tiles * ((M + 8 * MT - 1) / (8 * MT));
+  pl.chunks = (K + kChunkK - 1) / kChunkK;
+  pl.units = static_cast<int64_t>(pl.tiles) * pl.chunks;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * ctas_per_sm<BITS, MT>();
+  pl.grid = static_cast<int>(pl.units < cap ? pl.units : cap);
+  pl.slots = 1;
+  if (pl.tiles > kMaxSplitTiles) {  // too many tiles for the counter area: one CTA per tile, no split
+    pl.grid = pl.tiles;
+    return pl;
+  }
+  for (int T = 0; T < pl.tiles; ++T) {
+    const int n = unit_owner(static_cast<int64_t>(T + 1) * pl.chunks - 1, pl.units, pl.grid) -
+                  unit_owner(static_cast<int64_t>(T) * pl.chunks, pl.units, pl.grid) + 1;
+    if (n > pl.slots) pl.slots = n;
+  }
+  return pl;
+}
+
+template <int BITS, int MT>
+size_t plan_workspace(int M, int N, int K) {
+  const Plan pl = make_plan<BITS, MT>(M, N, K);
+  if (pl.slots == 1) return 0;
+  return kCounterBytes + static_cast<size_t>(pl.tiles) * pl.slots * (8 * MT) * kTileN * sizeof(float);
+}
+
+template <int BITS, int MT>
+cudaError_t launch_variant(const WoArgs& a, cudaStream_t s) {
+  using R = Ring<BITS>;
+  const size_t smem = skinny_smem_bytes<MT>();
+  auto kern = wo_skinny_kernel<BITS, MT>;
+  cudaError_t e = configure_kernel<BITS, MT>();
+  if (e != cudaSuccess) return e;
+  const Plan pl = make_plan<BITS, MT>(a.M, a.N, a.K);
+  CUtensorMap tW;
+  const uint64_t rows = BITS == 4 ? a.K / 2 : a.K;
+  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, rows, a.ldw, kTileN, R::kRows,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  kern<<<pl.grid, kThreads, smem, s>>>(tW, a, pl, device_error_word());
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-int wo_skinny_max_m() { return 16; }
-
-// Split-K heuristic: one warp per (128 columns, K slice); enough warps to keep
-// about 16 per SM busy, at least two 16-k steps per warp, clusters of 1..8.
-int wo_skinny_cluster(int N, int K, int warps) {
-  const int n_tiles = (N + kTileN - 1) / kTileN;
-  const int steps = (K + 15) / 16;
-  const int target_warps = sm_count() * 16;
-  int C = target_warps / (n_tiles * warps);
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
-  while (C > 1 && steps < 2 * C * warps) --C;
-  return C;
+size_t wo_skinny_workspace(int M, int N, int K, int bits) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const bool two = M > 8;
+  if (bits == 4) return two ? plan_workspace<4, 2>(M, N, K) : plan_workspace<4, 1>(M, N, K);
+  return two ? plan_workspace<8, 2>(M, N, K) : plan_workspace<8, 1>(M, N, K);
 }
 
 cudaError_t launch_wo_skinny(const WoArgs& a, int bits, cudaStream_t s) {
-  constexpr int kWarps = 8;
-  const int C = wo_skinny_cluster(a.N, a.K, kWarps);
+  if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
   const bool two = a.M > 8;
-  if (bits == 4) return two ? launch_variant<4, 2, kWarps>(a, C, s) : launch_variant<4, 1, kWarps>(a, C, s);
-  return two ? launch_variant<8, 2, kWarps>(a, C, s) : launch_variant<8, 1, kWarps>(a, C, s);
+  if (bits == 4) return two ? launch_variant<4, 2>(a, s) : launch_variant<4, 1>(a, s);
+  return two ? launch_variant<8, 2>(a, s) : launch_variant<8, 1>(a, s);
 }
 
 }  // namespace wq

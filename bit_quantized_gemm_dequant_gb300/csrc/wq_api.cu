@@ -63,11 +63,21 @@ static int check_weight_only(int M, int N, int K, const void* X, int64_t ldx, co
   return WQ_OK;
 }
 
+// M up to this bound runs the split-K skinny path (HBM-bound); larger M the
+// tiled tensor-memory GEMM.
+constexpr int kSkinnyMaxM = 64;
+
+static size_t weight_only_workspace(int bits, int M, int N, int K) {
+  return (M > 0 && M <= kSkinnyMaxM) ? wo_skinny_workspace(M, N, K, bits) : 0;
+}
+
 static int run_weight_only(int bits, int M, int N, int K, const void* X, int64_t ldx, const void* W, int64_t ldw,
-                           const void* scales, void* Y, int64_t ldy, cudaStream_t s) {
+                           const void* scales, void* Y, int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (M == 0 || N == 0) return WQ_OK;
-  WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy};
-  if (M <= wo_skinny_max_m()) return launch_status(launch_wo_skinny(a, bits, s));
+  const size_t need = weight_only_workspace(bits, M, N, K);
+  if (ws_bytes < need || (need > 0 && (!ws || !aligned(ws, 16)))) return WQ_ERR_WORKSPACE;
+  WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy, ws, ws_bytes};
+  if (M <= kSkinnyMaxM) return launch_status(launch_wo_skinny(a, bits, s));
   return launch_status(launch_wo_gemm(a, bits, s));
 }
 
@@ -80,24 +90,22 @@ extern "C" {
 int wq_gemm_w4a16(int M, int N, int K, const void* X, int64_t ldx, const uint8_t* Wq, int64_t ldw,
                   const void* scales, void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
                   wq_stream_t stream) {
-  (void)workspace;
   int st = check_weight_only(M, N, K, X, ldx, Wq, ldw, scales, Y, ldy);
   if (st != WQ_OK || M == 0 || N == 0) return st;
   if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
-  if (ws_bytes < wq_workspace_size(WQ_OP_W4A16, M, N, K)) return WQ_ERR_WORKSPACE;
-  return run_weight_only(4, M, N, K, X, ldx, Wq, ldw, scales, Y, ldy, reinterpret_cast<cudaStream_t>(stream));
+  return run_weight_only(4, M, N, K, X, ldx, Wq, ldw, scales, Y, ldy, workspace, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
                   const void* scales, void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
                   wq_stream_t stream) {
-  (void)workspace;
   if (K % 2 && K > 0 && M >= 0 && N >= 0) return WQ_ERR_UNSUPPORTED;
   int st = check_weight_only(M, N, K, X, ldx, W, ldw, scales, Y, ldy);
   if (st != WQ_OK || M == 0 || N == 0) return st;
   if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
-  if (ws_bytes < wq_workspace_size(WQ_OP_W8A16, M, N, K)) return WQ_ERR_WORKSPACE;
-  return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, reinterpret_cast<cudaStream_t>(stream));
+  return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, workspace, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_t* data, int64_t ld_data,
@@ -141,7 +149,9 @@ int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* 
 }
 
 size_t wq_workspace_size(int op, int M, int N, int K) {
-  (void)op; (void)M; (void)N; (void)K;
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (op == WQ_OP_W4A16 && K % 2 == 0) return weight_only_workspace(4, M, N, K);
+  if (op == WQ_OP_W8A16 && K % 2 == 0) return weight_only_workspace(8, M, N, K);
   return 0;
 }
 

@@ -28,6 +28,7 @@ struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
   const void* W; int64_t ldw;
   const void* scales;
   void* Y; int64_t ldy;
+  void* ws; size_t ws_bytes;  // caller scratch (split-K partial sums and tile counters)
 };
 
 struct MxQuantArgs {
@@ -62,9 +63,9 @@ cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_gemm(const Fp8GemmArgs& a, cudaStream_t s);
 
-// Shape dispatch: the largest M the skinny (split-K, register-dequant) path
-// takes; larger M goes to the tiled tensor-memory GEMM.
-int wo_skinny_max_m();
+// Scratch bytes the skinny path needs for this shape (0 when every tile is
+// finished by a single CTA).
+size_t wo_skinny_workspace(int M, int N, int K, int bits);
 
 int sm_count();
 

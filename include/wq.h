@@ -73,9 +73,17 @@ typedef struct CUstream_st* wq_stream_t;
  *   Wq       uint8 [K/2, N], row stride ldw (bytes, ldw >= N).
  *   scales   fp16 [N], one per output column.
  *   Y        fp16 [M, N] output, row stride ldy (elements, ldy >= N).
- *   workspace, ws_bytes  scratch of at least wq_workspace_size(WQ_OP_W4A16,
- *            M, N, K) bytes (0 for every shape served today: the split-K
- *            partial sums are reduced inside thread-block clusters).
+ *   workspace, ws_bytes  device scratch of at least
+ *            wq_workspace_size(WQ_OP_W4A16, M, N, K) bytes, 16-byte aligned
+ *            (may be NULL when that size is 0).  For M <= 64 the K dimension
+ *            is split across CTAs: the first 64 KiB hold one counter per
+ *            tile, the partial sums of split tiles follow.  Zero-fill the
+ *            workspace once before its first use; every call that returns
+ *            WQ_OK leaves the counter area zero again (the rest is scratch),
+ *            so one buffer serves any sequence of calls and shapes on one
+ *            stream.  Two calls in flight at the same time must not share a
+ *            workspace.  After WQ_ERR_DEVICE zero it again before reuse.  Too
+ *            small: WQ_ERR_WORKSPACE.
  * Alignment: X, Wq, Y 16-byte aligned; ldx and ldy multiples of 8; ldw a
  * multiple of 16; scales 2-byte aligned.  Otherwise WQ_ERR_MISALIGNED.
  */
@@ -96,7 +104,8 @@ int wq_gemm_w4a16(int M, int N, int K, const void* X, int64_t ldx,
  *   W        int8 [K, N], row stride ldw (bytes).
  *   scales   fp16 [N].
  *   Y        fp16 [M, N], row stride ldy (elements).
- *   workspace, ws_bytes  as for wq_gemm_w4a16.
+ *   workspace, ws_bytes  as for wq_gemm_w4a16, sized by
+ *            wq_workspace_size(WQ_OP_W8A16, M, N, K).
  * Alignment: as for wq_gemm_w4a16.  Odd K returns WQ_ERR_UNSUPPORTED.
  */
 int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx,
@@ -171,7 +180,8 @@ int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda,
              void* C, int64_t ldc, void* workspace, size_t ws_bytes,
              wq_stream_t stream);
 
-/* Scratch bytes an operation needs for this shape (0 when none). */
+/* Scratch bytes an operation needs for this shape on the current device (0
+ * when none).  The size depends on the device's SM count. */
 size_t wq_workspace_size(int op, int M, int N, int K);
 
 /* Static, human-readable name of a status code (never NULL). */

@@ -143,3 +143,31 @@ def test_w8a16_large_m_sampled(wq, M, K, N):
     rows = np.random.default_rng(N).choice(M, 32, replace=False)
     rows[:2] = [0, M - 1]
     assert_gemm_close(y[torch.from_numpy(rows).cuda()], _ref(8, case, rows), "fp16")
+
+
+@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 14336), (4, 1, 11008, 4096), (4, 64, 4096, 11008)])
+def test_split_k_workspace_contract(wq, bits, M, K, N):
+    """Split tiles need scratch; a call leaves the counter area (the first
+    64 KiB) zero again, repeated calls are bit-identical (fixed reduction
+    order), and a short buffer is refused before any launch."""
+    op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
+    need = wq.wq_workspace_size(op, M, N, K)
+    assert need > 0
+    case = _case(bits, M, K, N, seed=5)
+    x = torch.from_numpy(case.x).cuda()
+    w = torch.from_numpy(case.w).cuda()
+    s = torch.from_numpy(case.scales).cuda()
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+    y1 = fn(x, w, s, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[: 64 * 1024].count_nonzero()) == 0
+    y2 = fn(x, w, s, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert_gemm_close(y1, _ref(bits, case), "fp16")
+    with pytest.raises(wq.WqError) as ei:
+        fn(x, w, s, workspace=ws[: need - 16])
+    assert ei.value.status == wq.WQ_ERR_WORKSPACE
+    st, site = wq.wq_get_device_error()
+    assert st == wq.WQ_OK and site == 0
