@@ -39,6 +39,7 @@ _i, _i64, _p, _sz, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_
 _SIGS = {
     "wq_gemm_w4a16": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
     "wq_gemm_w8a16": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
+    "wq_gemm_w8a16_noalloc": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p],
     "mx_quantize_fp4": [_i, _i, _p, _i64, _p, _i64, _p, _i64, _p],
     "mx_gemm_fp4": [_i, _i, _i, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _sz, _p],
     "fp8_gemm": [_i, _i, _i, _p, _i64, _p, _i64, _f, _f, _p, _i64, _p, _sz, _p],
@@ -145,6 +146,20 @@ def wq_gemm_w8a16(x, w, scales, y=None, workspace=None, stream=None):
     wsp, wsb = _ws(workspace)
     _check(lib.wq_gemm_w8a16(M, N, K, _ptr(x), _ld(x), _ptr(w), _ld(w), _ptr(scales), _ptr(y), _ld(y),
                              wsp, wsb, _stream(stream)), "wq_gemm_w8a16")
+    return y
+
+
+def wq_gemm_w8a16_noalloc(x, w, scales, y=None, stream=None):
+    """wq_gemm_w8a16 with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory at call time)."""
+    import torch
+
+    M, K = x.shape
+    N = w.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib.wq_gemm_w8a16_noalloc(M, N, K, _ptr(x), _ld(x), _ptr(w), _ld(w), _ptr(scales), _ptr(y), _ld(y),
+                                     _stream(stream)), "wq_gemm_w8a16_noalloc")
     return y
 
 

@@ -34,6 +34,8 @@
 //     fixed order, so the result is deterministic, and resets the counter.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "tc_common.cuh"
 #include "tma_host.h"
 #include "wq_internal.h"
@@ -443,5 +445,42 @@ cudaError_t launch_wo_skinny(const WoArgs& a, int bits, cudaStream_t s) {
   if (bits == 4) return two ? launch_variant<4, 2>(a, s) : launch_variant<4, 1>(a, s);
   return two ? launch_variant<8, 2>(a, s) : launch_variant<8, 1>(a, s);
 }
+
+}  // namespace wq
+
+// --------------------------------------------------------------------------
+// Built-in scratch for callers that cannot allocate device memory.
+//
+// Some callers may not allocate at call time: an engine plugin whose enqueue
+// step must not allocate, a real-time loop that forbids cudaMalloc/cudaFree
+// once it runs, or a runtime that plans every device byte ahead.  For them the
+// INT8 skinny path can keep its split-K scratch (tile counters and partial
+// sums) in this fixed array instead of a caller workspace.  Every GPU that
+// loads the library holds the array until the process exits.
+namespace wq {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t noalloc_scratch(void** ptr) {
+  // The array's host-side name is not a device address: look the address up
+  // once per device, with that device current.
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
+
+size_t skinny_counter_bytes() { return kCounterBytes; }
 
 }  // namespace wq

@@ -108,6 +108,24 @@ int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t*
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int wq_gemm_w8a16_noalloc(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                          const void* scales, void* Y, int64_t ldy, wq_stream_t stream) {
+  if (K % 2 && K > 0 && M >= 0 && N >= 0) return WQ_ERR_UNSUPPORTED;
+  int st = check_weight_only(M, N, K, X, ldx, W, ldw, scales, Y, ldy);
+  if (st != WQ_OK || M == 0 || N == 0) return st;
+  if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
+  const size_t need = weight_only_workspace(8, M, N, K);
+  if (need > kNoAllocScratchBytes) return WQ_ERR_WORKSPACE;  // beyond the built-in scratch
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if (need > 0) {
+    if (noalloc_scratch(&scratch) != cudaSuccess) return launch_status(cudaErrorInvalidValue);
+    // The array keeps the previous call's bytes: the tile counters must start at zero.
+    if (cudaMemsetAsync(scratch, 0, skinny_counter_bytes(), s) != cudaSuccess) return launch_status(cudaErrorInvalidValue);
+  }
+  return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, scratch, need > 0 ? kNoAllocScratchBytes : 0, s);
+}
+
 int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_t* data, int64_t ld_data,
                     uint8_t* scales, int64_t ld_scales, wq_stream_t stream) {
   if (rows < 0 || cols < 0 || cols % 32) return WQ_ERR_INVALID_ARG;

@@ -69,4 +69,9 @@ size_t wo_skinny_workspace(int M, int N, int K, int bits);
 
 int sm_count();
 
+// Built-in scratch of the allocation-free INT8 entry point (wo_skinny.cu).
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+cudaError_t noalloc_scratch(void** ptr);  // device address on the current device
+size_t skinny_counter_bytes();            // leading counter area that must start at zero
+
 }  // namespace wq

@@ -114,6 +114,32 @@ int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx,
                   wq_stream_t stream);
 
 /*
+ * wq_gemm_w8a16_noalloc — wq_gemm_w8a16 without a caller workspace.
+ *
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot allocate device memory when they call (an engine plugin whose
+ * enqueue step may not allocate, a real-time loop that forbids cudaMalloc and
+ * cudaFree after start-up, a runtime that plans every device byte ahead).
+ * It computes exactly what wq_gemm_w8a16 computes, with the same arguments
+ * minus the workspace, and allocates nothing: the split-K scratch of the
+ * small-M path lives in a fixed 8 MiB array of device memory inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.
+ *
+ *   - Shapes whose scratch need (wq_workspace_size(WQ_OP_W8A16, M, N, K))
+ *     exceeds 8 MiB return WQ_ERR_WORKSPACE without launching.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before capturing the stream into a CUDA graph.
+ *   - Each call clears the array's counter area on `stream` before its
+ *     kernel.  All calls share the one array, so calls that overlap on the
+ *     GPU (different streams, or the same stream from different threads
+ *     without ordering) race and give wrong results.
+ */
+int wq_gemm_w8a16_noalloc(int M, int N, int K, const void* X, int64_t ldx,
+                          const int8_t* W, int64_t ldw, const void* scales,
+                          void* Y, int64_t ldy, wq_stream_t stream);
+
+/*
  * mx_quantize_fp4 — quantize FP32 rows to MXFP4 (E2M1 elements, E8M0 scales).
  *
  * [MXFP4] §三 simulator, per 32-element block of each row:
