@@ -198,6 +198,8 @@ def fp8_gemm(a, b, scale_a, scale_b, c=None, workspace=None, stream=None):
     N = b.shape[1]
     if c is None:
         c = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if workspace is None:
+        workspace = auto_workspace(WQ_OP_FP8_GEMM, M, N, K, a.device)
     wsp, wsb = _ws(workspace)
     _check(lib.fp8_gemm(M, N, K, _ptr(a), _ld(a), _ptr(b), _ld(b), float(scale_a), float(scale_b), _ptr(c), _ld(c),
                         wsp, wsb, _stream(stream)), "fp8_gemm")

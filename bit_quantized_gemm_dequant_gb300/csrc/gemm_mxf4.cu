@@ -44,7 +44,7 @@ constexpr int BKB = 128;                    // K bytes per stage (256 E2M1 eleme
 constexpr int kBlocksPerStage = BKB * 2 / 32;  // 8 scale blocks
 constexpr int kStages = 4;
 constexpr int kABytes = BM * BKB;           // 16 KB
-constexpr int kBBytes = BN * BKB;           // 16 KB
+constexpr int kBBytes = BN * BKB;           // 32 KB
 constexpr int kSfChunk = 512;               // 128 rows x 4 blocks
 constexpr int kSfRowBytes = 16;             // scale bytes per row and TMA box (two stages)
 constexpr int kSfBytes = (BM + BN) * kSfRowBytes;  // 6 KB: raw boxes, rewritten into 6 chunks in place

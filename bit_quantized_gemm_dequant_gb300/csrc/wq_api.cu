@@ -154,22 +154,25 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_
 
 int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb, float scale_a,
              float scale_b, void* C, int64_t ldc, void* workspace, size_t ws_bytes, wq_stream_t stream) {
-  (void)workspace;
   if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return WQ_OK;
   if (!C || (K > 0 && (!A || !B))) return WQ_ERR_INVALID_ARG;
   if (ldc < N || (K > 0 && (lda < K || ldb < N))) return WQ_ERR_INVALID_ARG;
   if (!aligned(C, 16) || ldc % 8) return WQ_ERR_MISALIGNED;
   if (K > 0 && (!aligned(A, 16) || !aligned(B, 16) || lda % 16 || ldb % 16)) return WQ_ERR_MISALIGNED;
-  if (ws_bytes < wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
-  Fp8GemmArgs a{M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc};
-  return launch_status(launch_fp8_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+  const size_t need = wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K);
+  if (ws_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 16)))) return WQ_ERR_WORKSPACE;
+  Fp8GemmArgs a{M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, workspace, ws_bytes};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M <= kFp8SkinnyMaxM) return launch_status(launch_fp8_skinny(a, workspace, s));
+  return launch_status(launch_fp8_gemm(a, s));
 }
 
 size_t wq_workspace_size(int op, int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == WQ_OP_W4A16 && K % 2 == 0) return weight_only_workspace(4, M, N, K);
   if (op == WQ_OP_W8A16 && K % 2 == 0) return weight_only_workspace(8, M, N, K);
+  if (op == WQ_OP_FP8_GEMM && M <= kFp8SkinnyMaxM) return fp8_skinny_workspace(M, N, K);
   return 0;
 }
 

@@ -53,6 +53,7 @@ struct Fp8GemmArgs {
   const uint8_t* B; int64_t ldb;
   float scale_a, scale_b;
   void* C; int64_t ldc;
+  void* ws; size_t ws_bytes;  // caller scratch of the small-M path
 };
 
 // Launchers (one per kernel family).  Each returns a cudaError_t from the
@@ -66,6 +67,12 @@ cudaError_t launch_fp8_gemm(const Fp8GemmArgs& a, cudaStream_t s);
 // Scratch bytes the skinny path needs for this shape (0 when every tile is
 // finished by a single CTA).
 size_t wo_skinny_workspace(int M, int N, int K, int bits);
+
+// Small-M FP8 (M <= kFp8SkinnyMaxM) runs on the skinny path as an e4m3
+// weight stream; its scratch bytes for this shape.
+constexpr int kFp8SkinnyMaxM = 16;
+size_t fp8_skinny_workspace(int M, int N, int K);
+cudaError_t launch_fp8_skinny(const Fp8GemmArgs& a, void* ws, cudaStream_t s);
 
 int sm_count();
 

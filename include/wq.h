@@ -192,12 +192,15 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
  * the per-tensor scales applied once to the accumulator, BF16 output
  * (round to nearest even).
  *
- *   M, N, K  problem size; K must be a multiple of 16.
+ *   M, N, K  problem size (any K).
  *   A        e4m3fn bytes [M, K], row stride lda (bytes).
  *   B        e4m3fn bytes [K, N], row stride ldb (bytes).
  *   scale_a, scale_b  per-tensor FP32 scales, passed by value.
  *   C        bf16 [M, N] output, row stride ldc (elements).
- *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K).
+ *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K)
+ *            bytes: for M <= 16 the K dimension is split across CTAs and the
+ *            contract of wq_gemm_w4a16's workspace applies (zero-fill once;
+ *            calls leave the counter area zero); 0 bytes otherwise.
  * Alignment: A, B, C 16-byte aligned; lda, ldb multiples of 16; ldc a
  * multiple of 8.
  */

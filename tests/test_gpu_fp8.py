@@ -37,7 +37,11 @@ def _run(wq, case, lda=None, ldb=None, ldc=None):
     (200, 96, 300, None, 304, 304),      # ragged M, N, K (K below one 128-byte step)
     (257, 640, 520, 656, 528, 528),      # padded leading dimensions
     (384, 1000, 1024, 1008, None, None),
-    (16, 8192, 8192, None, None, None),  # the M = 16 FP8 workload
+    (16, 8192, 8192, None, None, None),  # the M = 16 FP8 workload (skinny e4m3 path)
+    (3, 99, 300, 112, 304, 304),         # K not a multiple of 4: zero-masked tail bytes of A
+    (12, 1000, 520, 1008, 528, 528),     # second MMA column block, ragged N
+    (9, 4096, 14336, None, None, None),
+    (17, 512, 384, None, None, None),    # just above the skinny bound
 ])
 def test_fp8_cases(wq, M, K, N, lda, ldb, ldc):
     case = workloads.fp8_case(M, K, N, seed=M + K + N)
