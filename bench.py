@@ -12,7 +12,12 @@ more than the 129 MB L2, so no call starts with its weights in L2.
 
 Before the timed region the stream is held by a device-side spin long enough
 for the host to enqueue every timed launch, so CUDA events measure device time
-and not Python / launch latency.  Rank 0 prints one JSON line.
+and not Python / launch latency.  The K steps run back to back between two
+events, with nothing recorded between calls, so consecutive kernels overlap as
+they do in a real call sequence (the skinny kernels are launched as
+programmatic dependents).  Per-call kernel times, and the roofline of the
+dominant kernel, come from a second pass in which each call sits between its
+own pair of events.  Rank 0 prints one JSON line.
 
 `breakdown` carries the other workloads (INT4 Llama-7B linears, MXFP4 quantize
 + GEMM, FP8 GEMM), each call timed after an L2 flush, with its own roofline.
@@ -218,7 +223,9 @@ def _summary(c, ms):
 
 
 def time_steps(torch, wl, steps, warmup, replicas, ws):
-    """K steps over wl.calls, per-call CUDA events on the launching stream."""
+    """K steps over wl.calls, back to back on one stream, between two CUDA
+    events (nothing recorded between the calls, so consecutive kernels may
+    overlap the way they do in a real sequence of calls)."""
     stream = torch.cuda.current_stream()
     t_host = time.perf_counter()
     for s in range(warmup):
@@ -228,25 +235,42 @@ def time_steps(torch, wl, steps, warmup, replicas, ws):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wl.calls]
-          for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     _hold_stream(torch, 2.0 * host_per_step * steps + 2e-3)
     t0.record(stream)
     for s in range(steps):
-        for j, c in enumerate(wl.calls):
-            ev[s][j][0].record(stream)
+        for c in wl.calls:
             wl.run(s % replicas, c["index"])
-            ev[s][j][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    total_ms = _barrier_max(torch, t0.elapsed_time(t1), ws)
-    per_call = [_summary(c, statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(steps)))
-                for j, c in enumerate(wl.calls)]
-    return total_ms, per_call
+    return _barrier_max(torch, t0.elapsed_time(t1), ws)
+
+
+def time_each_call(torch, wl, steps, replicas):
+    """Per-call device time: the same K steps again, each call between its own
+    pair of CUDA events on the launching stream (the events serialise the
+    calls, so this is each kernel's duration alone)."""
+    stream = torch.cuda.current_stream()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wl.calls]
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    t_host = time.perf_counter()
+    for c in wl.calls:
+        wl.run(0, c["index"])
+    host_per_step = time.perf_counter() - t_host
+    torch.cuda.synchronize()
+    _hold_stream(torch, 2.0 * host_per_step * steps + 2e-3)
+    for s in range(steps):
+        for j, c in enumerate(wl.calls):
+            ev[s][j][0].record(stream)
+            wl.run(s % replicas, c["index"])
+            ev[s][j][1].record(stream)
+    torch.cuda.synchronize()
+    return [_summary(c, statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(steps)))
+            for j, c in enumerate(wl.calls)]
 
 
 def time_calls_flushed(torch, wl, steps, warmup):
@@ -388,8 +412,9 @@ def run_ours(args):
     unit = _unit_of(wl.calls)
 
     clock_proc = _sample_clocks() if rank == 0 else None
-    total_ms, per_call = time_steps(torch, wl, args.steps, args.warmup, replicas, ws)
+    total_ms = time_steps(torch, wl, args.steps, args.warmup, replicas, ws)
     clocks = _finish_clocks(clock_proc, _pci_bus_id(torch, local)) if rank == 0 else None
+    per_call = time_each_call(torch, wl, args.steps, replicas)
 
     value = _throughput(wl.calls, unit, total_ms * 1e-3 / args.steps, factor=ws)
     dominant = max(per_call, key=lambda c: c["ms"])

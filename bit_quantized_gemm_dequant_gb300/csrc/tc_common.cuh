@@ -93,6 +93,25 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Prefetch one box of a tiled tensor into L2 (no shared-memory destination,
+// no completion).  L2 is the point of coherence for global memory, so this is
+// safe even before the data's producer has finished: a later write still
+// lands in L2 and a later load sees it.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel of the stream (if it was
+// launched as a programmatic dependent) start taking SMs as they free up, and
+// wait until the kernels this one depends on have finished and their memory
+// operations are visible.  Both are no-ops without such a dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor core operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -10,36 +10,44 @@
 // layout), so it shares this path.
 //
 // Design (HBM-bound; the packed weights are read from HBM exactly once):
-//   * A CTA owns 128 output columns and a slice of K.  One producer thread
-//     streams the packed weight tile of every 64-k chunk (INT8: 64 rows x 128
-//     bytes, INT4: 32 rows x 128 bytes) with TMA into a 64 KB shared-memory
-//     ring, so up to 64 KB per CTA (three CTAs per SM) is in flight no matter
-//     what the consumers are doing.
-//   * Consumer warps take the chunks round-robin.  Each thread reads 16-byte
-//     vectors of packed weights from shared memory and dequantizes them in
-//     registers straight into the A operand of mma.sync.m16n8k16
-//     (Y^T = W^T X^T: weight columns are the MMA rows, the M <= 16 activation
-//     rows the MMA columns).  INT4 codes become exact fp16 (q - 8) with one
-//     LOP3 (0x6400 | nibble = 1024 + nibble) and one HSUB2/HFMA2 per two
-//     weights; INT8 with one LOP3 (byte ^ 0x80 | 0x6400) and one HSUB2.  The
-//     per-column scale factors out of the K sum and is applied once in the
-//     epilogue (exact reordering: it is per column).
+//   * One CTA of twelve warps per SM.  A work unit is one chunk of one
+//     128-column tile: 32 rows x 128 bytes of the packed weight matrix (64 k
+//     for INT4, 32 k for INT8 and e4m3).  The CTA's local units are dealt to
+//     its warps round-robin, and every warp streams its own units: lane 0
+//     issues the TMA loads of the unit's weight box (128-byte swizzle) and of
+//     the matching activation box into one of the warp's own ring slots
+//     (three per warp where they fit, else two), and refills a slot as soon as
+//     the warp has consumed it.  About 144 KB of weights per SM are in flight,
+//     no warp waits for another to free a slot, and none waits on a global
+//     load.  A slot is only ever filled and read by one warp, in order (an
+//     mbarrier wait names only the parity of a phase, so a reader that could
+//     reach a slot two fills ahead would take a stale phase for a fresh one).
+//   * A consumer thread reads 16-byte vectors of packed weights from shared
+//     memory (rows 2c, 2c + 1, ... so that, with the swizzle, the eight lanes
+//     of a quarter-warp hit eight different bank groups) and dequantizes them
+//     in registers straight into the A operand of mma.sync (Y^T = W^T X^T:
+//     weight columns are the MMA rows, the M <= 16 activation rows the MMA
+//     columns).  INT4 codes become exact fp16 (q - 8) with one LOP3 (0x6400 |
+//     nibble = 1024 + nibble) and one HSUB2/HFMA2 per two weights; INT8 with
+//     one LOP3 (byte ^ 0x80 | 0x6400) and one HSUB2.  The per-column scale
+//     factors out of the K sum and is applied once in the epilogue (exact
+//     reordering: it is per column).
 //   * e4m3 needs no dequantization: four K rows of 16 bytes are turned into
-//     K-contiguous 4-byte words by a 4 x 4 byte transpose (8 PRMT per 16
-//     bytes) and fed to mma.sync.m16n8k32.e4m3; the activation fragment is
-//     4 consecutive bytes of a row of A.
-//   * INT4 MMA k-order: a register of the A fragment holds the low (or high)
-//     nibbles of the same byte column from K-pair rows c and c + 4, so one
-//     PRMT serves four weights; the activation fragment is permuted to the
-//     same k order (k0+2c, k0+2c+8 | k0+2c+1, k0+2c+9).
-//   * Stream-K split: the grid is exactly the number of CTAs the GPU holds at
-//     once (three per SM), and the (M tile, 128-column tile, 64-k chunk) work
-//     units are dealt out as equal contiguous runs, so every SM streams the
-//     same number of bytes and the launch is a single wave.  Consumer warps
-//     reduce a tile's partial sums through shared memory; when a tile is
-//     split between CTAs, each writes its partial tile to the caller's
-//     workspace and the last one to arrive (per-tile counter) adds them in a
-//     fixed order, so the result is deterministic, and resets the counter.
+//     K-contiguous 4-byte words by a 4 x 4 byte transpose (PRMT) and fed to
+//     mma.sync.m16n8k32.e4m3.
+//   * MMA k-order: any bijection between the MMA's k slots and the real k
+//     indices gives the same sum as long as the weight and activation
+//     fragments use the same one.  Each fragment slot pair is mapped to the
+//     weight rows a thread loads (see the per-mode comments), and the
+//     activation fragment is gathered from shared memory in that order.
+//   * Stream-K split: the grid is the SM count and the (M tile, 128-column
+//     tile, chunk) units are dealt out as equal contiguous runs, so every SM
+//     streams the same number of bytes in a single wave.  The warps' partial
+//     sums of a tile meet in shared memory (lane-native float4
+//     layout, conflict free, fixed order); when a tile is split between
+//     CTAs, each writes its partial tile to the caller's workspace and the
+//     last one to arrive (per-tile counter) adds them in CTA order, so the
+//     result is deterministic, and resets the counter.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -52,13 +60,15 @@
 namespace wq {
 namespace {
 
-constexpr int kTileN = 256;       // output columns per tile: 256-byte rows per TMA box row
-constexpr int kHalfN = 128;       // columns per consumer warp (a warp pair splits a tile)
-constexpr int kChunkK = 32;       // k per pipeline stage
-constexpr int kRingBytes = 48 * 1024;
-constexpr int kConsumers = 4;     // consumer warps (plus one producer warp)
-constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kCtasPerSm = 3;
+constexpr int kTileN = 128;                  // output columns per tile = bytes per weight box row
+constexpr int kBoxRows = 32;                 // packed weight rows per unit
+constexpr int kWBytes = kBoxRows * kTileN;   // 4 KB of packed weights per unit
+constexpr int kWarps = 12;                   // warps per CTA; each loads and consumes its own units
+constexpr int kThreads = kWarps * 32;
+constexpr int kRedRounds = 3;                // rounds of the in-CTA reduction
+constexpr int kRedBufs = kWarps / kRedRounds;  // shared-memory partial tiles
+static_assert(kWarps % kRedRounds == 0, "reduction rounds must split the warps evenly");
+constexpr int kSmemLimit = 227 * 1024;
 // Workspace layout: a fixed counter area first (one int per tile, at most
 // kMaxSplitTiles tiles), so that the counters of any shape sit in bytes that
 // every call leaves zero; the partial tiles follow.
@@ -80,22 +90,29 @@ struct SkinnyArgs {
   void* ws;
 };
 
-template <int BITS>
-struct Ring {
-  static constexpr int kRows = BITS == kInt4 ? kChunkK / 2 : kChunkK;  // rows of the packed tile
-  static constexpr int kStageBytes = kRows * kTileN;
-  static constexpr int kStages = kRingBytes / kStageBytes;
-  // Slot i % kStages holds local chunk i and chunk i is consumed by warp pair
-  // i % 2: with an even slot count every slot belongs to one pair, which
-  // waits on it in order, so a wait can never see the slot's phase from two
-  // fills back (the parity of an mbarrier phase repeats every two phases).
-  static_assert(kStages % 2 == 0, "each ring slot must belong to one warp pair");
+template <int BITS, int MT>
+struct Cfg {
+  static constexpr int kChunkK = BITS == kInt4 ? 64 : 32;   // k per unit
+  static constexpr int kXRowBytes = kChunkK * (BITS == kE4m3 ? 1 : 2);  // 128, 64 or 32
+  static constexpr int kRows = 8 * MT;                      // activation rows per M tile
+  static constexpr int kXBytes = kRows * kXRowBytes;        // activation box
+  static constexpr int kXAlloc = (kXBytes + 1023) / 1024 * 1024;
+  static constexpr int kSlotBytes = kWBytes + kXAlloc;      // 1 KB multiple: swizzle atoms stay aligned
+  static constexpr int kOutF4 = MT * 8 * 32;                // float4 per partial tile (lane-native)
+  static constexpr int kRedBytes = kRedBufs * kOutF4 * 16;
+  static constexpr int kFixedBytes = kRedBytes + 1024 + 64;  // + alignment slack, flags
+  // Units in flight per warp: three where they fit in shared memory, else two.
+  static constexpr int kDepth = kWarps * 3 * (kSlotBytes + 8) + kFixedBytes <= kSmemLimit ? 3 : 2;
+  static constexpr int kStages = kWarps * kDepth;
+  static constexpr int kRingBytes = kStages * kSlotBytes;
+  static constexpr size_t kSmemBytes = kRingBytes + kStages * 8 + kFixedBytes;
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
-template <int MT>
-constexpr size_t skinny_smem_bytes() {
-  return kRingBytes + sizeof(float) * 8 * MT * kTileN + 512 + 128;
-}
+// Offset of byte `o` of a densely packed box after the TMA swizzle whose span
+// is `cpr` 16-byte chunks (2, 4, 8 for 32, 64, 128 bytes): the chunk index
+// (bits 4..) is XORed with bits 7.. of the offset.  Boxes sit 1 KB aligned.
+__device__ __forceinline__ int swz(int o, int cpr) { return o ^ (((o >> 7) & (cpr - 1)) << 4); }
 
 // Stream-K plan: U = tiles * chunks units over G CTAs; CTA b owns units
 // [b*U/G, (b+1)*U/G).
@@ -108,10 +125,6 @@ __host__ __device__ __forceinline__ int64_t unit_lo(int b, int64_t U, int G) { r
 // The CTA whose run contains unit u.
 __host__ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G) {
   return static_cast<int>(((u + 1) * G - 1) / U);
-}
-
-__device__ __forceinline__ uint32_t ldg_x2(const __half* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -143,9 +156,9 @@ __device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t 
   c[3] = __byte_perm(t2, t3, 0x7632);
 }
 
-// One 32-k step of e4m3: v[0..3] = rows 4c .. 4c+3 and v[4..7] = rows
-// 16 + 4c .. 16 + 4c + 3 of the step, 16 columns each.  MMA i takes columns
-// 2i (MMA row g) and 2i + 1 (row g + 8).
+// One 32-k step of e4m3: v[0..3] feed k slots 4c .. 4c+3 and v[4..7] slots
+// 16 + 4c .. 16 + 4c + 3, 16 columns each.  MMA i takes columns 2i (MMA row
+// g) and 2i + 1 (row g + 8).
 template <int MT>
 __device__ __forceinline__ void fp8_step(float (&acc)[MT][8][4], const uint4* v, const uint32_t (&xb)[MT][2]) {
   const uint32_t lo[4][4] = {{v[0].x, v[1].x, v[2].x, v[3].x}, {v[0].y, v[1].y, v[2].y, v[3].y},
@@ -185,8 +198,11 @@ __device__ __forceinline__ uint32_t int8_pair(uint32_t u) {
 }
 
 // One 16-k step: dequantize the thread's weight vectors and issue the MMAs.
-// INT4: wv[0] = K-pair row c, wv[1] = row c + 4 of the step's 8 K-pair rows.
-// INT8: wv[0..3] = rows 2c, 2c + 1, 2c + 8, 2c + 9 of the step's 16 rows.
+// INT4: wv[0], wv[1] = K-pair rows 2c, 2c + 1 of the step's 8 (k = 4c ..
+//   4c + 3); slots (2c, 2c+1) take k (4c, 4c+2) and slots (2c+8, 2c+9) take
+//   k (4c+1, 4c+3).
+// INT8: wv[0..3] = rows 2c, 2c + 1, 2c + 8, 2c + 9 of the step's 16 (natural
+//   k order).
 template <int BITS, int MT>
 __device__ __forceinline__ void wo_step(float (&acc)[MT][8][4], const uint4* wv, const uint32_t (&xb)[MT][2]) {
   if constexpr (BITS == kInt4) {
@@ -224,76 +240,140 @@ __device__ __forceinline__ void wo_step(float (&acc)[MT][8][4], const uint4* wv,
   }
 }
 
-// 4 consecutive e4m3 bytes of A at k .. k+3, zero beyond K (0x7F would be NaN).
-__device__ __forceinline__ uint32_t ldg_e4m3x4(const uint8_t* row, int k, int K) {
-  if (k + 4 <= K) return __ldg(reinterpret_cast<const unsigned int*>(row + k));
-  uint32_t w = 0;
-  for (int i = 0; i < 4; ++i)
-    if (k + i < K) w |= static_cast<uint32_t>(__ldg(row + k + i)) << (8 * i);
-  return w;
-}
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
-// Activation fragments of one chunk (rows 8mt + g of this M tile): four
-// 16-k steps of fp16 X, or two 32-k steps of e4m3 A.
+// One unit from its ring slot: w = 32 swizzled weight rows of 128 bytes,
+// x = the swizzled activation box (row m = 8 mt + g of this M tile).  The
+// thread's 16-byte column group is g; rows r with r % 8 == 2c sit at swizzled
+// column o0, rows with r % 8 == 2c + 1 at o1.
 template <int BITS, int MT>
-__device__ __forceinline__ void load_x_chunk(uint32_t (&xb)[4][MT][2], const SkinnyArgs& p, int m_base,
-                                             int k_chunk, int g, int c) {
+__device__ __forceinline__ void consume_unit(float (&acc)[MT][8][4], const uint8_t* w, const uint8_t* x, int g,
+                                             int c) {
+  using C = Cfg<BITS, MT>;
+  constexpr int cpr = C::kXRowBytes / 16;
+  const int o0 = (g ^ (2 * c)) << 4, o1 = (g ^ (2 * c + 1)) << 4;
   if constexpr (BITS == kE4m3) {
-    const uint8_t* X = static_cast<const uint8_t*>(p.X);
+    // Slots 4c .. 4c+3 <- rows 2c, 2c+1, 2c+8, 2c+9; slots 16+4c .. <- rows
+    // 2c+16, 2c+17, 2c+24, 2c+25: activation bytes at the same k.
+    uint32_t xb[MT][2];
 #pragma unroll
-    for (int j = 0; j < kChunkK / 32; ++j) {
-      const int ka = k_chunk + 32 * j + 4 * c, kb = ka + 16;
+    for (int mt = 0; mt < MT; ++mt) {
+      const int r = (8 * mt + g) * C::kXRowBytes + 2 * c;
+      xb[mt][0] = lds16(x + swz(r, cpr)) | (lds16(x + swz(r + 8, cpr)) << 16);
+      xb[mt][1] = lds16(x + swz(r + 16, cpr)) | (lds16(x + swz(r + 24, cpr)) << 16);
+    }
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 2 * c + 8 * i;  // rows row, row + 1
+      v[(i & 1) * 2 + (i >> 1) * 4] = lds128(w + row * kTileN + o0);
+      v[(i & 1) * 2 + (i >> 1) * 4 + 1] = lds128(w + (row + 1) * kTileN + o1);
+    }
+    fp8_step<MT>(acc, v, xb);
+  } else if constexpr (BITS == kInt8) {
+    uint32_t xb[2][MT][2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int m = m_base + 8 * mt + g;
-        const uint8_t* xr = X + static_cast<int64_t>(m) * p.ldx;
-        xb[j][mt][0] = (m < p.M && ka < p.K) ? ldg_e4m3x4(xr, ka, p.K) : 0u;
-        xb[j][mt][1] = (m < p.M && kb < p.K) ? ldg_e4m3x4(xr, kb, p.K) : 0u;
+        const int r = (8 * mt + g) * C::kXRowBytes + 32 * q + 4 * c;
+        xb[q][mt][0] = lds32(x + swz(r, cpr));        // k 16q + 2c, +1
+        xb[q][mt][1] = lds32(x + swz(r + 16, cpr));   // k 16q + 2c + 8, +9
       }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int row = 16 * q + 2 * c;
+      uint4 wv[4];
+      wv[0] = lds128(w + row * kTileN + o0);
+      wv[1] = lds128(w + (row + 1) * kTileN + o1);
+      wv[2] = lds128(w + (row + 8) * kTileN + o0);
+      wv[3] = lds128(w + (row + 9) * kTileN + o1);
+      wo_step<kInt8, MT>(acc, wv, xb[q]);
     }
   } else {
-    const __half* X = static_cast<const __half*>(p.X);
 #pragma unroll
-    for (int j = 0; j < kChunkK / 16; ++j) {
-      const int ka = k_chunk + 16 * j + 2 * c, kb = ka + 8;
+    for (int q = 0; q < 4; ++q) {
+      uint32_t xb[MT][2];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int m = m_base + 8 * mt + g;
-        const bool mok = m < p.M;
-        const __half* xr = X + static_cast<int64_t>(m) * p.ldx;
-        const uint32_t pa = (mok && ka < p.K) ? ldg_x2(xr + ka) : 0u;
-        const uint32_t pb = (mok && kb < p.K) ? ldg_x2(xr + kb) : 0u;
-        if constexpr (BITS == kInt4) {
-          xb[j][mt][0] = __byte_perm(pa, pb, 0x5410);  // {x[k0+2c], x[k0+2c+8]}
-          xb[j][mt][1] = __byte_perm(pa, pb, 0x7632);  // {x[k0+2c+1], x[k0+2c+9]}
-        } else {
-          xb[j][mt][0] = pa;
-          xb[j][mt][1] = pb;
-        }
+        const uint2 pp = lds64(x + swz((8 * mt + g) * C::kXRowBytes + 32 * q + 8 * c, cpr));  // k 16q + 4c .. +3
+        xb[mt][0] = __byte_perm(pp.x, pp.y, 0x5410);  // {x[4c], x[4c+2]}
+        xb[mt][1] = __byte_perm(pp.x, pp.y, 0x7632);  // {x[4c+1], x[4c+3]}
       }
+      const int row = 8 * q + 2 * c;
+      uint4 wv[2];
+      wv[0] = lds128(w + row * kTileN + o0);
+      wv[1] = lds128(w + (row + 1) * kTileN + o1);
+      wo_step<kInt4, MT>(acc, wv, xb);
     }
   }
 }
 
-// Barrier over the consumer warps only (the producer keeps streaming).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+// Write two adjacent outputs (row gm, columns gn and gn + 1) of the final
+// result, skipping columns at or beyond N.
+template <int BITS>
+__device__ __forceinline__ void store_pair(const SkinnyArgs& p, int gm, int gn, float v0, float v1) {
+  if (gn >= p.N) return;
+  const bool two = gn + 1 < p.N;
+  if constexpr (BITS == kE4m3) {
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.Y) + static_cast<int64_t>(gm) * p.ldy + gn;
+    if (two)
+      *reinterpret_cast<__nv_bfloat162*>(y) = __floats2bfloat162_rn(v0 * p.scale, v1 * p.scale);
+    else
+      *y = __float2bfloat16_rn(v0 * p.scale);
+  } else {
+    const __half* S = static_cast<const __half*>(p.scales) + gn;
+    __half* y = static_cast<__half*>(p.Y) + static_cast<int64_t>(gm) * p.ldy + gn;
+    if (two)
+      *reinterpret_cast<__half2*>(y) = __floats2half2_rn(__half2float(S[0]) * v0, __half2float(S[1]) * v1);
+    else
+      *y = __float2half_rn(__half2float(S[0]) * v0);
+  }
+}
+
+// Lane-native partial element e = (mt * 8 + q) * 32 + lane holds acc[mt][q]
+// of that lane: rows 8mt + 2c (.x, .z) and 8mt + 2c + 1 (.y, .w), columns
+// 16g + 2q (.x, .y) and 16g + 2q + 1 (.z, .w), with g = lane / 4, c = lane % 4.
+template <int BITS>
+__device__ __forceinline__ void store_elem(const SkinnyArgs& p, int e, int m_base, int n_base, float4 v) {
+  const int ln = e & 31, q = (e >> 5) & 7, mt = e >> 8;
+  const int gm = m_base + 8 * mt + 2 * (ln & 3), gn = n_base + 16 * (ln >> 2) + 2 * q;
+  if (gm < p.M) store_pair<BITS>(p, gm, gn, v.x, v.z);
+  if (gm + 1 < p.M) store_pair<BITS>(p, gm + 1, gn, v.y, v.w);
+}
+
+// Number of CTAs whose runs touch tile T.
+__device__ __forceinline__ int tile_contributors(int T, int64_t U, int G, int ch) {
+  return unit_owner(static_cast<int64_t>(T + 1) * ch - 1, U, G) - unit_owner(static_cast<int64_t>(T) * ch, U, G) + 1;
+}
+
+__device__ __forceinline__ bool elem_live(int e, int rows_valid) { return 8 * (e >> 8) + 2 * (e & 3) < rows_valid; }
+
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// Barrier over the CTA's warps (all of them load and consume).
+__device__ __forceinline__ void cta_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
 template <int BITS, int MT>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, SkinnyArgs p, Plan pl, int* err) {
-  using R = Ring<BITS>;
-  constexpr int kRows = 8 * MT;
-  constexpr int kOut = kRows * kTileN;  // outputs per tile
+__global__ void __launch_bounds__(kThreads, 1)
+wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, SkinnyArgs p,
+                 Plan pl, int* err) {
+  using C = Cfg<BITS, MT>;
+  constexpr int D = C::kDepth;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((128 - (tc::smem_u32(smem_raw) & 127)) & 127);
+  uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* ring = smem;
-  float* part = reinterpret_cast<float*>(smem + kRingBytes);  // [kRows][kTileN]
-  uint64_t* full = reinterpret_cast<uint64_t*>(part + kOut);
-  uint64_t* empty = full + R::kStages;
-  volatile int* abort = reinterpret_cast<volatile int*>(empty + R::kStages);
-  volatile int* last_flag = abort + 1;
+  float4* red = reinterpret_cast<float4*>(smem + C::kRingBytes);  // [kRedBufs][kOutF4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kRedBytes);
+  volatile int* abort = reinterpret_cast<volatile int*>(full + C::kStages);
+  volatile int* last_flag = abort + 1;  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -302,52 +382,61 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, SkinnyArgs p, Plan pl,
   const int ch = pl.chunks;
   const int64_t lo = unit_lo(b, U, G);
   const int n_local = static_cast<int>(unit_lo(b + 1, U, G) - lo);
+  // This warp's units are local indices warp, warp + kWarps, ...; its k-th
+  // unit goes to its own slot warp * D + k % D.
+  const int n_mine = n_local > warp ? (n_local - warp + kWarps - 1) / kWarps : 0;
 
+  // The next call in the stream may start claiming SMs as this grid's CTAs
+  // leave; it waits (griddep_wait) before touching memory this grid writes.
+  tc::griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < R::kStages; ++s) {
-      tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 2);  // both warps of the consuming pair
-    }
+    for (int s = 0; s < C::kStages; ++s) tc::mbar_init(&full[s], 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kConsumers) {
-    // Producer: one elected thread keeps the ring full across the CTA's run.
-    if (lane == 0 && n_local > 0) {
-      tc::tma_prefetch_desc(&tmW);
-      int issued = 0;
-      for (int i = 0; i < n_local; ++i) {
-        const int64_t u = lo + i;
-        const int T = static_cast<int>(u / ch), chunk = static_cast<int>(u % ch);
-        const int s = i % R::kStages;
-        if (!tc::mbar_wait(&empty[s], ((i / R::kStages) & 1) ^ 1, abort, err, kSiteGemmProducer)) break;
-        tc::mbar_arrive_expect_tx(&full[s], R::kStageBytes);
-        tc::tma_load_2d(ring + s * R::kStageBytes, &tmW, (T % pl.n_tiles) * kTileN, chunk * R::kRows, &full[s]);
-        issued = i + 1;
-      }
-      // Let the last copies land before this thread leaves: the CTA must not
-      // exit with TMA writes into its shared memory still in flight.
-      for (int i = issued > R::kStages ? issued - R::kStages : 0; i < issued; ++i)
-        tc::mbar_wait_drain(&full[i % R::kStages], (i / R::kStages) & 1);
+  // Lane 0 of a warp starts the TMA loads of the warp's k-th unit.
+  auto issue = [&](int k) {
+    const int64_t u = lo + warp + static_cast<int64_t>(k) * kWarps;
+    const int T = static_cast<int>(u / ch), chunk = static_cast<int>(u % ch);
+    const int s = warp * D + k % D;
+    uint8_t* slot = ring + s * C::kSlotBytes;
+    tc::mbar_arrive_expect_tx(&full[s], kWBytes + C::kXBytes);
+    tc::tma_load_2d(slot, &tmW, (T % pl.n_tiles) * kTileN, chunk * kBoxRows, &full[s]);
+    tc::tma_load_2d(slot + kWBytes, &tmX, chunk * C::kChunkK, (T / pl.n_tiles) * C::kRows, &full[s]);
+  };
+  if (lane == 0) {
+    tc::tma_prefetch_desc(&tmW);
+    tc::tma_prefetch_desc(&tmX);
+    // Pull the warp's first weight boxes into L2 while the previous kernel of
+    // the stream may still be running (a prefetch cannot read stale data).
+    for (int k = 0; k < D && k < n_mine; ++k) {
+      const int64_t u = lo + warp + static_cast<int64_t>(k) * kWarps;
+      tc::tma_prefetch_l2_2d(&tmW, static_cast<int>((u / ch) % pl.n_tiles) * kTileN,
+                             static_cast<int>(u % ch) * kBoxRows);
     }
-    return;
   }
+  // Everything below reads inputs or writes outputs and workspace that
+  // earlier work in the stream may still own.
+  tc::griddep_wait();
+  if (lane == 0)
+    for (int k = 0; k < D && k < n_mine; ++k) issue(k);
 
-  // Consumers: one segment per tile the run touches.
   int* ws_count = static_cast<int*>(p.ws);
-  float* ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(p.ws) + kCounterBytes);
-  const __half* S = static_cast<const __half*>(p.scales);
-  uint32_t xb[4][MT][2];
+  float4* ws_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(p.ws) + kCounterBytes);
+  const int t = threadIdx.x;
+  int k = 0;  // the warp's next unit to consume
+  bool ok = true;
+  int pend0 = -1, pend1 = -1;  // shared tiles of this run (its first and last segment at most)
+  // One segment per tile the CTA's run touches.
   for (int i = 0; i < n_local;) {
     const int64_t u0 = lo + i;
     const int T = static_cast<int>(u0 / ch);
     const int64_t seg_end = static_cast<int64_t>(T + 1) * ch < lo + n_local ? static_cast<int64_t>(T + 1) * ch
                                                                              : lo + n_local;
     const int seg = static_cast<int>(seg_end - u0);
-    const int m_base = (T / pl.n_tiles) * kRows, n_base = (T % pl.n_tiles) * kTileN;
-    const int chunk0 = static_cast<int>(u0 - static_cast<int64_t>(T) * ch);
+    const int m_base = (T / pl.n_tiles) * C::kRows, n_base = (T % pl.n_tiles) * kTileN;
 
     float acc[MT][8][4];
 #pragma unroll
@@ -357,136 +446,110 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, SkinnyArgs p, Plan pl,
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[mt][q][r] = 0.0f;
 
-    // Warp pair (warp >> 1) takes the chunks whose local index has its
-    // parity (so it always uses the same ring slots); the two warps of a pair
-    // take the two 128-column halves of the tile.
-    const int half = warp & 1, pair = warp >> 1;
-    for (int j = ((i & 1) == pair) ? 0 : 1; j < seg; j += kConsumers / 2) {
-      const int li = i + j;
-      const int s = li % R::kStages;
-      load_x_chunk<BITS, MT>(xb, p, m_base, (chunk0 + j) * kChunkK, g, c);
-      const bool ok = tc::mbar_wait(&full[s], (li / R::kStages) & 1, abort, err, kSiteGemmMma);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      const uint8_t* st = ring + s * R::kStageBytes + kHalfN * half + 16 * g;
-      if constexpr (BITS == kE4m3) {
-#pragma unroll
-        for (int q = 0; q < kChunkK / 32; ++q) {  // 32-k steps
-          uint4 v[8];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            v[r] = *reinterpret_cast<const uint4*>(st + (32 * q + 4 * c + r) * kTileN);
-            v[4 + r] = *reinterpret_cast<const uint4*>(st + (32 * q + 16 + 4 * c + r) * kTileN);
-          }
-          fp8_step<MT>(acc, v, xb[q]);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < kChunkK / 16; ++q) {  // 16-k steps
-          uint4 wv[BITS == kInt4 ? 2 : 4];
-          if constexpr (BITS == kInt4) {
-            wv[0] = *reinterpret_cast<const uint4*>(st + (8 * q + c) * kTileN);
-            wv[1] = *reinterpret_cast<const uint4*>(st + (8 * q + c + 4) * kTileN);
-          } else {
-            wv[0] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c) * kTileN);
-            wv[1] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c + 1) * kTileN);
-            wv[2] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c + 8) * kTileN);
-            wv[3] = *reinterpret_cast<const uint4*>(st + (16 * q + 2 * c + 9) * kTileN);
-          }
-          wo_step<BITS, MT>(acc, wv, xb[q]);
-        }
-      }
-      // The slot's next contents arrive through TMA (async proxy): order this
-      // thread's generic-proxy reads of the slot before releasing it.
+    for (; ok && k < n_mine && warp + k * kWarps < i + seg; ++k) {
+      const int s = warp * D + k % D;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[s], (k / D) & 1, abort, err, kSiteGemmMma));
+      if (!ok) break;
+      const uint8_t* slot = ring + s * C::kSlotBytes;
+      consume_unit<BITS, MT>(acc, slot, slot + kWBytes, g, c);
+      // The slot's next contents arrive through TMA (async proxy): order the
+      // warp's generic-proxy reads of the slot before lane 0 refills it.
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&empty[s]);
+      if (lane == 0 && k + D < n_mine) issue(k + D);
     }
 
-    // Sum the two warp pairs' partial tiles in a fixed order.  acc[mt][q]
-    // covers MMA rows (weight columns) 128 * half + 16g + 2q and + 1, MMA
-    // columns (rows of X) 8mt + 2c and 8mt + 2c + 1.
-    for (int r = 0; r < kConsumers / 2; ++r) {
-      if (pair == r) {
+    // Warp w adds into buffer w % kRedBufs in round w / kRedBufs; the buffers
+    // are then summed in index order (a fixed order: deterministic).
+    float4* buf = red + (warp % kRedBufs) * C::kOutF4;
+    for (int r = 0; r < kRedRounds; ++r) {
+      if (warp / kRedBufs == r) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const int n = kHalfN * half + 16 * g + 2 * q, m = 8 * mt + 2 * c;
-            float2* p0 = reinterpret_cast<float2*>(part + m * kTileN + n);
-            float2* p1 = reinterpret_cast<float2*>(part + (m + 1) * kTileN + n);
-            float2 v0 = make_float2(acc[mt][q][0], acc[mt][q][2]);
-            float2 v1 = make_float2(acc[mt][q][1], acc[mt][q][3]);
-            if (r > 0) {
-              const float2 o0 = *p0, o1 = *p1;
-              v0.x += o0.x; v0.y += o0.y; v1.x += o1.x; v1.y += o1.y;
-            }
-            *p0 = v0;
-            *p1 = v1;
+            float4 v = make_float4(acc[mt][q][0], acc[mt][q][1], acc[mt][q][2], acc[mt][q][3]);
+            float4* d = buf + (mt * 8 + q) * 32 + lane;
+            if (r > 0) v = f4add(*d, v);
+            *d = v;
           }
       }
-      consumer_sync();
+      cta_sync();
     }
 
-    // Finish the tile, or hand this CTA's share to the last contributor.
-    // Only the tile's valid rows travel through the workspace.
-    const int f0 = unit_owner(static_cast<int64_t>(T) * ch, U, G);
-    const int f1 = unit_owner(static_cast<int64_t>(T + 1) * ch - 1, U, G);
-    const int contributors = f1 - f0 + 1;
-    const int t = threadIdx.x;  // 0 .. 127 across the consumer warps
-    const int rows_valid = p.M - m_base < kRows ? p.M - m_base : kRows;
-    const int n_out = rows_valid * kTileN;
-    bool finish = true;
-    const float* src = part;
-    if (contributors > 1) {
-      float* mine = ws_part + (static_cast<size_t>(T) * pl.slots + (b - f0)) * kOut;
-      for (int o = 4 * t; o < n_out; o += 4 * kConsumers * 32)
-        __stcg(reinterpret_cast<float4*>(mine + o), *reinterpret_cast<const float4*>(part + o));
-      __threadfence();
-      consumer_sync();
-      if (t == 0) *last_flag = (atomicAdd(&ws_count[T], 1) == contributors - 1);
-      consumer_sync();
-      finish = *last_flag != 0;
-      if (finish) __threadfence();
-      src = ws_part + static_cast<size_t>(T) * pl.slots * kOut;
-    }
-    if (finish) {
-      for (int o = 4 * t; o < n_out; o += 4 * kConsumers * 32) {
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (contributors > 1) {
-          // Eight partial tiles in flight at a time; summed in contributor order.
-          for (int q0 = 0; q0 < contributors; q0 += 8) {
-            float4 v[8];
+    // A tile inside the run is this CTA's alone: finish it now.  Only the
+    // first and the last segment of a contiguous run can share their tile
+    // with other CTAs; their partial tiles go to the workspace now, and the
+    // hand-shake with the other contributors waits for the end of the run,
+    // so that it never stalls the stream.
+    if (tile_contributors(T, U, G, ch) == 1) {
+      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+      for (int e = t; e < C::kOutF4; e += kThreads) {
+        if (!elem_live(e, rows_valid)) continue;
+        float4 v = red[e];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              v[u] = q0 + u < contributors
-                         ? __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(q0 + u) * kOut + o))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              sum.x += v[u].x; sum.y += v[u].y; sum.z += v[u].z; sum.w += v[u].w;
-            }
-          }
-        } else {
-          sum = *reinterpret_cast<const float4*>(src + o);
-        }
-        const int m = o / kTileN, n = o % kTileN;
-        const int gm = m_base + m;
-        const float v[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int gn = n_base + n + e;
-          if (gn >= p.N) continue;
-          if constexpr (BITS == kE4m3)
-            static_cast<__nv_bfloat16*>(p.Y)[static_cast<int64_t>(gm) * p.ldy + gn] = __float2bfloat16_rn(v[e] * p.scale);
-          else
-            static_cast<__half*>(p.Y)[static_cast<int64_t>(gm) * p.ldy + gn] = __float2half_rn(__half2float(S[gn]) * v[e]);
-        }
+        for (int q = 1; q < kRedBufs; ++q) v = f4add(v, red[q * C::kOutF4 + e]);
+        store_elem<BITS>(p, e, m_base, n_base, v);
       }
-      if (contributors > 1 && t == 0) ws_count[T] = 0;  // ready for the next call
+    } else {
+      const int f0 = unit_owner(static_cast<int64_t>(T) * ch, U, G);
+      float4* mine = ws_part + (static_cast<size_t>(T) * pl.slots + (b - f0)) * C::kOutF4;
+      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+      for (int e = t; e < C::kOutF4; e += kThreads) {
+        if (!elem_live(e, rows_valid)) continue;
+        float4 v = red[e];
+#pragma unroll
+        for (int q = 1; q < kRedBufs; ++q) v = f4add(v, red[q * C::kOutF4 + e]);
+        __stcg(mine + e, v);
+      }
+      if (pend0 < 0) pend0 = T; else pend1 = T;
     }
-    consumer_sync();  // `part` is rewritten by the next segment
+    cta_sync();  // `red` is reused by the next segment
     i += seg;
   }
+
+  // Hand-shake for the shared tiles: publish this CTA's partials, count it in
+  // on each tile, and finish the tiles it was the last to reach (summing the
+  // partials in CTA order, so the result does not depend on who came last).
+  if (pend0 >= 0) {
+    __threadfence();
+    cta_sync();
+    if (t < 2) {
+      const int T = t == 0 ? pend0 : pend1;
+      last_flag[t] = T >= 0 && atomicAdd(&ws_count[T], 1) == tile_contributors(T, U, G, ch) - 1;
+    }
+    cta_sync();
+    for (int j = 0; j < 2; ++j) {
+      if (last_flag[j] == 0) continue;
+      __threadfence();
+      const int T = j == 0 ? pend0 : pend1;
+      const int contributors = tile_contributors(T, U, G, ch);
+      const int m_base = (T / pl.n_tiles) * C::kRows, n_base = (T % pl.n_tiles) * kTileN;
+      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+      const float4* src = ws_part + static_cast<size_t>(T) * pl.slots * C::kOutF4;
+      for (int e = t; e < C::kOutF4; e += kThreads) {
+        if (!elem_live(e, rows_valid)) continue;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        // Eight partial tiles in flight at a time; summed in contributor order.
+        for (int q0 = 0; q0 < contributors; q0 += 8) {
+          float4 v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            v[q] = q0 + q < contributors ? __ldcg(src + static_cast<size_t>(q0 + q) * C::kOutF4 + e)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) sum = f4add(sum, v[q]);
+        }
+        store_elem<BITS>(p, e, m_base, n_base, sum);
+      }
+      if (t == 0) ws_count[T] = 0;  // ready for the next call
+    }
+  }
+
+  // After a give-up, let this warp's copies still in flight land before the
+  // CTA exits (no TMA write may target the shared memory of a finished CTA).
+  if (!ok && lane == 0)
+    for (int kk = k; kk < n_mine && kk < k + D; ++kk) tc::mbar_wait_drain(&full[warp * D + kk % D], (kk / D) & 1);
 }
 
 // Opt the kernel into its dynamic shared memory (above the 48 KB default);
@@ -495,7 +558,7 @@ template <int BITS, int MT>
 cudaError_t configure_kernel() {
   static cudaError_t status = cudaFuncSetAttribute(wo_skinny_kernel<BITS, MT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(skinny_smem_bytes<MT>()));
+                                                   static_cast<int>(Cfg<BITS, MT>::kSmemBytes));
   return status;
 }
 
@@ -506,7 +569,7 @@ int ctas_per_sm() {
     int n = 0;
     if (configure_kernel<BITS, MT>() != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wo_skinny_kernel<BITS, MT>, kThreads,
-                                                      skinny_smem_bytes<MT>()) != cudaSuccess || n < 1)
+                                                      Cfg<BITS, MT>::kSmemBytes) != cudaSuccess || n < 1)
       return 1;  // not cached: a later call may succeed
     cached = n;
   }
@@ -515,10 +578,11 @@ int ctas_per_sm() {
 
 template <int BITS, int MT>
 Plan make_plan(int M, int N, int K) {
+  using C = Cfg<BITS, MT>;
   Plan pl;
   pl.n_tiles = (N + kTileN - 1) / kTileN;
-  pl.tiles = pl.n_tiles * ((M + 8 * MT - 1) / (8 * MT));
-  pl.chunks = (K + kChunkK - 1) / kChunkK;
+  pl.tiles = pl.n_tiles * ((M + C::kRows - 1) / C::kRows);
+  pl.chunks = (K + C::kChunkK - 1) / C::kChunkK;
   pl.units = static_cast<int64_t>(pl.tiles) * pl.chunks;
   const int64_t cap = static_cast<int64_t>(sm_count()) * ctas_per_sm<BITS, MT>();
   pl.grid = static_cast<int>(pl.units < cap ? pl.units : cap);
@@ -539,23 +603,42 @@ template <int BITS, int MT>
 size_t plan_workspace(int M, int N, int K) {
   const Plan pl = make_plan<BITS, MT>(M, N, K);
   if (pl.slots == 1) return 0;
-  return kCounterBytes + static_cast<size_t>(pl.tiles) * pl.slots * (8 * MT) * kTileN * sizeof(float);
+  return kCounterBytes + static_cast<size_t>(pl.tiles) * pl.slots * Cfg<BITS, MT>::kOutF4 * 16;
 }
 
 template <int BITS, int MT>
 cudaError_t launch_variant(const SkinnyArgs& a, cudaStream_t s) {
-  using R = Ring<BITS>;
-  const size_t smem = skinny_smem_bytes<MT>();
-  auto kern = wo_skinny_kernel<BITS, MT>;
+  using C = Cfg<BITS, MT>;
   cudaError_t e = configure_kernel<BITS, MT>();
   if (e != cudaSuccess) return e;
   const Plan pl = make_plan<BITS, MT>(a.M, a.N, a.K);
-  CUtensorMap tW;
+  CUtensorMap tW, tX;
   const uint64_t rows = BITS == kInt4 ? a.K / 2 : a.K;
-  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, rows, a.ldw, kTileN, R::kRows,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, rows, a.ldw, kTileN, kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  kern<<<pl.grid, kThreads, smem, s>>>(tW, a, pl, device_error_word());
+  const CUtensorMapSwizzle xs = C::kXRowBytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : C::kXRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_32B;
+  if constexpr (BITS == kE4m3)
+    e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K, a.M, a.ldx, C::kChunkK, C::kRows, xs);
+  else
+    e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.K, a.M, a.ldx * 2, C::kChunkK, C::kRows, xs);
+  if (e != cudaSuccess) return e;
+  // Launched as a programmatic dependent of the previous kernel in the stream:
+  // its prologue and weight prefetch overlap that kernel's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, wo_skinny_kernel<BITS, MT>, tW, tX, a, pl, device_error_word());
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
