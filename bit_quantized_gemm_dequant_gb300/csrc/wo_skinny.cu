@@ -245,69 +245,94 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpre
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
-// One unit from its ring slot: w = 32 swizzled weight rows of 128 bytes,
+// One unit, held in registers: the thread's 8 weight vectors (16 bytes each)
+// and its activation fragments.  Reading the whole unit out of its ring slot
+// first lets the slot be refilled while the math runs.
+template <int BITS, int MT>
+struct UnitRegs {
+  static constexpr int kXWords = BITS == kInt4 ? 4 * MT * 2 : (BITS == kInt8 ? 2 * MT * 2 : MT * 2);
+  uint4 w[8];
+  uint32_t x[kXWords];
+};
+
+// Load one unit from its ring slot: w = 32 swizzled weight rows of 128 bytes,
 // x = the swizzled activation box (row m = 8 mt + g of this M tile).  The
 // thread's 16-byte column group is g; rows r with r % 8 == 2c sit at swizzled
 // column o0, rows with r % 8 == 2c + 1 at o1.
 template <int BITS, int MT>
-__device__ __forceinline__ void consume_unit(float (&acc)[MT][8][4], const uint8_t* w, const uint8_t* x, int g,
-                                             int c) {
+__device__ __forceinline__ void load_unit(UnitRegs<BITS, MT>& u, const uint8_t* w, const uint8_t* x, int g, int c) {
   using C = Cfg<BITS, MT>;
   constexpr int cpr = C::kXRowBytes / 16;
   const int o0 = (g ^ (2 * c)) << 4, o1 = (g ^ (2 * c + 1)) << 4;
   if constexpr (BITS == kE4m3) {
     // Slots 4c .. 4c+3 <- rows 2c, 2c+1, 2c+8, 2c+9; slots 16+4c .. <- rows
     // 2c+16, 2c+17, 2c+24, 2c+25: activation bytes at the same k.
-    uint32_t xb[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int r = (8 * mt + g) * C::kXRowBytes + 2 * c;
-      xb[mt][0] = lds16(x + swz(r, cpr)) | (lds16(x + swz(r + 8, cpr)) << 16);
-      xb[mt][1] = lds16(x + swz(r + 16, cpr)) | (lds16(x + swz(r + 24, cpr)) << 16);
+      u.x[2 * mt] = lds16(x + swz(r, cpr)) | (lds16(x + swz(r + 8, cpr)) << 16);
+      u.x[2 * mt + 1] = lds16(x + swz(r + 16, cpr)) | (lds16(x + swz(r + 24, cpr)) << 16);
     }
-    uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int row = 2 * c + 8 * i;  // rows row, row + 1
-      v[(i & 1) * 2 + (i >> 1) * 4] = lds128(w + row * kTileN + o0);
-      v[(i & 1) * 2 + (i >> 1) * 4 + 1] = lds128(w + (row + 1) * kTileN + o1);
+      u.w[(i & 1) * 2 + (i >> 1) * 4] = lds128(w + row * kTileN + o0);
+      u.w[(i & 1) * 2 + (i >> 1) * 4 + 1] = lds128(w + (row + 1) * kTileN + o1);
     }
-    fp8_step<MT>(acc, v, xb);
   } else if constexpr (BITS == kInt8) {
-    uint32_t xb[2][MT][2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int q = 0; q < 2; ++q) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int r = (8 * mt + g) * C::kXRowBytes + 32 * q + 4 * c;
-        xb[q][mt][0] = lds32(x + swz(r, cpr));        // k 16q + 2c, +1
-        xb[q][mt][1] = lds32(x + swz(r + 16, cpr));   // k 16q + 2c + 8, +9
+        u.x[(q * MT + mt) * 2] = lds32(x + swz(r, cpr));           // k 16q + 2c, +1
+        u.x[(q * MT + mt) * 2 + 1] = lds32(x + swz(r + 16, cpr));  // k 16q + 2c + 8, +9
       }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
       const int row = 16 * q + 2 * c;
-      uint4 wv[4];
-      wv[0] = lds128(w + row * kTileN + o0);
-      wv[1] = lds128(w + (row + 1) * kTileN + o1);
-      wv[2] = lds128(w + (row + 8) * kTileN + o0);
-      wv[3] = lds128(w + (row + 9) * kTileN + o1);
-      wo_step<kInt8, MT>(acc, wv, xb[q]);
+      u.w[4 * q] = lds128(w + row * kTileN + o0);
+      u.w[4 * q + 1] = lds128(w + (row + 1) * kTileN + o1);
+      u.w[4 * q + 2] = lds128(w + (row + 8) * kTileN + o0);
+      u.w[4 * q + 3] = lds128(w + (row + 9) * kTileN + o1);
     }
   } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint32_t xb[MT][2];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const uint2 pp = lds64(x + swz((8 * mt + g) * C::kXRowBytes + 32 * q + 8 * c, cpr));  // k 16q + 4c .. +3
-        xb[mt][0] = __byte_perm(pp.x, pp.y, 0x5410);  // {x[4c], x[4c+2]}
-        xb[mt][1] = __byte_perm(pp.x, pp.y, 0x7632);  // {x[4c+1], x[4c+3]}
+        u.x[(q * MT + mt) * 2] = __byte_perm(pp.x, pp.y, 0x5410);      // {x[4c], x[4c+2]}
+        u.x[(q * MT + mt) * 2 + 1] = __byte_perm(pp.x, pp.y, 0x7632);  // {x[4c+1], x[4c+3]}
       }
       const int row = 8 * q + 2 * c;
-      uint4 wv[2];
-      wv[0] = lds128(w + row * kTileN + o0);
-      wv[1] = lds128(w + (row + 1) * kTileN + o1);
-      wo_step<kInt4, MT>(acc, wv, xb);
+      u.w[2 * q] = lds128(w + row * kTileN + o0);
+      u.w[2 * q + 1] = lds128(w + (row + 1) * kTileN + o1);
+    }
+  }
+}
+
+// The math of one unit from registers.
+template <int BITS, int MT>
+__device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], const UnitRegs<BITS, MT>& u) {
+  if constexpr (BITS == kE4m3) {
+    uint32_t xb[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      xb[mt][0] = u.x[2 * mt];
+      xb[mt][1] = u.x[2 * mt + 1];
+    }
+    fp8_step<MT>(acc, u.w, xb);
+  } else {
+    constexpr int kSteps = BITS == kInt4 ? 4 : 2;
+    constexpr int kVec = 8 / kSteps;  // weight vectors per 16-k step
+#pragma unroll
+    for (int q = 0; q < kSteps; ++q) {
+      uint32_t xb[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        xb[mt][0] = u.x[(q * MT + mt) * 2];
+        xb[mt][1] = u.x[(q * MT + mt) * 2 + 1];
+      }
+      wo_step<BITS, MT>(acc, u.w + kVec * q, xb);
     }
   }
 }
@@ -396,25 +421,45 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   }
   __syncthreads();
 
-  // Lane 0 of a warp starts the TMA loads of the warp's k-th unit.
+  // Lane 0 of a warp starts the TMA loads of the warp's units in order; the
+  // cursor (tile, chunk) of the next one advances by kWarps units at a time
+  // (no division in the loop).
+  int cur_n = 0, cur_m = 0, cur_c = 0;  // n tile, m tile, chunk
+  if (n_mine > 0) {
+    const int64_t u = lo + warp;
+    const int t0 = static_cast<int>(u / ch);
+    cur_c = static_cast<int>(u - static_cast<int64_t>(t0) * ch);
+    cur_n = t0 % pl.n_tiles;
+    cur_m = t0 / pl.n_tiles;
+  }
   auto issue = [&](int k) {
-    const int64_t u = lo + warp + static_cast<int64_t>(k) * kWarps;
-    const int T = static_cast<int>(u / ch), chunk = static_cast<int>(u % ch);
     const int s = warp * D + k % D;
     uint8_t* slot = ring + s * C::kSlotBytes;
     tc::mbar_arrive_expect_tx(&full[s], kWBytes + C::kXBytes);
-    tc::tma_load_2d(slot, &tmW, (T % pl.n_tiles) * kTileN, chunk * kBoxRows, &full[s]);
-    tc::tma_load_2d(slot + kWBytes, &tmX, chunk * C::kChunkK, (T / pl.n_tiles) * C::kRows, &full[s]);
+    tc::tma_load_2d(slot, &tmW, cur_n * kTileN, cur_c * kBoxRows, &full[s]);
+    tc::tma_load_2d(slot + kWBytes, &tmX, cur_c * C::kChunkK, cur_m * C::kRows, &full[s]);
+    cur_c += kWarps;
+    while (cur_c >= ch) {
+      cur_c -= ch;
+      if (++cur_n == pl.n_tiles) {
+        cur_n = 0;
+        ++cur_m;
+      }
+    }
   };
   if (lane == 0) {
     tc::tma_prefetch_desc(&tmW);
     tc::tma_prefetch_desc(&tmX);
     // Pull the warp's first weight boxes into L2 while the previous kernel of
     // the stream may still be running (a prefetch cannot read stale data).
+    int pn = cur_n, pc = cur_c;
     for (int k = 0; k < D && k < n_mine; ++k) {
-      const int64_t u = lo + warp + static_cast<int64_t>(k) * kWarps;
-      tc::tma_prefetch_l2_2d(&tmW, static_cast<int>((u / ch) % pl.n_tiles) * kTileN,
-                             static_cast<int>(u % ch) * kBoxRows);
+      tc::tma_prefetch_l2_2d(&tmW, pn * kTileN, pc * kBoxRows);
+      pc += kWarps;
+      while (pc >= ch) {
+        pc -= ch;
+        if (++pn == pl.n_tiles) pn = 0;
+      }
     }
   }
   // Everything below reads inputs or writes outputs and workspace that
@@ -451,12 +496,15 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[s], (k / D) & 1, abort, err, kSiteGemmMma));
       if (!ok) break;
       const uint8_t* slot = ring + s * C::kSlotBytes;
-      consume_unit<BITS, MT>(acc, slot, slot + kWBytes, g, c);
+      UnitRegs<BITS, MT> ur;
+      load_unit<BITS, MT>(ur, slot, slot + kWBytes, g, c);
       // The slot's next contents arrive through TMA (async proxy): order the
-      // warp's generic-proxy reads of the slot before lane 0 refills it.
+      // warp's generic-proxy reads of the slot before lane 0 refills it, and
+      // refill it before the math, so that the copy overlaps the math.
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && k + D < n_mine) issue(k + D);
+      compute_unit<BITS, MT>(acc, ur);
     }
 
     // Warp w adds into buffer w % kRedBufs in round w / kRedBufs; the buffers
@@ -586,6 +634,10 @@ Plan make_plan(int M, int N, int K) {
   pl.units = static_cast<int64_t>(pl.tiles) * pl.chunks;
   const int64_t cap = static_cast<int64_t>(sm_count()) * ctas_per_sm<BITS, MT>();
   pl.grid = static_cast<int>(pl.units < cap ? pl.units : cap);
+  // Enough tiles to occupy at least half of the GPU: one CTA per tile, no
+  // split of K, so no hand-shake between CTAs (its round trips cost more than
+  // the SMs left idle).
+  if (2 * static_cast<int64_t>(pl.tiles) >= cap && pl.tiles <= cap) pl.grid = pl.tiles;
   pl.slots = 1;
   if (pl.tiles > kMaxSplitTiles) {  // too many tiles for the counter area: one CTA per tile, no split
     pl.grid = pl.tiles;
