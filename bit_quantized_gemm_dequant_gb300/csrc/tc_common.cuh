@@ -50,6 +50,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the
+// instruction (it wakes when the phase completes), instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait built on mbar_try_wait_sleep (same give-up rules as mbar_wait).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort, int* err_word,
+                                                int site, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (err_word) atomicCAS(err_word, 0, site);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Wait for the phase with `parity` to complete, giving up after `limit_ns`
 // (or at once when another role already gave up: *abort != 0).  On giving up
 // it records `site` in the device error word and raises *abort, so that every
@@ -101,6 +131,32 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
                : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+
+// All threads of every CTA of the cluster: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Load 16 bytes from the shared memory of CTA `rank` of this cluster, at the
+// offset where `local` sits in this CTA's shared memory.
+__device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
 }
 
 // Programmatic dependent launch: let the next kernel of the stream (if it was

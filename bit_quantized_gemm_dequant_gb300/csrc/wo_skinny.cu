@@ -116,8 +116,12 @@ __device__ __forceinline__ int swz(int o, int cpr) { return o ^ (((o >> 7) & (cp
 
 // Stream-K plan: U = tiles * chunks units over G CTAs; CTA b owns units
 // [b*U/G, (b+1)*U/G).
+// cluster > 1: the grid is tiles * cluster CTAs in clusters of that size;
+// CTA b's run is then chunks [r ch / S, (r + 1) ch / S) of tile b / S (r its
+// rank), and the cluster adds its partial tiles through distributed shared
+// memory instead of the workspace.
 struct Plan {
-  int n_tiles, tiles, chunks, grid, slots;
+  int n_tiles, tiles, chunks, grid, slots, cluster;
   int64_t units;
 };
 
@@ -191,11 +195,12 @@ __device__ __forceinline__ uint32_t int4_hi_pair(uint32_t u) {
   const uint32_t t = (u & 0x00F000F0u) | 0x64006400u;
   return h2_bits(__hfma2(bits_h2(t), bits_h2(0x2C002C00u), bits_h2(0xD480D480u)));  // 1/16, -72
 }
-// fp16 pair {1024 + (byte0 ^ 0x80), 1024 + (byte2 ^ 0x80)} -> minus 1152 = signed bytes.
-__device__ __forceinline__ uint32_t int8_pair(uint32_t u) {
-  const uint32_t t = (u & 0x00FF00FFu) ^ 0x64806480u;
-  return h2_bits(__hsub2(bits_h2(t), bits_h2(0x64806480u)));  // 1152 = 1024 + 128
-}
+// fp16 pair {1024 + (byte0 ^ 0x80), 1024 + (byte2 ^ 0x80)} = 1152 + the signed
+// bytes (exact).  The offset is not subtracted here: the MMA sums
+// (1152 + w) x, and one extra MMA per k step with a constant -1152 operand
+// (kInt8Offset) takes 1152 * sum(x) back out, in FP32.
+__device__ __forceinline__ uint32_t int8_pair(uint32_t u) { return (u & 0x00FF00FFu) ^ 0x64806480u; }
+constexpr uint32_t kInt8Offset = 0xE480E480u;  // fp16 pair {-1152, -1152}
 
 // One 16-k step: dequantize the thread's weight vectors and issue the MMAs.
 // INT4: wv[0], wv[1] = K-pair rows 2c, 2c + 1 of the step's 8 (k = 4c ..
@@ -312,7 +317,7 @@ __device__ __forceinline__ void load_unit(UnitRegs<BITS, MT>& u, const uint8_t* 
 
 // The math of one unit from registers.
 template <int BITS, int MT>
-__device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], const UnitRegs<BITS, MT>& u) {
+__device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], float (&corr)[MT][4], const UnitRegs<BITS, MT>& u) {
   if constexpr (BITS == kE4m3) {
     uint32_t xb[MT][2];
 #pragma unroll
@@ -333,6 +338,11 @@ __device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], const UnitR
         xb[mt][1] = u.x[(q * MT + mt) * 2 + 1];
       }
       wo_step<BITS, MT>(acc, u.w + kVec * q, xb);
+      if constexpr (BITS == kInt8) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          mma16816(corr[mt], kInt8Offset, kInt8Offset, kInt8Offset, kInt8Offset, xb[mt][0], xb[mt][1]);
+      }
     }
   }
 }
@@ -483,17 +493,20 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     const int seg = static_cast<int>(seg_end - u0);
     const int m_base = (T / pl.n_tiles) * C::kRows, n_base = (T % pl.n_tiles) * kTileN;
 
-    float acc[MT][8][4];
+    float acc[MT][8][4], corr[MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[mt][q][r] = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) corr[mt][r] = 0.0f;
+    }
 
     for (; ok && k < n_mine && warp + k * kWarps < i + seg; ++k) {
       const int s = warp * D + k % D;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[s], (k / D) & 1, abort, err, kSiteGemmMma));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait_sleep(&full[s], (k / D) & 1, abort, err, kSiteGemmMma));
       if (!ok) break;
       const uint8_t* slot = ring + s * C::kSlotBytes;
       UnitRegs<BITS, MT> ur;
@@ -504,7 +517,16 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && k + D < n_mine) issue(k + D);
-      compute_unit<BITS, MT>(acc, ur);
+      compute_unit<BITS, MT>(acc, corr, ur);
+    }
+    if constexpr (BITS == kInt8) {
+      // The correction is the same for every MMA row (weight column).
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[mt][q][r] += corr[mt][r];
     }
 
     // Warp w adds into buffer w % kRedBufs in round w / kRedBufs; the buffers
@@ -530,7 +552,28 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     // with other CTAs; their partial tiles go to the workspace now, and the
     // hand-shake with the other contributors waits for the end of the run,
     // so that it never stalls the stream.
-    if (tile_contributors(T, U, G, ch) == 1) {
+    if (pl.cluster > 1) {
+      // The cluster's CTAs each hold one part of this tile: publish the sum
+      // in `red` (buffer 0), then each CTA finishes a slice of the tile from
+      // all of them, adding in rank order.
+      for (int e = t; e < C::kOutF4; e += kThreads) {
+        float4 v = red[e];
+#pragma unroll
+        for (int q = 1; q < kRedBufs; ++q) v = f4add(v, red[q * C::kOutF4 + e]);
+        red[e] = v;
+      }
+      tc::cluster_sync_all();
+      const int S = pl.cluster, r = static_cast<int>(tc::cluster_ctarank());
+      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+      const int e1 = (r + 1) * C::kOutF4 / S;
+      for (int e = r * C::kOutF4 / S + t; e < e1; e += kThreads) {
+        if (!elem_live(e, rows_valid)) continue;
+        float4 sum = tc::ld_dsmem_f4(red + e, 0);
+        for (int q = 1; q < S; ++q) sum = f4add(sum, tc::ld_dsmem_f4(red + e, q));
+        store_elem<BITS>(p, e, m_base, n_base, sum);
+      }
+      tc::cluster_sync_all();  // no CTA leaves while another still reads it
+    } else if (tile_contributors(T, U, G, ch) == 1) {
       const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
       for (int e = t; e < C::kOutF4; e += kThreads) {
         if (!elem_live(e, rows_valid)) continue;
@@ -624,6 +667,33 @@ int ctas_per_sm() {
   return cached;
 }
 
+// Clusters of S of these CTAs that the GPU holds at once (0 when it holds
+// none or the query fails; not cached then).
+template <int BITS, int MT>
+int max_clusters(int S) {
+  static int cached[9] = {0};
+  if (S < 2 || S > 8) return 0;
+  if (cached[S] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<BITS, MT>::kSmemBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (configure_kernel<BITS, MT>() != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, wo_skinny_kernel<BITS, MT>, &cfg) != cudaSuccess || n < 1)
+      return 0;
+    cached[S] = n;
+  }
+  return cached[S];
+}
+
 template <int BITS, int MT>
 Plan make_plan(int M, int N, int K) {
   using C = Cfg<BITS, MT>;
@@ -639,6 +709,20 @@ Plan make_plan(int M, int N, int K) {
   // the SMs left idle).
   if (2 * static_cast<int64_t>(pl.tiles) >= cap && pl.tiles <= cap) pl.grid = pl.tiles;
   pl.slots = 1;
+  pl.cluster = 1;
+  // Fewer tiles: split each tile's K among a cluster of S CTAs that reduce
+  // through distributed shared memory (no workspace, no round trip through
+  // L2), if the clusters fit in one wave and cover at least half the GPU.
+  if (2 * static_cast<int64_t>(pl.tiles) < cap) {
+    for (int S = 8; S >= 2; S /= 2) {
+      const int64_t g = static_cast<int64_t>(pl.tiles) * S;
+      if (g <= cap && 2 * g >= cap && S <= pl.chunks && pl.tiles <= max_clusters<BITS, MT>(S)) {
+        pl.cluster = S;
+        pl.grid = static_cast<int>(g);
+        return pl;
+      }
+    }
+  }
   if (pl.tiles > kMaxSplitTiles) {  // too many tiles for the counter area: one CTA per tile, no split
     pl.grid = pl.tiles;
     return pl;
@@ -684,11 +768,18 @@ cudaError_t launch_variant(const SkinnyArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (pl.cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = pl.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   e = cudaLaunchKernelEx(&cfg, wo_skinny_kernel<BITS, MT>, tW, tX, a, pl, device_error_word());
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

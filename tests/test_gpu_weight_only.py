@@ -145,7 +145,7 @@ def test_w8a16_large_m_sampled(wq, M, K, N):
     assert_gemm_close(y[torch.from_numpy(rows).cuda()], _ref(8, case, rows), "fp16")
 
 
-@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 4096), (4, 1, 11008, 4096), (4, 64, 4096, 11008)])
+@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 512), (4, 1, 11008, 512), (4, 64, 4096, 11008)])
 def test_split_k_workspace_contract(wq, bits, M, K, N):
     """Split tiles need scratch; a call leaves the counter area (the first
     64 KiB) zero again, repeated calls are bit-identical (fixed reduction
@@ -173,10 +173,13 @@ def test_split_k_workspace_contract(wq, bits, M, K, N):
     assert st == wq.WQ_OK and site == 0
 
 
-@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 14336), (4, 1, 4096, 11008)])
+@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 14336), (4, 1, 4096, 11008), (8, 1, 4096, 4096),
+                                         (4, 16, 11008, 4096), (8, 9, 1000, 4000)])
 def test_whole_tile_shapes_need_no_workspace(wq, bits, M, K, N):
     """With at least half as many 128-column tiles as SMs each CTA owns whole
-    tiles: no split of K, no scratch, and the call runs without a workspace."""
+    tiles; with fewer, a cluster of CTAs splits each tile's K and adds the
+    parts in distributed shared memory.  Neither needs scratch, and the call
+    runs without a workspace."""
     op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
     assert wq.wq_workspace_size(op, M, N, K) == 0
     case = _case(bits, M, K, N, seed=6)
