@@ -23,11 +23,10 @@
 //               of a 512-byte chunk).  Each lane reads exactly the rows whose
 //               bytes it then overwrites, so no lane waits on another.
 //   warp 1      TMEM allocator and MMA issuer: per stage, six tcgen05.cp
-//               32x128b.warpx4 (scale chunks -> TMEM) and eight
-//               tcgen05.mma 128 x 128 x 64 with scale_vec::2X (four K steps
-//               x two 128-column halves sharing the A tile and its scales),
-//               the scale byte pair chosen by the descriptor's scale-factor
-//               ids.
+//               32x128b.warpx4 (scale chunks -> TMEM) and four
+//               tcgen05.mma 128 x 256 x 64 with scale_vec::2X (one per K
+//               step; the A tile is read once per step), the scale byte pair
+//               chosen by the descriptor's scale-factor ids.
 //   warps 2-5   epilogue: tcgen05.ld and FP32 stores.
 // Scale arrays whose row stride is not a multiple of 16 bytes cannot be
 // described to TMA; for them the producer warp gathers the bytes with plain
@@ -208,20 +207,23 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t b = a + kABytes;
       const uint32_t sf = b + kBBytes;
       const uint32_t sf_col = tmem + kAccCols + s * kSfColsPerStage;
+      // Shared-memory chunk order: [A kb 0-3][A kb 4-7][W 0-127 kb 0-3]
+      // [W 0-127 kb 4-7][W 128-255 kb 0-3][W 128-255 kb 4-7].  In TMEM the two
+      // W halves of one block group sit side by side (columns +8, +12 for kb
+      // 0-3 and +16, +20 for kb 4-7): the N = 256 MMA reads the scale factors
+      // of W rows 128-255 four columns after those of rows 0-127.
 #pragma unroll
-      for (int c = 0; c < 6; ++c)  // A chunks 0-1, W rows 0-127 chunks 0-1, W rows 128-255 chunks 0-1
-        tc::tmem_cp_32x128b_warpx4(sf_col + 4 * c, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
+      for (int c = 0; c < 6; ++c) {
+        const int pos = (c == 3 || c == 4) ? 7 - c : c;  // chunk order 0, 1, 2, 4, 3, 5
+        tc::tmem_cp_32x128b_warpx4(sf_col + 4 * pos, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {  // 64 elements = 32 bytes per MMA
+      for (int j = 0; j < 4; ++j) {  // 64 elements = 32 bytes per MMA: 128 x 256 x 64
         const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
+        const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
         const uint32_t id = 2 * (j & 1);
-        const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, 128, id, id);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint64_t bdesc = tc::smem_desc(b + h * 128 * BKB + 32 * j, 1024, 1024, tc::kSwizzle128B);
-          tc::mma_mxf4(tmem + 128 * h, adesc, bdesc, idesc, sf_col + 4 * (j >> 1),
-                       sf_col + 8 + 8 * h + 4 * (j >> 1), (kt | j) != 0);
-        }
+        const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
+        tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), (kt | j) != 0);
       }
       tc::tc_commit(&empty[s]);
     }
