@@ -68,6 +68,7 @@ def test_per_row_and_per_block_scales(wq):
     (200, 300, 800, 400, 25, 400, 27, 304),         # ragged M/N/K, odd scale strides
     (130, 256, 8192, None, None, None, None, None),
     (384, 128, 4096, 2064, 130, 2048, 128, 132),
+    (300, 520, 1024, None, None, None, None, None),  # odd number of 128-row tiles, ragged N, TMA scales
 ])
 def test_random_quantized(wq, M, N, K, lda, ldsa, ldw, ldsw, ldc):
     a = workloads.mx_source(M, K, seed=M + K, stream=0)
