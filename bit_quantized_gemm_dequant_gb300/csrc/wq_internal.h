@@ -77,7 +77,7 @@ cudaError_t launch_fp8_skinny(const Fp8GemmArgs& a, void* ws, cudaStream_t s);
 int sm_count();
 
 // Built-in scratch of the allocation-free INT8 entry point (wo_skinny.cu).
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
 cudaError_t noalloc_scratch(void** ptr);  // device address on the current device
 size_t skinny_counter_bytes();            // leading counter area that must start at zero
 

@@ -122,12 +122,14 @@ int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx,
  * cudaFree after start-up, a runtime that plans every device byte ahead).
  * It computes exactly what wq_gemm_w8a16 computes, with the same arguments
  * minus the workspace, and allocates nothing: the split-K scratch of the
- * small-M path lives in a fixed 8 MiB array of device memory inside the
+ * small-M path lives in a fixed 1 MiB array of device memory inside the
  * library, which every GPU that loads the library holds until the process
  * exits.
  *
  *   - Shapes whose scratch need (wq_workspace_size(WQ_OP_W8A16, M, N, K))
- *     exceeds 8 MiB return WQ_ERR_WORKSPACE without launching.
+ *     exceeds 1 MiB return WQ_ERR_WORKSPACE without launching.  Only
+ *     shapes whose K is split across CTAs through scratch need any (small N
+ *     with long K); most decode shapes need none.
  *   - The first call on a device looks up the array's device address; make
  *     that first call before capturing the stream into a CUDA graph.
  *   - Each call clears the array's counter area on `stream` before its

@@ -37,7 +37,7 @@ def _noalloc(wq, x, w, s, y):
 
 # The first two shapes split K across CTAs and so use the built-in scratch;
 # the others need none (whole tiles per CTA, or a cluster per tile).
-@pytest.mark.parametrize("M,K,N", [(16, 4096, 512), (1, 8192, 1024), (16, 4096, 14336), (5, 1000, 3008)])
+@pytest.mark.parametrize("M,K,N", [(4, 4096, 512), (1, 8192, 1024), (16, 4096, 14336), (5, 1000, 3008)])
 def test_noalloc_matches_workspace_entry_point_twice(wq, M, K, N):
     case = workloads.w8a16_case(M, K, N, seed=21)
     x = torch.from_numpy(case.x).cuda()
@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_entry_point_twice(wq, M, K, N):
     s = torch.from_numpy(case.scales).cuda()
     need = wq.wq_workspace_size(wq.WQ_OP_W8A16, M, N, K)
     if N <= 1024:
-        assert need > 0  # these shapes do go through the scratch
+        assert 0 < need <= 1 << 20  # these shapes do go through the scratch, and fit it
     ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
     ref = wq.wq_gemm_w8a16(x, w, s, workspace=ws)
     for _ in range(2):
@@ -58,9 +58,9 @@ def test_noalloc_matches_workspace_entry_point_twice(wq, M, K, N):
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(wq):
-    """A shape whose split-K scratch exceeds the built-in 8 MiB is refused before launch."""
-    M, K, N = 64, 4096, 65536
-    assert wq.wq_workspace_size(wq.WQ_OP_W8A16, M, N, K) > 8 << 20
+    """A shape whose split-K scratch exceeds the built-in 1 MiB is refused before launch."""
+    M, K, N = 16, 16384, 1024
+    assert wq.wq_workspace_size(wq.WQ_OP_W8A16, M, N, K) > 1 << 20
     x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     w = torch.zeros((K, N), dtype=torch.int8, device="cuda")
     s = torch.ones(N, dtype=torch.float16, device="cuda")
