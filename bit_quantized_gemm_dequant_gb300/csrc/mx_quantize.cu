@@ -27,30 +27,49 @@ __device__ __forceinline__ uint32_t e2m1_code(float x, float inv_scale) {
   return (x < 0.0f ? 8u : 0u) | j;
 }
 
+// Element offsets of 32-element block `item` in the source, data and scale
+// arrays.  kDense: rows are packed back to back (every leading dimension is
+// the row length), so the block index alone gives them; otherwise the row is
+// found with a 32-bit division (the launcher keeps block counts below 2^31).
+template <bool kDense>
+__device__ __forceinline__ void block_offsets(const MxQuantArgs& p, uint32_t blocks_per_row, uint32_t item,
+                                              int64_t& src, int64_t& data, int64_t& sc) {
+  if (kDense) {
+    src = static_cast<int64_t>(item) * 32;
+    data = static_cast<int64_t>(item) * 16;
+    sc = item;
+  } else {
+    const uint32_t r = item / blocks_per_row, b = item - r * blocks_per_row;
+    src = static_cast<int64_t>(r) * p.ld_src + b * 32;
+    data = static_cast<int64_t>(r) * p.ld_data + b * 16;
+    sc = static_cast<int64_t>(r) * p.ld_scales + b;
+  }
+}
+
+template <bool kDense>
 __global__ void __launch_bounds__(kThreads, 3)
-mx_quantize_kernel(MxQuantArgs p, int64_t n_items) {
+mx_quantize_kernel(MxQuantArgs p, uint32_t n_items) {
   // A warp owns 8 consecutive blocks (1 KB of source) per step; the loop
   // bound is warp-uniform so that every lane reaches the quad shuffles.
   const int lane = threadIdx.x & 31;
   const int quad_lane = lane & 3;
-  const int64_t blocks_per_row = p.cols / 32;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  const int64_t step = n_warps * 8;
+  const uint32_t blocks_per_row = static_cast<uint32_t>(p.cols / 32);
+  const uint32_t warp0 = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const uint32_t step = ((gridDim.x * kThreads) >> 5) * 8;
 
-  for (int64_t base = warp0 * 8; base < n_items; base += step * kUnroll) {
+  for (uint32_t base = warp0 * 8; base < n_items; base += step * kUnroll) {
     float4 v[kUnroll][2];
-    int64_t item[kUnroll];
+    int64_t src[kUnroll], data[kUnroll], sc[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      item[u] = base + u * step + (lane >> 2);
-      if (item[u] < n_items) {
-        const int64_t r = item[u] / blocks_per_row;
-        const int64_t b = item[u] - r * blocks_per_row;
-        const float4* src = reinterpret_cast<const float4*>(p.src + r * p.ld_src + b * 32 + quad_lane * 8);
-        v[u][0] = __ldcs(src);
-        v[u][1] = __ldcs(src + 1);
+      const uint32_t item = base + u * step + (lane >> 2);
+      if (item < n_items) {
+        block_offsets<kDense>(p, blocks_per_row, item, src[u], data[u], sc[u]);
+        const float4* ps = reinterpret_cast<const float4*>(p.src + src[u] + quad_lane * 8);
+        v[u][0] = __ldcs(ps);
+        v[u][1] = __ldcs(ps + 1);
       } else {
+        src[u] = -1;
         v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
@@ -73,11 +92,9 @@ mx_quantize_kernel(MxQuantArgs p, int64_t n_items) {
       uint32_t word = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) word |= e2m1_code(xs[i], inv_scale) << (4 * i);
-      if (item[u] < n_items) {
-        const int64_t r = item[u] / blocks_per_row;
-        const int64_t b = item[u] - r * blocks_per_row;
-        *reinterpret_cast<uint32_t*>(p.data + r * p.ld_data + b * 16 + quad_lane * 4) = word;
-        if (quad_lane == 0) p.scales[r * p.ld_scales + b] = static_cast<uint8_t>(e + 127);
+      if (src[u] >= 0) {
+        __stcs(reinterpret_cast<unsigned int*>(p.data + data[u] + quad_lane * 4), word);
+        if (quad_lane == 0) p.scales[sc[u]] = static_cast<uint8_t>(e + 127);
       }
     }
   }
@@ -88,11 +105,16 @@ mx_quantize_kernel(MxQuantArgs p, int64_t n_items) {
 cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s) {
   const int64_t n_items = static_cast<int64_t>(a.rows) * (a.cols / 32);
   if (n_items == 0) return cudaSuccess;
+  // 32-bit block indices: under 2^31 blocks (a 256 GB source) the loop
+  // counter cannot wrap.
+  if (n_items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t blocks_per_cta = kThreads / 4;  // one 32-element block per thread quad
   int64_t ctas = (n_items + blocks_per_cta * kUnroll - 1) / (blocks_per_cta * kUnroll);
   const int64_t cap = static_cast<int64_t>(sm_count()) * 3;  // resident CTAs per SM (<= 85 registers)
   if (ctas > cap) ctas = cap;
-  mx_quantize_kernel<<<static_cast<unsigned>(ctas), kThreads, 0, s>>>(a, n_items);
+  const bool dense = a.ld_src == a.cols && a.ld_data == a.cols / 2 && a.ld_scales == a.cols / 32;
+  auto kern = dense ? mx_quantize_kernel<true> : mx_quantize_kernel<false>;
+  kern<<<static_cast<unsigned>(ctas), kThreads, 0, s>>>(a, static_cast<uint32_t>(n_items));
   return cudaGetLastError();
 }
 
