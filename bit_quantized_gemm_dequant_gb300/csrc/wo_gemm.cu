@@ -245,8 +245,19 @@ cudaError_t launch_tc(const WoArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Rows of X per CTA.  A CTA's time is set mostly by its K loop (weight
+// dequantization and the ring), not by its rows: a 128-row CTA takes about
+// 0.85x a 256-row one.  So take 128-row tiles, which use twice the SMs, when
+// they need no more waves (M = 512 at N = 4096: 128 CTAs instead of 64).
+int wo_gemm_rows(int M, int N) {
+  const int64_t sms = sm_count(), nt = (N + BN - 1) / BN;
+  auto waves = [&](int bm) { return (nt * ((M + bm - 1) / bm) + sms - 1) / sms; };
+  return waves(128) <= waves(256) ? 128 : 256;
+}
+
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
+  if (wo_gemm_rows(a.M, a.N) == 128) return bits == 4 ? launch_tc<4, 128>(a, s) : launch_tc<8, 128>(a, s);
   return bits == 4 ? launch_tc<4, 256>(a, s) : launch_tc<8, 256>(a, s);
 }
 
