@@ -55,6 +55,22 @@ constexpr int kThreads = 192;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 
 static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+
+// K splits: when the output tiles cannot fill half the GPU (M = 128 at
+// N = 8192: 32 tiles), split K so that tiles x splits fill it, keeping at
+// least four K steps per split.  The splits add their partial tiles into C
+// with FP32 reductions, so the order of those (at most 8) additions, and the
+// last bits of C, can differ from call to call.
+int mx_splits(int M, int N, int K) {
+  const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  const int kt = (K / 2 + BKB - 1) / BKB;
+  const int sms = sm_count();
+  if (2 * tiles >= sms) return 1;
+  int S = sms / tiles;
+  if (S > kt / 4) S = kt / 4;
+  if (S > 8) S = 8;
+  return S < 1 ? 1 : S;
+}
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
 // Gather 8 scale bytes (blocks kb0 .. kb0+7) of one row; rows or blocks
@@ -103,6 +119,14 @@ __device__ __forceinline__ void sf_to_chunks(uint8_t* sf, int h, int lane) {
           make_uint4(v[grp][half][0], v[grp][half][1], v[grp][half][2], v[grp][half][3]);
 }
 
+// Add four floats to C (16-byte aligned) in one reduction, without reading
+// them back.
+__device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+               : "memory");
+}
+
 template <bool kSfTma>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -120,7 +144,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int nkb = p.K / 32;
-  const int KT = (p.K / 2 + BKB - 1) / BKB;
+  // K steps [kt0, kt1) of this CTA: all of K, or split z of gridDim.z.
+  const int KT_all = (p.K / 2 + BKB - 1) / BKB;
+  const int kt0 = static_cast<int>(static_cast<int64_t>(blockIdx.z) * KT_all / gridDim.z);
+  const int kt1 = static_cast<int>(static_cast<int64_t>(blockIdx.z + 1) * KT_all / gridDim.z);
+  const int KT = kt1 - kt0;  // steps here; step kt0 + i uses ring slot i % kStages
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -155,9 +183,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const bool a4 = ((reinterpret_cast<uintptr_t>(p.SA) | static_cast<uintptr_t>(p.ldsa)) & 3) == 0;
     const bool w4 = ((reinterpret_cast<uintptr_t>(p.SW) | static_cast<uintptr_t>(p.ldsw)) & 3) == 0;
     int issued = 0;
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % kStages;
-      const bool free_slot = tc::mbar_wait(&empty[s], ((kt / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
+    for (int i = 0; i < KT; ++i) {
+      const int kt = kt0 + i, s = i % kStages;
+      const bool free_slot = tc::mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
       if (!__all_sync(0xffffffffu, free_slot)) break;  // warp-uniform exit
       uint8_t* st = smem + s * kStageBytes;
       uint8_t* sf = st + kABytes + kBBytes;
@@ -191,17 +219,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&full[s]);
       }
-      issued = kt + 1;
+      issued = i + 1;
     }
     if (*abort && lane == 0) {
-      for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
-        tc::mbar_wait_drain(&full[kt % kStages], (kt / kStages) & 1);
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        tc::mbar_wait_drain(&full[i % kStages], (i / kStages) & 1);
     }
   } else if (warp == 1 && lane == 0) {
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % kStages;
+    for (int i = 0; i < KT; ++i) {
+      const int s = i % kStages;
       uint64_t* ready = kSfTma ? &sf_ready[s] : &full[s];
-      if (!tc::mbar_wait(ready, (kt / kStages) & 1, abort, err, kSiteGemmMma)) break;
+      if (!tc::mbar_wait(ready, (i / kStages) & 1, abort, err, kSiteGemmMma)) break;
       tc::tc_fence_after();
       const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
       const uint32_t b = a + kABytes;
@@ -223,7 +251,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
         const uint32_t id = 2 * (j & 1);
         const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
-        tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), (kt | j) != 0);
+        tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), (i | j) != 0);
       }
       tc::tc_commit(&empty[s]);
     }
@@ -231,9 +259,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp >= 2) {
     if (kSfTma && warp == 2) {
       // Scale-layout duty during the main loop.
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kStages;
-        const bool ok = tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmMma);
+      for (int i = 0; i < KT; ++i) {
+        const int kt = kt0 + i, s = i % kStages;
+        const bool ok = tc::mbar_wait(&full[s], (i / kStages) & 1, abort, err, kSiteGemmMma);
         if (!__all_sync(0xffffffffu, ok)) break;
         sf_to_chunks(smem + s * kStageBytes + kABytes + kBBytes, kt & 1, lane);
         tc::fence_proxy_async_smem();  // chunk bytes -> visible to tcgen05.cp
@@ -244,12 +272,28 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const bool ok = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
     const int q = warp & 3;
-    const int row = m0 + 32 * q + lane;
+    const int row_l = 32 * q + lane, row = m0 + row_l;
+    // Split K (gridDim.z > 1): C was zeroed on the stream before the launch,
+    // and every split adds its FP32 partial tile into it.
+    const int S = gridDim.z;
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
       tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
       tc::tmem_ld_wait();
-      if (!ok || row >= p.M) continue;
+      if (!ok) continue;
+      if (S > 1) {
+        const int col0 = n0 + 32 * c;
+        if (row >= p.M || col0 >= p.N) continue;
+        float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+        if (col0 + 32 <= p.N) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) red_add_v4(dst + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        } else {
+          for (int t = 0; col0 + t < p.N; ++t) atomicAdd(dst + t, __uint_as_float(r[t]));
+        }
+        continue;
+      }
+      if (row >= p.M) continue;
       const int col0 = n0 + 32 * c;
       float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col0;
       if (col0 + 32 <= p.N) {
@@ -301,7 +345,12 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured[sf_tma] = true;
   }
-  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
+  const int splits = mx_splits(a.M, a.N, a.K);
+  if (splits > 1) {  // the splits add into C
+    e = cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
   kern<<<grid, kThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
   return cudaGetLastError();
 }

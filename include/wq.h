@@ -177,9 +177,15 @@ int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
  *            writes them.
  *   W, SW    the same for W [N, K] (row strides ldw, ldsw).
  *   C        fp32 [M, N] output, row stride ldc (elements).
- *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_MX_GEMM, M, N, K).
+ *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_MX_GEMM, M, N, K)
+ *            (currently 0 for every shape).
  * Alignment: A, W 16-byte aligned with lda, ldw multiples of 16; C 16-byte
  * aligned with ldc a multiple of 4.
+ * When the output tiles are too few to fill the GPU (small M), K is split
+ * across CTAs: C is zeroed on `stream` and each split adds its FP32 partial
+ * into it.  The order of those additions is not fixed, so the last bits of
+ * C may differ between two calls on the same inputs; larger M computes each
+ * output in one pass, in a fixed order.
  */
 int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
                 const uint8_t* SA, int64_t ldsa, const uint8_t* W,

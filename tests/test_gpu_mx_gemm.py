@@ -106,3 +106,26 @@ def test_k_zero(wq):
     wq.mx_gemm_fp4(e, e, f, f, c=c)
     torch.cuda.synchronize()
     assert torch.all(c == 0)
+
+
+def test_split_k_adds_into_c(wq):
+    """M = 128 at N = 8192 has too few tiles to fill the GPU, so K is split and
+    the splits add their partial tiles into C (zeroed first, inside the call).
+    No workspace is needed; repeated calls agree within the tolerance (the
+    order of the additions may differ), and C's previous contents do not
+    matter."""
+    M, N, K = 128, 8192, 4096
+    assert wq.wq_workspace_size(wq.WQ_OP_MX_GEMM, M, N, K) == 0
+    a = workloads.mx_source(M, K, seed=3, stream=0)
+    w = workloads.mx_source(N, K, seed=3, stream=1)
+    ad, asc = wq.mx_quantize_fp4(torch.from_numpy(a).cuda())
+    wd, wsc = wq.mx_quantize_fp4(torch.from_numpy(w).cuda())
+    c = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    wq.mx_gemm_fp4(ad, asc, wd, wsc, c=c)
+    c2 = wq.mx_gemm_fp4(ad, asc, wd, wsc)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 63, 127])
+    ref = O.mx_gemm_fp4(ad.cpu().numpy(), asc.cpu().numpy(), wd.cpu().numpy(), wsc.cpu().numpy(), rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    assert_gemm_close(c[idx], ref, "fp32")
+    assert_gemm_close(c2[idx], ref, "fp32")
