@@ -620,8 +620,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: " + ", ".join(f"{m}x{k}x{n}" for (m, k, n) in shapes),
-                   "parallelism": "host cores"},
+        "config": {"workload": f"{args.workload}: " + ", ".join(f"{spec['op']}_{m}x{k}x{n}" for (m, k, n) in shapes),
+                   "seed": 0, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
