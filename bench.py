@@ -209,11 +209,15 @@ def _hold_stream(torch, seconds):
 
 
 def _barrier_max(torch, value, ws):
+    """The largest of the ranks' values (the slowest rank's time); every rank
+    gets it.  The reduction tensor lives where the process group's backend
+    wants it: on the GPU for NCCL, on the host for gloo."""
     if ws == 1:
         return value
     import torch.distributed as dist
 
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    device = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
