@@ -146,17 +146,53 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// Load 16 bytes from the shared memory of CTA `rank` of this cluster, at the
-// offset where `local` sits in this CTA's shared memory.
-__device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) {
+// The shared::cluster address of `local`'s counterpart in CTA `rank` of the
+// cluster (the same offset in that CTA's shared memory).
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(ra)
+  return ra;
+}
+
+// Store 16 bytes into another CTA's shared memory at shared::cluster address
+// `dst`; the bytes count toward the transaction count of that CTA's mbarrier
+// at shared::cluster address `bar`.  The source is registers, so nothing of
+// the sending CTA stays in use after the instruction.
+__device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
                : "memory");
-  return v;
+}
+
+// try_wait with cluster-scope acquire: data that other CTAs of the cluster
+// delivered through the barrier's transaction count is visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for data sent by cluster peers.  It ignores the CTA's abort
+// flag: the peers send unconditionally, and this CTA must not leave while
+// their stores may still land in its shared memory.  Gives up (recording
+// `site`) only after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err_word, int site,
+                                                  uint64_t limit_ns = 4000000000ull) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (err_word) atomicCAS(err_word, 0, site);
+      return false;
+    }
+  }
 }
 
 // Programmatic dependent launch: let the next kernel of the stream (if it was

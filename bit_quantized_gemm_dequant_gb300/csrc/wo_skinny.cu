@@ -90,6 +90,14 @@ struct SkinnyArgs {
   void* ws;
 };
 
+// The deepest per-warp ring (2..8 slots) whose slots, one 8-byte barrier
+// each, and the fixed areas fit in the shared-memory budget.
+constexpr int ring_depth(int slot_bytes, int fixed_bytes) {
+  int d = 8;
+  while (d > 2 && kWarps * d * (slot_bytes + 8) + fixed_bytes > kSmemLimit) --d;
+  return d;
+}
+
 template <int BITS, int MT>
 struct Cfg {
   static constexpr int kChunkK = BITS == kInt4 ? 64 : 32;   // k per unit
@@ -100,9 +108,10 @@ struct Cfg {
   static constexpr int kSlotBytes = kWBytes + kXAlloc;      // 1 KB multiple: swizzle atoms stay aligned
   static constexpr int kOutF4 = MT * 8 * 32;                // float4 per partial tile (lane-native)
   static constexpr int kRedBytes = kRedBufs * kOutF4 * 16;
-  static constexpr int kFixedBytes = kRedBytes + 1024 + 64;  // + alignment slack, flags
-  // Units in flight per warp: three where they fit in shared memory, else two.
-  static constexpr int kDepth = kWarps * 3 * (kSlotBytes + 8) + kFixedBytes <= kSmemLimit ? 3 : 2;
+  static constexpr int kRxBytes = kOutF4 * 16;              // cluster peers' slices of the partial tile
+  static constexpr int kFixedBytes = kRedBytes + kRxBytes + 1024 + 64;  // + alignment slack, flags
+  // Units in flight per warp: as many as fit in shared memory (two to eight).
+  static constexpr int kDepth = ring_depth(kSlotBytes, kFixedBytes);
   static constexpr int kStages = kWarps * kDepth;
   static constexpr int kRingBytes = kStages * kSlotBytes;
   static constexpr size_t kSmemBytes = kRingBytes + kStages * 8 + kFixedBytes;
@@ -348,36 +357,49 @@ __device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], float (&cor
 }
 
 // Write two adjacent outputs (row gm, columns gn and gn + 1) of the final
-// result, skipping columns at or beyond N.
+// result, skipping columns at or beyond N; f = the factors of the two columns.
 template <int BITS>
-__device__ __forceinline__ void store_pair(const SkinnyArgs& p, int gm, int gn, float v0, float v1) {
+__device__ __forceinline__ void store_pair(const SkinnyArgs& p, int gm, int gn, float v0, float v1, float2 f) {
   if (gn >= p.N) return;
   const bool two = gn + 1 < p.N;
   if constexpr (BITS == kE4m3) {
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.Y) + static_cast<int64_t>(gm) * p.ldy + gn;
     if (two)
-      *reinterpret_cast<__nv_bfloat162*>(y) = __floats2bfloat162_rn(v0 * p.scale, v1 * p.scale);
+      *reinterpret_cast<__nv_bfloat162*>(y) = __floats2bfloat162_rn(v0 * f.x, v1 * f.y);
     else
-      *y = __float2bfloat16_rn(v0 * p.scale);
+      *y = __float2bfloat16_rn(v0 * f.x);
   } else {
-    const __half* S = static_cast<const __half*>(p.scales) + gn;
     __half* y = static_cast<__half*>(p.Y) + static_cast<int64_t>(gm) * p.ldy + gn;
     if (two)
-      *reinterpret_cast<__half2*>(y) = __floats2half2_rn(__half2float(S[0]) * v0, __half2float(S[1]) * v1);
+      *reinterpret_cast<__half2*>(y) = __floats2half2_rn(f.x * v0, f.y * v1);
     else
-      *y = __float2half_rn(__half2float(S[0]) * v0);
+      *y = __float2half_rn(f.x * v0);
   }
 }
 
 // Lane-native partial element e = (mt * 8 + q) * 32 + lane holds acc[mt][q]
 // of that lane: rows 8mt + 2c (.x, .z) and 8mt + 2c + 1 (.y, .w), columns
 // 16g + 2q (.x, .y) and 16g + 2q + 1 (.z, .w), with g = lane / 4, c = lane % 4.
+__device__ __forceinline__ int elem_col(int e) { return 16 * ((e & 31) >> 2) + 2 * ((e >> 5) & 7); }
+
+// The output factors of element e's two columns: the per-column scales
+// (weight-only) or scale_a * scale_b (e4m3); columns at or beyond N read 0.
 template <int BITS>
-__device__ __forceinline__ void store_elem(const SkinnyArgs& p, int e, int m_base, int n_base, float4 v) {
-  const int ln = e & 31, q = (e >> 5) & 7, mt = e >> 8;
-  const int gm = m_base + 8 * mt + 2 * (ln & 3), gn = n_base + 16 * (ln >> 2) + 2 * q;
-  if (gm < p.M) store_pair<BITS>(p, gm, gn, v.x, v.z);
-  if (gm + 1 < p.M) store_pair<BITS>(p, gm + 1, gn, v.y, v.w);
+__device__ __forceinline__ float2 elem_factors(const SkinnyArgs& p, int e, int n_base) {
+  if constexpr (BITS == kE4m3) {
+    return make_float2(p.scale, p.scale);
+  } else {
+    const int gn = n_base + elem_col(e);
+    const __half* S = static_cast<const __half*>(p.scales);
+    return make_float2(gn < p.N ? __half2float(S[gn]) : 0.0f, gn + 1 < p.N ? __half2float(S[gn + 1]) : 0.0f);
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ void store_elem(const SkinnyArgs& p, int e, int m_base, int n_base, float4 v, float2 f) {
+  const int gm = m_base + 8 * (e >> 8) + 2 * (e & 3), gn = n_base + elem_col(e);
+  if (gm < p.M) store_pair<BITS>(p, gm, gn, v.x, v.z, f);
+  if (gm + 1 < p.M) store_pair<BITS>(p, gm + 1, gn, v.y, v.w, f);
 }
 
 // Number of CTAs whose runs touch tile T.
@@ -402,13 +424,17 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                  Plan pl, int* err) {
   using C = Cfg<BITS, MT>;
   constexpr int D = C::kDepth;
+  constexpr int kFinElems = (C::kOutF4 + kThreads - 1) / kThreads;  // partial elements a thread finishes
+  constexpr bool kEarlyFactors = MT == 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* ring = smem;
   float4* red = reinterpret_cast<float4*>(smem + C::kRingBytes);  // [kRedBufs][kOutF4]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kRedBytes);
+  float4* rx = red + kRedBufs * C::kOutF4;  // [S][kOutF4 / S]: peer q's part of this CTA's slice at q
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kRedBytes + C::kRxBytes);
   volatile int* abort = reinterpret_cast<volatile int*>(full + C::kStages);
   volatile int* last_flag = abort + 1;  // [2]
+  uint64_t* rx_bar = reinterpret_cast<uint64_t*>(const_cast<int*>(abort) + 4);  // 8-byte aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -426,10 +452,18 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   tc::griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) tc::mbar_init(&full[s], 1);
+    if (pl.cluster > 1) tc::mbar_init(rx_bar, 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
   __syncthreads();
+  if (pl.cluster > 1) {
+    // The receive barrier expects the other CTAs' slices of this CTA's part of
+    // the tile; every CTA's barrier is armed before any CTA sends.
+    if (threadIdx.x == 0)
+      tc::mbar_arrive_expect_tx(rx_bar, static_cast<uint32_t>((pl.cluster - 1) * (C::kOutF4 / pl.cluster) * 16));
+    tc::cluster_sync_all();
+  }
 
   // Lane 0 of a warp starts the TMA loads of the warp's units in order; the
   // cursor (tile, chunk) of the next one advances by kWarps units at a time
@@ -492,6 +526,19 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                                                                              : lo + n_local;
     const int seg = static_cast<int>(seg_end - u0);
     const int m_base = (T / pl.n_tiles) * C::kRows, n_base = (T % pl.n_tiles) * kTileN;
+    // Elements this thread finishes if the tile ends here (the CTA's own tile,
+    // or its slice of a cluster's tile).  With one M tile of 8 rows their
+    // factors are loaded now, so that the epilogue does not wait on them after
+    // the stream; with 16 rows the registers are worth more to the main loop,
+    // and the factors are loaded at the end.
+    const int e_first = pl.cluster > 1 ? static_cast<int>(tc::cluster_ctarank()) * C::kOutF4 / pl.cluster + t : t;
+    float2 fac[kFinElems] = {};
+    if constexpr (kEarlyFactors) {
+#pragma unroll
+      for (int j = 0; j < kFinElems; ++j)
+        fac[j] = e_first + j * kThreads < C::kOutF4 ? elem_factors<BITS>(p, e_first + j * kThreads, n_base)
+                                                    : make_float2(0.0f, 0.0f);
+    }
 
     float acc[MT][8][4], corr[MT][4];
 #pragma unroll
@@ -553,34 +600,46 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     // hand-shake with the other contributors waits for the end of the run,
     // so that it never stalls the stream.
     if (pl.cluster > 1) {
-      // The cluster's CTAs each hold one part of this tile: publish the sum
-      // in `red` (buffer 0), then each CTA finishes a slice of the tile from
-      // all of them, adding in rank order.
-      for (int e = t; e < C::kOutF4; e += kThreads) {
-        float4 v = red[e];
-#pragma unroll
-        for (int q = 1; q < kRedBufs; ++q) v = f4add(v, red[q * C::kOutF4 + e]);
-        red[e] = v;
-      }
-      tc::cluster_sync_all();
+      // The cluster's CTAs each hold one part of this tile, and CTA q
+      // finishes slice q of it.  Each CTA adds its four buffers and sends
+      // every other slice straight into the owner's receive area (one-way
+      // stores that count toward the owner's receive barrier); the owner
+      // then adds the S parts of its slice in rank order, so the result does
+      // not depend on arrival order.  No CTA reads another's shared memory,
+      // so none has to wait for its peers before leaving.
       const int S = pl.cluster, r = static_cast<int>(tc::cluster_ctarank());
-      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
-      const int e1 = (r + 1) * C::kOutF4 / S;
-      for (int e = r * C::kOutF4 / S + t; e < e1; e += kThreads) {
-        if (!elem_live(e, rows_valid)) continue;
-        float4 sum = tc::ld_dsmem_f4(red + e, 0);
-        for (int q = 1; q < S; ++q) sum = f4add(sum, tc::ld_dsmem_f4(red + e, q));
-        store_elem<BITS>(p, e, m_base, n_base, sum);
-      }
-      tc::cluster_sync_all();  // no CTA leaves while another still reads it
-    } else if (tile_contributors(T, U, G, ch) == 1) {
-      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+      const int slice = C::kOutF4 / S;
       for (int e = t; e < C::kOutF4; e += kThreads) {
-        if (!elem_live(e, rows_valid)) continue;
+        const int q = e / slice;
+        if (q == r) continue;
+        float4 v = red[e];
+#pragma unroll
+        for (int b2 = 1; b2 < kRedBufs; ++b2) v = f4add(v, red[b2 * C::kOutF4 + e]);
+        tc::st_async_f4(tc::dsmem_addr(rx + r * slice + (e - q * slice), q), v, tc::dsmem_addr(rx_bar, q));
+      }
+      if (t < slice) {
+        const int e = e_first;  // r * slice + t
+        float4 own = red[e];
+#pragma unroll
+        for (int b2 = 1; b2 < kRedBufs; ++b2) own = f4add(own, red[b2 * C::kOutF4 + e]);
+        const bool got = tc::mbar_wait_cluster(rx_bar, 0, err, kSiteClusterRecv);
+        const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+        if (got && elem_live(e, rows_valid)) {
+          float4 sum = r == 0 ? own : rx[t];
+          for (int q = 1; q < S; ++q) sum = f4add(sum, q == r ? own : rx[q * slice + t]);
+          store_elem<BITS>(p, e, m_base, n_base, sum, kEarlyFactors ? fac[0] : elem_factors<BITS>(p, e, n_base));
+        }
+      }
+    } else if (seg == ch || tile_contributors(T, U, G, ch) == 1) {  // the whole tile is in this run
+      const int rows_valid = p.M - m_base < C::kRows ? p.M - m_base : C::kRows;
+#pragma unroll
+      for (int j = 0; j < kFinElems; ++j) {
+        const int e = t + j * kThreads;
+        if (e >= C::kOutF4 || !elem_live(e, rows_valid)) continue;
         float4 v = red[e];
 #pragma unroll
         for (int q = 1; q < kRedBufs; ++q) v = f4add(v, red[q * C::kOutF4 + e]);
-        store_elem<BITS>(p, e, m_base, n_base, v);
+        store_elem<BITS>(p, e, m_base, n_base, v, kEarlyFactors ? fac[j] : elem_factors<BITS>(p, e, n_base));
       }
     } else {
       const int f0 = unit_owner(static_cast<int64_t>(T) * ch, U, G);
@@ -631,7 +690,7 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 #pragma unroll
           for (int q = 0; q < 8; ++q) sum = f4add(sum, v[q]);
         }
-        store_elem<BITS>(p, e, m_base, n_base, sum);
+        store_elem<BITS>(p, e, m_base, n_base, sum, elem_factors<BITS>(p, e, n_base));
       }
       if (t == 0) ws_count[T] = 0;  // ready for the next call
     }

@@ -20,6 +20,7 @@ enum ErrorSite : int {
   kSiteGemmMma = 2,        // MMA issuer waited too long for a full stage
   kSiteGemmEpilogue = 3,   // epilogue waited too long for the accumulator
   kSiteGemmTmemFree = 4,   // MMA issuer waited too long for the epilogue
+  kSiteClusterRecv = 5,    // a CTA waited too long for its cluster peers' partial sums
 };
 
 struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
