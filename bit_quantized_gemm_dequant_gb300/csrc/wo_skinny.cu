@@ -109,7 +109,8 @@ struct Cfg {
   static constexpr int kOutF4 = MT * 8 * 32;                // float4 per partial tile (lane-native)
   static constexpr int kRedBytes = kRedBufs * kOutF4 * 16;
   static constexpr int kRxBytes = kOutF4 * 16;              // cluster peers' slices of the partial tile
-  static constexpr int kFixedBytes = kRedBytes + kRxBytes + 1024 + 64;  // + alignment slack, flags
+  static constexpr int kFacBytes = kTileN * 4;              // the tile's output factors
+  static constexpr int kFixedBytes = kRedBytes + kRxBytes + kFacBytes + 1024 + 64;  // + alignment slack, flags
   // Units in flight per warp: as many as fit in shared memory (two to eight).
   static constexpr int kDepth = ring_depth(kSlotBytes, kFixedBytes);
   static constexpr int kStages = kWarps * kDepth;
@@ -425,13 +426,14 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   using C = Cfg<BITS, MT>;
   constexpr int D = C::kDepth;
   constexpr int kFinElems = (C::kOutF4 + kThreads - 1) / kThreads;  // partial elements a thread finishes
-  constexpr bool kEarlyFactors = MT == 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* ring = smem;
   float4* red = reinterpret_cast<float4*>(smem + C::kRingBytes);  // [kRedBufs][kOutF4]
   float4* rx = red + kRedBufs * C::kOutF4;  // [S][kOutF4 / S]: peer q's part of this CTA's slice at q
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kRedBytes + C::kRxBytes);
+  float* col_fac = reinterpret_cast<float*>(rx + C::kOutF4);  // [kTileN]
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kRedBytes + C::kRxBytes + C::kFacBytes);
   volatile int* abort = reinterpret_cast<volatile int*>(full + C::kStages);
   volatile int* last_flag = abort + 1;  // [2]
   uint64_t* rx_bar = reinterpret_cast<uint64_t*>(const_cast<int*>(abort) + 4);  // 8-byte aligned
@@ -518,6 +520,14 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   int k = 0;  // the warp's next unit to consume
   bool ok = true;
   int pend0 = -1, pend1 = -1;  // shared tiles of this run (its first and last segment at most)
+  const bool stage_fac = BITS != kE4m3 && (pl.cluster > 1 || pl.grid == pl.tiles);
+  int fac_n_base = 0;  // n_base of the staged factors
+  // Factors of element e's two columns in the current tile.
+  auto fin_factors = [&](int e) {
+    if (!stage_fac) return elem_factors<BITS>(p, e, fac_n_base);
+    const int col = elem_col(e);
+    return make_float2(col_fac[col], col_fac[col + 1]);
+  };
   // One segment per tile the CTA's run touches.
   for (int i = 0; i < n_local;) {
     const int64_t u0 = lo + i;
@@ -526,18 +536,16 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                                                                              : lo + n_local;
     const int seg = static_cast<int>(seg_end - u0);
     const int m_base = (T / pl.n_tiles) * C::kRows, n_base = (T % pl.n_tiles) * kTileN;
-    // Elements this thread finishes if the tile ends here (the CTA's own tile,
-    // or its slice of a cluster's tile).  With one M tile of 8 rows their
-    // factors are loaded now, so that the epilogue does not wait on them after
-    // the stream; with 16 rows the registers are worth more to the main loop,
-    // and the factors are loaded at the end.
+    fac_n_base = n_base;
+    // The first element this thread finishes if the tile ends here (the CTA's
+    // own tile, or its slice of a cluster's tile).
     const int e_first = pl.cluster > 1 ? static_cast<int>(tc::cluster_ctarank()) * C::kOutF4 / pl.cluster + t : t;
-    float2 fac[kFinElems] = {};
-    if constexpr (kEarlyFactors) {
-#pragma unroll
-      for (int j = 0; j < kFinElems; ++j)
-        fac[j] = e_first + j * kThreads < C::kOutF4 ? elem_factors<BITS>(p, e_first + j * kThreads, n_base)
-                                                    : make_float2(0.0f, 0.0f);
+    // Plans with one segment per CTA stage the tile's per-column scales in
+    // shared memory now, while the first weight boxes are in flight, so that
+    // the epilogue does not wait on global loads after the stream.
+    if (stage_fac && t < kTileN) {
+      const int gn = n_base + t;
+      col_fac[t] = gn < p.N ? __half2float(static_cast<const __half*>(p.scales)[gn]) : 0.0f;
     }
 
     float acc[MT][8][4], corr[MT][4];
@@ -627,7 +635,7 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (got && elem_live(e, rows_valid)) {
           float4 sum = r == 0 ? own : rx[t];
           for (int q = 1; q < S; ++q) sum = f4add(sum, q == r ? own : rx[q * slice + t]);
-          store_elem<BITS>(p, e, m_base, n_base, sum, kEarlyFactors ? fac[0] : elem_factors<BITS>(p, e, n_base));
+          store_elem<BITS>(p, e, m_base, n_base, sum, fin_factors(e));
         }
       }
     } else if (seg == ch || tile_contributors(T, U, G, ch) == 1) {  // the whole tile is in this run
@@ -639,7 +647,7 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         float4 v = red[e];
 #pragma unroll
         for (int q = 1; q < kRedBufs; ++q) v = f4add(v, red[q * C::kOutF4 + e]);
-        store_elem<BITS>(p, e, m_base, n_base, v, kEarlyFactors ? fac[j] : elem_factors<BITS>(p, e, n_base));
+        store_elem<BITS>(p, e, m_base, n_base, v, fin_factors(e));
       }
     } else {
       const int f0 = unit_owner(static_cast<int64_t>(T) * ch, U, G);
