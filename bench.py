@@ -307,9 +307,9 @@ def time_calls_flushed(torch, wl, steps, warmup):
 # kernel source it was taken on is unchanged (same SHA-256); else the roofline
 # reports traffic null.
 CAPTURED_TRAFFIC = {
-    "w8a16_16x4096x14336": {"bytes": 58_916_608 + 92_672,
+    "w8a16_16x4096x14336": {"bytes": 58_923_008 + 90_368,
                             "source": "bit_quantized_gemm_dequant_gb300/csrc/wo_skinny.cu",
-                            "sha256": "e4cf046bf1e23d538f4ad848eb548441a321e460ad1fc6d41ce2a64a262d78f5",
+                            "sha256": "782b4d22380f29824cf0b8febcbddfb232741c93387b53907e997ce0646d54da",
                             "profile": "profiles/wo_skinny_w8a16_16x4096x14336.md"},
 }
 
