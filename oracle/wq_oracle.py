@@ -98,6 +98,53 @@ def gemm_w8a16(x: np.ndarray, w: np.ndarray, scales: np.ndarray) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# Column-grouped scales and zero points (W8A16 page, "扩展说明": when N is
+# large several columns may share one scale, and a zero_point turns the
+# symmetric scheme asymmetric; W4A16 page §一, the naive dequantization
+# w = (w_int4 - zero_point) * scale)
+# --------------------------------------------------------------------------
+
+
+def dequant_grouped(q: np.ndarray, scales: np.ndarray, zeros, group_n: int, default_zero: int) -> np.ndarray:
+    """W[k, n] = (q[k, n] - z[n // group_n]) * s[n // group_n] in float64.
+
+    ``q`` are the integer codes ``[K, N]``.  Columns ``g*group_n ..
+    (g+1)*group_n - 1`` share scale ``s[g]`` and zero point ``z[g]``; the
+    last group may be short.  ``zeros=None`` is the symmetric scheme, with
+    the fixed zero point ``default_zero``.
+    """
+    q = np.asarray(q, dtype=np.int64)
+    n = q.shape[1]
+    g = np.arange(n) // int(group_n)
+    s = np.asarray(scales).astype(np.float64)[g]
+    z = np.full(n, default_zero, np.int64) if zeros is None else np.asarray(zeros).astype(np.int64)[g]
+    return (q - z[None, :]).astype(np.float64) * s[None, :]
+
+
+def gemm_w4a16_grouped(x: np.ndarray, wq: np.ndarray, scales: np.ndarray, zeros=None, group_n: int = 1) -> np.ndarray:
+    """Y[m, n] = sum_k x[m, k] * (q[k, n] - z[n // G]) * s[n // G], float64.
+
+    Packed INT4 codes as in ``unpack_int4``; ``zeros`` are integers (one per
+    column group) or None for the W4A16 page's fixed zero point 8.  With
+    ``group_n = 1`` and ``zeros=None`` this is ``gemm_w4a16``.
+    """
+    xf = np.asarray(x).astype(np.float64)
+    return xf @ dequant_grouped(unpack_int4(wq), scales, zeros, group_n, INT4_ZERO_POINT)
+
+
+def gemm_w8a16_grouped(x: np.ndarray, w: np.ndarray, scales: np.ndarray, zeros=None, group_n: int = 1) -> np.ndarray:
+    """Y[m, n] = sum_k x[m, k] * (q[k, n] - z[n // G]) * s[n // G], float64.
+
+    INT8 codes ``[K, N]``; ``zeros`` are integers (one per column group) or
+    None for the W8A16 page's symmetric scheme (zero point 0).  With
+    ``group_n = 1`` and ``zeros=None`` this is ``gemm_w8a16``.
+    """
+    xf = np.asarray(x).astype(np.float64)
+    q = np.asarray(w, dtype=np.int8).astype(np.int64)
+    return xf @ dequant_grouped(q, scales, zeros, group_n, 0)
+
+
+# --------------------------------------------------------------------------
 # MXFP4 (MXFP4 page: micro-block format, §二 equations, §三 simulator)
 # --------------------------------------------------------------------------
 

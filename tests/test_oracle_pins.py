@@ -120,6 +120,89 @@ def test_w8_full_int8_range_and_sign():
     assert y[0, 0] == -2.0
 
 
+# ------------------------------------------- grouped / asymmetric weight-only pins
+
+
+def check_grouped_worked(gemm4=None, gemm8=None):
+    gemm4 = gemm4 or O.gemm_w4a16_grouped
+    gemm8 = gemm8 or O.gemm_w8a16_grouped
+    g = _load("weight_only_grouped_worked.json")
+    a = g["w4a16"]
+    y = gemm4(np.array(a["x"], np.float16), np.array(a["w_bytes"], np.uint8), np.array(a["scales"], np.float16),
+              np.array(a["zeros"], np.uint8), a["group_n"])
+    np.testing.assert_array_equal(y, np.array(a["y"], np.float64))
+    b = g["w8a16"]
+    y = gemm8(np.array(b["x"], np.float16), np.array(b["w"], np.int8), np.array(b["scales"], np.float16),
+              np.array(b["zeros"], np.int8), b["group_n"])
+    np.testing.assert_array_equal(y, np.array(b["y"], np.float64))
+
+
+def test_grouped_worked_example():
+    check_grouped_worked()
+
+
+def _brute_grouped(x, codes, s, z, group_n):
+    m, k = x.shape
+    n = codes.shape[1]
+    out = np.zeros((m, n))
+    for i in range(m):
+        for j in range(n):
+            g = j // group_n
+            out[i, j] = float(sum(_frac(x[i, kk]) * (int(codes[kk, j]) - int(z[g])) * _frac(s[g]) for kk in range(k)))
+    return out
+
+
+def check_grouped_bruteforce(gemm4=None, gemm8=None):
+    gemm4 = gemm4 or O.gemm_w4a16_grouped
+    gemm8 = gemm8 or O.gemm_w8a16_grouped
+    rng = np.random.default_rng(11)
+    for group_n, n in ((3, 7), (1, 4), (7, 7)):
+        groups = -(-n // group_n)
+        x = rng.standard_normal((2, 48)).astype(np.float16)
+        s = rng.uniform(0.005, 0.02, groups).astype(np.float16)
+        codes4 = rng.integers(0, 16, (48, n))
+        wq = (codes4[0::2] | (codes4[1::2] << 4)).astype(np.uint8)
+        z4 = rng.integers(0, 16, groups).astype(np.uint8)
+        np.testing.assert_allclose(gemm4(x, wq, s, z4, group_n), _brute_grouped(x, codes4, s, z4, group_n),
+                                   rtol=1e-13, atol=1e-15)
+        w8 = rng.integers(-128, 128, (48, n)).astype(np.int8)
+        z8 = rng.integers(-128, 128, groups).astype(np.int8)
+        np.testing.assert_allclose(gemm8(x, w8, s, z8, group_n), _brute_grouped(x, w8, s, z8, group_n),
+                                   rtol=1e-13, atol=1e-15)
+
+
+def test_grouped_bruteforce_exact_rational():
+    check_grouped_bruteforce()
+
+
+def test_grouped_reduces_to_per_column_symmetric():
+    """One column per group and no zero points is the per-column symmetric GEMM
+    (pinned above); a constant zero point equal to the fixed one is too."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((3, 32)).astype(np.float16)
+    wq = rng.integers(0, 256, (16, 6), dtype=np.uint8)
+    w8 = rng.integers(-128, 128, (32, 6)).astype(np.int8)
+    s = rng.uniform(0.005, 0.02, 6).astype(np.float16)
+    np.testing.assert_array_equal(O.gemm_w4a16_grouped(x, wq, s), O.gemm_w4a16(x, wq, s))
+    np.testing.assert_array_equal(O.gemm_w4a16_grouped(x, wq, s, np.full(6, 8, np.uint8), 1), O.gemm_w4a16(x, wq, s))
+    np.testing.assert_array_equal(O.gemm_w8a16_grouped(x, w8, s), O.gemm_w8a16(x, w8, s))
+    np.testing.assert_array_equal(O.gemm_w8a16_grouped(x, w8, s, np.zeros(6, np.int8), 1), O.gemm_w8a16(x, w8, s))
+
+
+def test_grouped_zero_point_is_a_rank_one_correction():
+    """(q - z) s = q s - z s: the zero point subtracts z[g] s[g] sum_k x[m, k]
+    from every column of group g (an invariant of the definition)."""
+    rng = np.random.default_rng(13)
+    x = rng.integers(-3, 4, (2, 16)).astype(np.float16)
+    w8 = rng.integers(-128, 128, (16, 5)).astype(np.int8)
+    s = np.array([0.5, 0.25], np.float16)
+    z = np.array([7, -9], np.int8)
+    g = np.arange(5) // 3
+    expect = O.gemm_w8a16_grouped(x, w8, s, None, 3) - np.outer(x.astype(np.float64).sum(1),
+                                                                 z.astype(np.float64)[g] * s.astype(np.float64)[g])
+    np.testing.assert_array_equal(O.gemm_w8a16_grouped(x, w8, s, z, 3), expect)
+
+
 # ------------------------------------------------------------------ MXFP4 pins
 
 
@@ -438,6 +521,43 @@ def _mutant_fp8_no_subnormals(a, b, sa, sb, rows=None):
     da = O.e4m3_decode(a)
     da = np.where((np.asarray(a) & 0x78) == 0, 0.0, da)
     return (da @ O.e4m3_decode(b)) * sa * sb
+
+
+def _mutant_grouped_zero_sign(x, w, s, z=None, group_n=1, four=False):
+    q = O.unpack_int4(w) if four else np.asarray(w, np.int8).astype(np.int64)
+    g = np.arange(q.shape[1]) // group_n
+    zz = np.full(q.shape[1], 8 if four else 0) if z is None else np.asarray(z).astype(np.int64)[g]
+    return x.astype(np.float64) @ ((q + zz) * s.astype(np.float64)[g])
+
+
+def _mutant_grouped_interleaved(x, w, s, z=None, group_n=1, four=False):
+    q = O.unpack_int4(w) if four else np.asarray(w, np.int8).astype(np.int64)
+    groups = -(-q.shape[1] // group_n)
+    g = np.arange(q.shape[1]) % groups  # columns dealt round-robin instead of in runs
+    zz = np.full(q.shape[1], 8 if four else 0) if z is None else np.asarray(z).astype(np.int64)[g]
+    return x.astype(np.float64) @ ((q - zz) * s.astype(np.float64)[g])
+
+
+def _mutant_grouped_k_axis(x, w, s, z=None, group_n=1, four=False):
+    q = O.unpack_int4(w) if four else np.asarray(w, np.int8).astype(np.int64)
+    g = np.minimum(np.arange(q.shape[0]) // group_n, len(s) - 1)  # grouped along K instead of N
+    zz = np.full(q.shape[0], 8 if four else 0) if z is None else np.asarray(z).astype(np.int64)[g]
+    return x.astype(np.float64) @ ((q - zz[:, None]) * s.astype(np.float64)[g][:, None])
+
+
+@pytest.mark.parametrize("mutant", [_mutant_grouped_zero_sign, _mutant_grouped_interleaved, _mutant_grouped_k_axis])
+@pytest.mark.parametrize("which", ["w4", "w8"])
+def test_grouped_pins_catch_planted_mistakes(mutant, which):
+    four = which == "w4"
+    g4 = (lambda *a: mutant(*a, four=True)) if four else O.gemm_w4a16_grouped
+    g8 = O.gemm_w8a16_grouped if four else (lambda *a: mutant(*a, four=False))
+    caught = 0
+    for check in (check_grouped_worked, check_grouped_bruteforce):
+        try:
+            check(g4, g8)
+        except AssertionError:
+            caught += 1
+    assert caught >= 1
 
 
 @pytest.mark.parametrize("mutant,checks", [
