@@ -64,54 +64,82 @@ def load_peaks():
 # HBM-bound, TFLOP/s otherwise.
 
 
-def _wo_bytes(bits, M, K, N):
-    return (K * N // 2 if bits == 4 else K * N) + 2 * N + 2 * M * K + 2 * M * N
+def _wo_bytes(bits, M, K, N, group_n=1, asym=False):
+    groups = -(-N // group_n)
+    return (K * N // 2 if bits == 4 else K * N) + 2 * groups + (groups if asym else 0) + 2 * M * K + 2 * M * N
+
+
+def _wo_tag(bits, group_n=None, asym=False):
+    """Call-name prefix of a weight-only workload, shared by both bench arms."""
+    return ("w4a16" if bits == 4 else "w8a16") + (f"_g{group_n}" + ("zp" if asym else "") if group_n else "")
 
 
 class WeightOnly:
-    def __init__(self, torch, wq, bits, shapes, replicas, seed=0):
-        self.torch, self.bits = torch, bits
-        self.cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, seed)
-                      for (M, K, N) in shapes]
-        self.fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+    """Weight-only GEMMs; with ``group_n`` the column-grouped entry points
+    (one scale, and with ``asym`` one zero point, per group of columns)."""
+
+    def __init__(self, torch, wq, bits, shapes, replicas, seed=0, group_n=None, asym=False):
+        self.torch, self.bits, self.group_n, self.asym = torch, bits, group_n, asym
+        if group_n:
+            self.cases = [workloads.grouped_case(bits, M, K, N, group_n, asym, seed) for (M, K, N) in shapes]
+            self.fn = wq.wq_gemm_w4a16_grouped if bits == 4 else wq.wq_gemm_w8a16_grouped
+        else:
+            self.cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, seed)
+                          for (M, K, N) in shapes]
+            self.fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
         self.dev = []
         for _ in range(replicas):
             reps = []
             for c in self.cases:
+                z = getattr(c, "zeros", None)
                 reps.append((torch.from_numpy(c.x).cuda(), torch.from_numpy(c.w).cuda(),
                              torch.from_numpy(c.scales).cuda(),
-                             torch.empty((c.x.shape[0], c.w.shape[1]), dtype=torch.float16, device="cuda")))
+                             torch.empty((c.x.shape[0], c.w.shape[1]), dtype=torch.float16, device="cuda"),
+                             torch.from_numpy(z).cuda() if z is not None else None))
             self.dev.append(reps)
         # One zero-filled workspace serves every call: they run one after the
         # other on one stream and each leaves it zero-filled.
         op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
         need = max(wq.wq_workspace_size(op, M, N, K) for (M, K, N) in shapes)
         self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
-        tag = "w4a16" if bits == 4 else "w8a16"
+        tag = _wo_tag(bits, group_n, asym)
         self.calls = []
         for i, (M, K, N) in enumerate(shapes):
-            self.calls.append({"call": f"{tag}_{M}x{K}x{N}", "index": i, "bytes": _wo_bytes(bits, M, K, N),
+            self.calls.append({"call": f"{tag}_{M}x{K}x{N}", "index": i,
+                               "bytes": _wo_bytes(bits, M, K, N, group_n or 1, asym),
                                "flops": 2 * M * N * K, "bound": "hbm" if M <= 64 else "tensor", "dtype": "fp16"})
 
+    def _call(self, x, w, s, z, y=None):
+        if self.group_n:
+            return self.fn(x, w, s, z, self.group_n, y=y, workspace=self.ws)
+        return self.fn(x, w, s, y=y, workspace=self.ws)
+
     def run(self, r, i):
-        x, w, s, y = self.dev[r][i]
-        self.fn(x, w, s, y=y, workspace=self.ws)
+        x, w, s, y, z = self.dev[r][i]
+        self._call(x, w, s, z, y)
 
     def host_inputs(self):
-        return [tuple(self.torch.from_numpy(a).pin_memory() for a in (c.x, c.w, c.scales)) for c in self.cases]
+        out = []
+        for c in self.cases:
+            arrs = [c.x, c.w, c.scales] + ([c.zeros] if getattr(c, "zeros", None) is not None else [])
+            out.append(tuple(self.torch.from_numpy(a).pin_memory() for a in arrs))
+        return out
 
     def e2e_call(self, host, i):
-        hx, hw, hs = host[i]
-        y = self.fn(hx.to("cuda", non_blocking=True), hw.to("cuda", non_blocking=True),
-                    hs.to("cuda", non_blocking=True))
+        dev = [a.to("cuda", non_blocking=True) for a in host[i]]
+        y = self._call(dev[0], dev[1], dev[2], dev[3] if len(dev) > 3 else None)
         y.to("cpu", non_blocking=True)
-        return sum(a.numel() * a.element_size() for a in (hx, hw, hs)), y.numel() * y.element_size()
+        return sum(a.numel() * a.element_size() for a in host[i]), y.numel() * y.element_size()
 
     def oracle_call(self, i):
         from oracle import wq_oracle as O
 
         c = self.cases[i]
-        (O.gemm_w4a16 if self.bits == 4 else O.gemm_w8a16)(c.x, c.w, c.scales)
+        if self.group_n:
+            (O.gemm_w4a16_grouped if self.bits == 4 else O.gemm_w8a16_grouped)(c.x, c.w, c.scales, c.zeros,
+                                                                               c.group_n)
+        else:
+            (O.gemm_w4a16 if self.bits == 4 else O.gemm_w8a16)(c.x, c.w, c.scales)
         return self.calls[i]["bytes"], self.calls[i]["flops"]
 
 
@@ -180,7 +208,8 @@ def make_workload(torch, wq, name, replicas, only=None):
     spec = workloads.WORKLOADS[name]
     shapes = spec["shapes"]
     if spec["op"] in ("w4a16", "w8a16"):
-        wl = WeightOnly(torch, wq, 4 if spec["op"] == "w4a16" else 8, shapes, replicas)
+        wl = WeightOnly(torch, wq, 4 if spec["op"] == "w4a16" else 8, shapes, replicas,
+                        group_n=spec.get("group_n"), asym=spec.get("asym", False))
     elif spec["op"] == "mxfp4":
         wl = MxFp4(torch, wq, shapes, replicas)
     else:
@@ -536,7 +565,7 @@ def run_ours(args):
 
     breakdown = []
     if not args.no_breakdown and rank == 0:
-        for name in ("w4a16_llama7b", "mxfp4", "fp8"):
+        for name in ("w4a16_llama7b", "w8a16_grouped_decode", "mxfp4", "fp8"):
             if name == args.workload:
                 continue
             other = make_workload(torch, wq, name, 1)
@@ -604,18 +633,29 @@ def run_reference(args):
 
     bits = 4 if spec["op"] == "w4a16" else 8
     shapes = spec["shapes"]
-    cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, 0) for (M, K, N) in shapes]
-    fn = O.gemm_w4a16 if bits == 4 else O.gemm_w8a16
+    group_n, asym = spec.get("group_n"), spec.get("asym", False)
+    if group_n:
+        cases = [workloads.grouped_case(bits, M, K, N, group_n, asym, 0) for (M, K, N) in shapes]
+        gfn = O.gemm_w4a16_grouped if bits == 4 else O.gemm_w8a16_grouped
+
+        def fn(c):
+            return gfn(c.x, c.w, c.scales, c.zeros, c.group_n)
+    else:
+        cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, 0) for (M, K, N) in shapes]
+        pfn = O.gemm_w4a16 if bits == 4 else O.gemm_w8a16
+
+        def fn(c):
+            return pfn(c.x, c.w, c.scales)
     # A bounded sample of the workload per step: the first `per_step` calls.
     per_step = len(cases) if args.steps + args.warmup <= 4 else 2
-    sample_bytes = sum(_wo_bytes(bits, *shapes[i]) for i in range(per_step))
+    sample_bytes = sum(_wo_bytes(bits, *shapes[i], group_n or 1, asym) for i in range(per_step))
     for _ in range(args.warmup):
         for c in cases[:per_step]:
-            fn(c.x, c.w, c.scales)
+            fn(c)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         for c in cases[:per_step]:
-            fn(c.x, c.w, c.scales)
+            fn(c)
     dt = time.perf_counter() - t0
     value = sample_bytes * args.steps / dt / 1e9
     sample = f"first {per_step} call(s) of the workload per step: " + ", ".join(
@@ -624,7 +664,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: " + ", ".join(f"{spec['op']}_{m}x{k}x{n}" for (m, k, n) in shapes),
+        "config": {"workload": f"{args.workload}: " + ", ".join(f"{_wo_tag(bits, group_n, asym)}_{m}x{k}x{n}"
+                                                                for (m, k, n) in shapes),
                    "seed": 0, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},

@@ -40,6 +40,8 @@ _SIGS = {
     "wq_gemm_w4a16": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
     "wq_gemm_w8a16": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
     "wq_gemm_w8a16_noalloc": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p],
+    "wq_gemm_w4a16_grouped": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i, _p, _i64, _p, _sz, _p],
+    "wq_gemm_w8a16_grouped": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i, _p, _i64, _p, _sz, _p],
     "mx_quantize_fp4": [_i, _i, _p, _i64, _p, _i64, _p, _i64, _p],
     "mx_gemm_fp4": [_i, _i, _i, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _sz, _p],
     "fp8_gemm": [_i, _i, _i, _p, _i64, _p, _i64, _f, _f, _p, _i64, _p, _sz, _p],
@@ -161,6 +163,33 @@ def wq_gemm_w8a16_noalloc(x, w, scales, y=None, stream=None):
     _check(lib.wq_gemm_w8a16_noalloc(M, N, K, _ptr(x), _ld(x), _ptr(w), _ld(w), _ptr(scales), _ptr(y), _ld(y),
                                      _stream(stream)), "wq_gemm_w8a16_noalloc")
     return y
+
+
+def _grouped(name, op, x, w, scales, zeros, group_n, y, workspace, stream):
+    import torch
+
+    M, K = x.shape
+    N = w.shape[1]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = auto_workspace(op, M, N, K, x.device)
+    wsp, wsb = _ws(workspace)
+    _check(getattr(lib, name)(M, N, K, _ptr(x), _ld(x), _ptr(w), _ld(w), _ptr(scales), _ptr(zeros), int(group_n),
+                              _ptr(y), _ld(y), wsp, wsb, _stream(stream)), name)
+    return y
+
+
+def wq_gemm_w4a16_grouped(x, wq, scales, zeros=None, group_n=1, y=None, workspace=None, stream=None):
+    """Y = X * ((unpack(wq) - z[n // group_n]) * scales[n // group_n]); zeros uint8
+    [ceil(N / group_n)] or None (zero point 8)."""
+    return _grouped("wq_gemm_w4a16_grouped", WQ_OP_W4A16, x, wq, scales, zeros, group_n, y, workspace, stream)
+
+
+def wq_gemm_w8a16_grouped(x, w, scales, zeros=None, group_n=1, y=None, workspace=None, stream=None):
+    """Y = X * ((w - z[n // group_n]) * scales[n // group_n]); zeros int8
+    [ceil(N / group_n)] or None (symmetric)."""
+    return _grouped("wq_gemm_w8a16_grouped", WQ_OP_W8A16, x, w, scales, zeros, group_n, y, workspace, stream)
 
 
 def mx_quantize_fp4(src, data=None, scales=None, stream=None):

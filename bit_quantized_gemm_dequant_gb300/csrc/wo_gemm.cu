@@ -25,6 +25,10 @@
 //               multiply by the per-column scale (exact to move out of the K
 //               sum: it is per column), round to fp16 and store; a warp writes
 //               32 consecutive columns of one row of Y per store.
+// Column-grouped scales and zero points ("Triton 量化算子：W8A16 权重量化融合矩
+// 阵乘法", 扩展说明): the scale of column n is scales[n / group_n], and a
+// zero point z replaces the fixed 8 (INT4) or 0 (INT8) in the constant each
+// thread subtracts for its own column.
 #include <cuda_fp16.h>
 
 #include "tc_common.cuh"
@@ -164,6 +168,17 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const int q = warp & 3;
     const int nl = 32 * q + lane;  // this thread's weight column inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    const int gn = n0 + nl;
+    // The fp16 constant the dequantization subtracts from 1024 + q (INT4) or
+    // 1152 + q (INT8): the fixed zero point, or this column's group zero point
+    // (1024 + z and 1152 + z are integers below 2048, exact in fp16).
+    uint32_t sub = BITS == 4 ? 0x64086408u : 0x64806480u;
+    if (p.zeros != nullptr && gn < p.N) {
+      const int g = gn / p.group_n;
+      const uint32_t z = BITS == 4 ? static_cast<uint32_t>(static_cast<const uint8_t*>(p.zeros)[g])
+                                   : static_cast<uint32_t>(static_cast<int>(static_cast<const int8_t*>(p.zeros)[g]) + 128);
+      sub = (0x6400u | z) * 0x10001u;
+    }
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % kStages, t = kt % kAStages;
       bool ok = tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmProducer);
@@ -176,13 +191,13 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         for (int c = 0; c < 32; ++c) {
           const uint32_t b = wt[c * BN];  // codes of k = 2c (low nibble), 2c + 1
           const uint32_t v = ((b * 0x1001u) & 0x000F000Fu) | 0x64006400u;
-          r[c] = h2_sub(v, 0x64086408u);  // minus 1032
+          r[c] = h2_sub(v, sub);  // minus 1024 + zero point
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const uint32_t b = static_cast<uint32_t>(wt[(2 * c) * BN]) | (static_cast<uint32_t>(wt[(2 * c + 1) * BN]) << 16);
-          r[c] = h2_sub((b ^ 0x00800080u) | 0x64006400u, 0x64806480u);  // minus 1152
+          r[c] = h2_sub((b ^ 0x00800080u) | 0x64006400u, sub);  // minus 1152 + zero point
         }
       }
       tc::fence_proxy_async_smem();  // generic reads of the tile before its TMA refill
@@ -197,8 +212,7 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     const bool done = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
-    const int gn = n0 + nl;
-    const float sc = (gn < p.N) ? __half2float(static_cast<const __half*>(p.scales)[gn]) : 0.0f;
+    const float sc = (gn < p.N) ? __half2float(static_cast<const __half*>(p.scales)[gn / p.group_n]) : 0.0f;
     __half* Y = static_cast<__half*>(p.Y);
     for (int c = 0; c < BM / 32; ++c) {
       uint32_t v[32];

@@ -88,6 +88,8 @@ struct SkinnyArgs {
   const void* scales; float scale;
   void* Y; int64_t ldy;
   void* ws;
+  const void* zeros;  // weight-only: one zero point per column group, or nullptr
+  int group_n;        // weight-only: columns per scale / zero-point group
 };
 
 // The deepest per-warp ring (2..8 slots) whose slots, one 8-byte barrier
@@ -109,7 +111,7 @@ struct Cfg {
   static constexpr int kOutF4 = MT * 8 * 32;                // float4 per partial tile (lane-native)
   static constexpr int kRedBytes = kRedBufs * kOutF4 * 16;
   static constexpr int kRxBytes = kOutF4 * 16;              // cluster peers' slices of the partial tile
-  static constexpr int kFacBytes = kTileN * 4;              // the tile's output factors
+  static constexpr int kFacBytes = 2 * kTileN * 4;          // the tile's output and zero-point factors
   static constexpr int kFixedBytes = kRedBytes + kRxBytes + kFacBytes + 1024 + 64;  // + alignment slack, flags
   // Units in flight per warp: as many as fit in shared memory (two to eight).
   static constexpr int kDepth = ring_depth(kSlotBytes, kFixedBytes);
@@ -211,6 +213,7 @@ __device__ __forceinline__ uint32_t int4_hi_pair(uint32_t u) {
 // (kInt8Offset) takes 1152 * sum(x) back out, in FP32.
 __device__ __forceinline__ uint32_t int8_pair(uint32_t u) { return (u & 0x00FF00FFu) ^ 0x64806480u; }
 constexpr uint32_t kInt8Offset = 0xE480E480u;  // fp16 pair {-1152, -1152}
+constexpr uint32_t kOnes = 0x3C003C00u;        // fp16 pair {1, 1}
 
 // One 16-k step: dequantize the thread's weight vectors and issue the MMAs.
 // INT4: wv[0], wv[1] = K-pair rows 2c, 2c + 1 of the step's 8 (k = 4c ..
@@ -325,8 +328,10 @@ __device__ __forceinline__ void load_unit(UnitRegs<BITS, MT>& u, const uint8_t* 
   }
 }
 
-// The math of one unit from registers.
-template <int BITS, int MT>
+// The math of one unit from registers.  kSumX (INT4 with zero points): one
+// extra MMA per k step against a constant 1.0 operand sums the activations
+// into corr, for the zero-point correction.
+template <int BITS, int MT, bool kSumX = false>
 __device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], float (&corr)[MT][4], const UnitRegs<BITS, MT>& u) {
   if constexpr (BITS == kE4m3) {
     uint32_t xb[MT][2];
@@ -352,6 +357,9 @@ __device__ __forceinline__ void compute_unit(float (&acc)[MT][8][4], float (&cor
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
           mma16816(corr[mt], kInt8Offset, kInt8Offset, kInt8Offset, kInt8Offset, xb[mt][0], xb[mt][1]);
+      } else if constexpr (kSumX) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) mma16816(corr[mt], kOnes, kOnes, kOnes, kOnes, xb[mt][0], xb[mt][1]);
       }
     }
   }
@@ -392,7 +400,8 @@ __device__ __forceinline__ float2 elem_factors(const SkinnyArgs& p, int e, int n
   } else {
     const int gn = n_base + elem_col(e);
     const __half* S = static_cast<const __half*>(p.scales);
-    return make_float2(gn < p.N ? __half2float(S[gn]) : 0.0f, gn + 1 < p.N ? __half2float(S[gn + 1]) : 0.0f);
+    return make_float2(gn < p.N ? __half2float(S[gn / p.group_n]) : 0.0f,
+                       gn + 1 < p.N ? __half2float(S[(gn + 1) / p.group_n]) : 0.0f);
   }
 }
 
@@ -419,7 +428,9 @@ __device__ __forceinline__ void cta_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
-template <int BITS, int MT>
+// kZp: the weight-only modes with zero points (a separate instance, so that
+// the symmetric kernels carry none of their code).
+template <int BITS, int MT, bool kZp>
 __global__ void __launch_bounds__(kThreads, 1)
 wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, SkinnyArgs p,
                  Plan pl, int* err) {
@@ -431,7 +442,8 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   uint8_t* ring = smem;
   float4* red = reinterpret_cast<float4*>(smem + C::kRingBytes);  // [kRedBufs][kOutF4]
   float4* rx = red + kRedBufs * C::kOutF4;  // [S][kOutF4 / S]: peer q's part of this CTA's slice at q
-  float* col_fac = reinterpret_cast<float*>(rx + C::kOutF4);  // [kTileN]
+  float* col_fac = reinterpret_cast<float*>(rx + C::kOutF4);  // [kTileN] output factors
+  float* col_zf = col_fac + kTileN;  // [kTileN] zero-point correction factors
   uint64_t* full =
       reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kRedBytes + C::kRxBytes + C::kFacBytes);
   volatile int* abort = reinterpret_cast<volatile int*>(full + C::kStages);
@@ -545,7 +557,23 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     // the epilogue does not wait on global loads after the stream.
     if (stage_fac && t < kTileN) {
       const int gn = n_base + t;
-      col_fac[t] = gn < p.N ? __half2float(static_cast<const __half*>(p.scales)[gn]) : 0.0f;
+      col_fac[t] = gn < p.N ? __half2float(static_cast<const __half*>(p.scales)[gn / p.group_n]) : 0.0f;
+    }
+    // With zero points, each column's factor for the activation-sum term:
+    // INT8 sums x (1152 + q) and corr holds -1152 sum x, so corr (1152 + z) /
+    // 1152 completes sum x (q - z); INT4 sums x (q - 8) and corr holds sum x,
+    // so corr (8 - z) does.
+    if (kZp && t < kTileN) {
+      const int gn = n_base + t;
+      float f = 0.0f;
+      if (gn < p.N) {
+        const int g = gn / p.group_n;
+        if constexpr (BITS == kInt8)
+          f = static_cast<float>(1152 + static_cast<const int8_t*>(p.zeros)[g]) * (1.0f / 1152.0f);
+        else
+          f = static_cast<float>(8 - static_cast<int>(static_cast<const uint8_t*>(p.zeros)[g]));
+      }
+      col_zf[t] = f;
     }
 
     float acc[MT][8][4], corr[MT][4];
@@ -572,9 +600,20 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && k + D < n_mine) issue(k + D);
-      compute_unit<BITS, MT>(acc, corr, ur);
+      compute_unit<BITS, MT, kZp && BITS == kInt4>(acc, corr, ur);
     }
-    if constexpr (BITS == kInt8) {
+    if constexpr (kZp) {
+      // Per-column zero points: corr times the column's factor (staged at the
+      // start of the segment; the barrier makes it visible).  acc[mt][q][r]
+      // is column 16g + 2q + r / 2 of the tile.
+      cta_sync();
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[mt][q][r] += corr[mt][r] * col_zf[16 * g + 2 * q + (r >> 1)];
+    } else if constexpr (BITS == kInt8) {
       // The correction is the same for every MMA row (weight column).
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -712,9 +751,9 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 
 // Opt the kernel into its dynamic shared memory (above the 48 KB default);
 // must precede both the occupancy query and the first launch.
-template <int BITS, int MT>
+template <int BITS, int MT, bool kZp = false>
 cudaError_t configure_kernel() {
-  static cudaError_t status = cudaFuncSetAttribute(wo_skinny_kernel<BITS, MT>,
+  static cudaError_t status = cudaFuncSetAttribute(wo_skinny_kernel<BITS, MT, kZp>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(Cfg<BITS, MT>::kSmemBytes));
   return status;
@@ -726,7 +765,7 @@ int ctas_per_sm() {
   if (cached == 0) {
     int n = 0;
     if (configure_kernel<BITS, MT>() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wo_skinny_kernel<BITS, MT>, kThreads,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wo_skinny_kernel<BITS, MT, false>, kThreads,
                                                       Cfg<BITS, MT>::kSmemBytes) != cudaSuccess || n < 1)
       return 1;  // not cached: a later call may succeed
     cached = n;
@@ -754,7 +793,7 @@ int max_clusters(int S) {
     cfg.numAttrs = 1;
     int n = 0;
     if (configure_kernel<BITS, MT>() != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, wo_skinny_kernel<BITS, MT>, &cfg) != cudaSuccess || n < 1)
+        cudaOccupancyMaxActiveClusters(&n, wo_skinny_kernel<BITS, MT, false>, &cfg) != cudaSuccess || n < 1)
       return 0;
     cached[S] = n;
   }
@@ -809,10 +848,10 @@ size_t plan_workspace(int M, int N, int K) {
   return kCounterBytes + static_cast<size_t>(pl.tiles) * pl.slots * Cfg<BITS, MT>::kOutF4 * 16;
 }
 
-template <int BITS, int MT>
+template <int BITS, int MT, bool kZp>
 cudaError_t launch_variant(const SkinnyArgs& a, cudaStream_t s) {
   using C = Cfg<BITS, MT>;
-  cudaError_t e = configure_kernel<BITS, MT>();
+  cudaError_t e = configure_kernel<BITS, MT, kZp>();
   if (e != cudaSuccess) return e;
   const Plan pl = make_plan<BITS, MT>(a.M, a.N, a.K);
   CUtensorMap tW, tX;
@@ -847,14 +886,18 @@ cudaError_t launch_variant(const SkinnyArgs& a, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  e = cudaLaunchKernelEx(&cfg, wo_skinny_kernel<BITS, MT>, tW, tX, a, pl, device_error_word());
+  e = cudaLaunchKernelEx(&cfg, wo_skinny_kernel<BITS, MT, kZp>, tW, tX, a, pl, device_error_word());
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int BITS>
 cudaError_t launch_mode(const SkinnyArgs& a, cudaStream_t s) {
-  return a.M > 8 ? launch_variant<BITS, 2>(a, s) : launch_variant<BITS, 1>(a, s);
+  if constexpr (BITS != kE4m3) {
+    if (a.zeros != nullptr)
+      return a.M > 8 ? launch_variant<BITS, 2, true>(a, s) : launch_variant<BITS, 1, true>(a, s);
+  }
+  return a.M > 8 ? launch_variant<BITS, 2, false>(a, s) : launch_variant<BITS, 1, false>(a, s);
 }
 
 template <int BITS>
@@ -873,13 +916,14 @@ size_t fp8_skinny_workspace(int M, int N, int K) { return mode_workspace<kE4m3>(
 
 cudaError_t launch_wo_skinny(const WoArgs& a, int bits, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
-  const SkinnyArgs sa{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, a.ws};
+  const SkinnyArgs sa{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, a.ws, a.zeros, a.group_n};
   return bits == 4 ? launch_mode<kInt4>(sa, s) : launch_mode<kInt8>(sa, s);
 }
 
 cudaError_t launch_fp8_skinny(const Fp8GemmArgs& a, void* ws, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.C, a.ldc * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
-  const SkinnyArgs sa{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, nullptr, a.scale_a * a.scale_b, a.C, a.ldc, ws};
+  const SkinnyArgs sa{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, nullptr, a.scale_a * a.scale_b, a.C, a.ldc, ws,
+                      nullptr, 1};
   return launch_mode<kE4m3>(sa, s);
 }
 

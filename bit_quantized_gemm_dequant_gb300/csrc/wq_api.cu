@@ -72,11 +72,12 @@ static size_t weight_only_workspace(int bits, int M, int N, int K) {
 }
 
 static int run_weight_only(int bits, int M, int N, int K, const void* X, int64_t ldx, const void* W, int64_t ldw,
-                           const void* scales, void* Y, int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s) {
+                           const void* scales, void* Y, int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s,
+                           const void* zeros = nullptr, int group_n = 1) {
   if (M == 0 || N == 0) return WQ_OK;
   const size_t need = weight_only_workspace(bits, M, N, K);
   if (ws_bytes < need || (need > 0 && (!ws || !aligned(ws, 16)))) return WQ_ERR_WORKSPACE;
-  WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy, ws, ws_bytes};
+  WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy, ws, ws_bytes, zeros, group_n};
   if (M <= kSkinnyMaxM) return launch_status(launch_wo_skinny(a, bits, s));
   return launch_status(launch_wo_gemm(a, bits, s));
 }
@@ -106,6 +107,29 @@ int wq_gemm_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t*
   if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
   return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, workspace, ws_bytes,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wq_gemm_w4a16_grouped(int M, int N, int K, const void* X, int64_t ldx, const uint8_t* Wq, int64_t ldw,
+                          const void* scales, const uint8_t* zeros, int group_n, void* Y, int64_t ldy,
+                          void* workspace, size_t ws_bytes, wq_stream_t stream) {
+  if (group_n < 1) return WQ_ERR_INVALID_ARG;
+  int st = check_weight_only(M, N, K, X, ldx, Wq, ldw, scales, Y, ldy);
+  if (st != WQ_OK || M == 0 || N == 0) return st;
+  if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
+  return run_weight_only(4, M, N, K, X, ldx, Wq, ldw, scales, Y, ldy, workspace, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream), zeros, group_n);
+}
+
+int wq_gemm_w8a16_grouped(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                          const void* scales, const int8_t* zeros, int group_n, void* Y, int64_t ldy,
+                          void* workspace, size_t ws_bytes, wq_stream_t stream) {
+  if (group_n < 1) return WQ_ERR_INVALID_ARG;
+  if (K % 2 && K > 0 && M >= 0 && N >= 0) return WQ_ERR_UNSUPPORTED;
+  int st = check_weight_only(M, N, K, X, ldx, W, ldw, scales, Y, ldy);
+  if (st != WQ_OK || M == 0 || N == 0) return st;
+  if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
+  return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, workspace, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream), zeros, group_n);
 }
 
 int wq_gemm_w8a16_noalloc(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,

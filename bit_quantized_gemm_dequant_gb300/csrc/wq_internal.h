@@ -30,6 +30,10 @@ struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
   const void* scales;
   void* Y; int64_t ldy;
   void* ws; size_t ws_bytes;  // caller scratch (split-K partial sums and tile counters)
+  // Column groups: scales[n / group_n]; zeros (uint8 for INT4, int8 for
+  // INT8, one per group) or nullptr for the fixed zero point (8 / 0).
+  const void* zeros = nullptr;
+  int group_n = 1;
 };
 
 struct MxQuantArgs {

@@ -142,6 +142,42 @@ int wq_gemm_w8a16_noalloc(int M, int N, int K, const void* X, int64_t ldx,
                           void* Y, int64_t ldy, wq_stream_t stream);
 
 /*
+ * wq_gemm_w4a16_grouped, wq_gemm_w8a16_grouped — weight-only GEMMs whose
+ * scales, and optional zero points, are shared by groups of columns.
+ *
+ * [W8A16] 扩展说明 (extensions): when N is large several columns may share one
+ * scale, and a zero_point turns the symmetric scheme asymmetric; [W4A16] §一:
+ * the dequantization w = (w_int4 - zero_point) * scale.  Columns
+ * g*group_n .. (g+1)*group_n - 1 share scale s[g] and zero point z[g] (the
+ * last group may be shorter):
+ *     Y[m, n] = sum_k X[m, k] * (q[k, n] - z[n / group_n]) * s[n / group_n],
+ * q being the INT4 code (0..15, unpacked as for wq_gemm_w4a16) or the INT8
+ * value.  Both factors are constant along K; the products accumulate in FP32
+ * and Y is stored as FP16.
+ *
+ *   group_n  columns per group, >= 1 (otherwise WQ_ERR_INVALID_ARG).
+ *   scales   fp16 [ceil(N / group_n)], 2-byte aligned.
+ *   zeros    NULL for the symmetric scheme (zero point 8 for INT4, 0 for
+ *            INT8), else [ceil(N / group_n)] zero points: uint8 for INT4 (any
+ *            value 0..255), int8 for INT8.
+ *   Every other argument, the workspace size (wq_workspace_size with
+ *   WQ_OP_W4A16 or WQ_OP_W8A16) and the alignment rules are those of
+ *   wq_gemm_w4a16 / wq_gemm_w8a16.
+ * group_n = 1 with zeros = NULL computes exactly what wq_gemm_w4a16 and
+ * wq_gemm_w8a16 compute.
+ */
+int wq_gemm_w4a16_grouped(int M, int N, int K, const void* X, int64_t ldx,
+                          const uint8_t* Wq, int64_t ldw, const void* scales,
+                          const uint8_t* zeros, int group_n,
+                          void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                          wq_stream_t stream);
+int wq_gemm_w8a16_grouped(int M, int N, int K, const void* X, int64_t ldx,
+                          const int8_t* W, int64_t ldw, const void* scales,
+                          const int8_t* zeros, int group_n,
+                          void* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                          wq_stream_t stream);
+
+/*
  * mx_quantize_fp4 — quantize FP32 rows to MXFP4 (E2M1 elements, E8M0 scales).
  *
  * [MXFP4] §三 simulator, per 32-element block of each row:

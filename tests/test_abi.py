@@ -24,6 +24,7 @@ def wq():
 def test_header_declares_the_five_entry_points(wq):
     names = wq.header_functions()
     for n in ("wq_gemm_w4a16", "wq_gemm_w8a16", "mx_quantize_fp4", "mx_gemm_fp4", "fp8_gemm",
+              "wq_gemm_w4a16_grouped", "wq_gemm_w8a16_grouped",
               "wq_workspace_size", "wq_status_string", "wq_get_device_error", "wq_version"):
         assert n in names
 
@@ -62,6 +63,24 @@ def test_weight_only_validation(wq):
     assert _w4(wq, ldx=68) == wq.WQ_ERR_MISALIGNED
     assert _w4(wq, M=0) == wq.WQ_OK and _w4(wq, N=0) == wq.WQ_OK   # empty: no launch
     assert wq.lib.wq_gemm_w8a16(4, 64, 63, FAKE, 64, FAKE, 64, FAKE, FAKE, 64, None, 0, None) == wq.WQ_ERR_UNSUPPORTED
+
+
+def _g(wq, bits=4, M=4, N=64, K=64, X=FAKE, ldx=64, W=FAKE, ldw=64, S=FAKE, Z=FAKE, G=8, Y=FAKE, ldy=64):
+    fn = wq.lib.wq_gemm_w4a16_grouped if bits == 4 else wq.lib.wq_gemm_w8a16_grouped
+    return fn(M, N, K, X, ldx, W, ldw, S, Z, G, Y, ldy, None, 0, None)
+
+
+def test_grouped_validation(wq):
+    for bits in (4, 8):
+        assert _g(wq, bits, G=0) == wq.WQ_ERR_INVALID_ARG      # a group has at least one column
+        assert _g(wq, bits, G=-3) == wq.WQ_ERR_INVALID_ARG
+        assert _g(wq, bits, X=0) == wq.WQ_ERR_INVALID_ARG
+        assert _g(wq, bits, S=0) == wq.WQ_ERR_INVALID_ARG
+        assert _g(wq, bits, ldw=32) == wq.WQ_ERR_INVALID_ARG
+        assert _g(wq, bits, X=FAKE + 2) == wq.WQ_ERR_MISALIGNED
+        assert _g(wq, bits, M=0) == wq.WQ_OK and _g(wq, bits, N=0) == wq.WQ_OK
+    assert _g(wq, 4, K=63) == wq.WQ_ERR_INVALID_ARG
+    assert _g(wq, 8, K=63) == wq.WQ_ERR_UNSUPPORTED
 
 
 def test_mx_and_fp8_validation(wq):

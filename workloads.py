@@ -73,6 +73,36 @@ def w8a16_case(m: int, k: int, n: int, seed: int = 0) -> WeightOnlyCase:
                           column_scales_fp16(n, 0.001, 0.01, seed), 8)
 
 
+_Z_STREAM = 5
+
+
+@dataclass
+class GroupedCase:
+    x: np.ndarray        # fp16 [M, K]
+    w: np.ndarray        # uint8 [K/2, N] (INT4) or int8 [K, N] (INT8)
+    scales: np.ndarray   # fp16 [ceil(N / group_n)]
+    zeros: object        # uint8 (INT4) / int8 (INT8) [ceil(N / group_n)], or None
+    group_n: int
+    bits: int
+
+
+def grouped_case(bits: int, m: int, k: int, n: int, group_n: int, asym: bool, seed: int = 0) -> GroupedCase:
+    """Weight-only case with column-grouped scales and optional zero points.
+    Codes and activations as in ``w4a16_case`` / ``w8a16_case``; one scale per
+    group of ``group_n`` columns (same ranges); zero points U{0..15} (INT4) or
+    U{-32..32} (INT8)."""
+    groups = -(-n // group_n)
+    base = w4a16_case(m, k, n, seed) if bits == 4 else w8a16_case(m, k, n, seed)
+    lo, hi = (0.005, 0.02) if bits == 4 else (0.001, 0.01)
+    scales = column_scales_fp16(groups, lo, hi, seed + 1000 * group_n)
+    zeros = None
+    if asym:
+        g = _rng(seed, _Z_STREAM, groups, group_n)
+        zeros = (g.integers(0, 16, groups).astype(np.uint8) if bits == 4
+                 else g.integers(-32, 33, groups).astype(np.int8))
+    return GroupedCase(base.x, base.w, scales, zeros, group_n, bits)
+
+
 # ---------------------------------------------------------------------- MXFP4
 
 
@@ -119,6 +149,9 @@ def fp8_case(m: int, k: int, n: int, seed: int = 0) -> Fp8Case:
 WORKLOADS = {
     "w4a16_tiny": {"op": "w4a16", "shapes": [(16, 512, 512)]},
     "w8a16_decode": {"op": "w8a16", "shapes": [(m, 4096, n) for n in (4096, 14336) for m in (1, 4, 16)]},
+    # The decode sweep with one scale and one zero point per 128 columns.
+    "w8a16_grouped_decode": {"op": "w8a16", "group_n": 128, "asym": True,
+                             "shapes": [(m, 4096, n) for n in (4096, 14336) for m in (1, 16)]},
     "w4a16_llama7b": {"op": "w4a16", "shapes": [(m, k, n) for (k, n) in ((4096, 4096), (4096, 11008), (11008, 4096))
                                                 for m in (1, 8, 64, 512, 4096)]},
     "mxfp4": {"op": "mxfp4", "shapes": [(m, 8192, 8192) for m in (128, 2048, 8192)]},
