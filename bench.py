@@ -336,9 +336,9 @@ def time_calls_flushed(torch, wl, steps, warmup):
 # kernel source it was taken on is unchanged (same SHA-256); else the roofline
 # reports traffic null.
 CAPTURED_TRAFFIC = {
-    "w8a16_16x4096x14336": {"bytes": 58_923_008 + 90_368,
+    "w8a16_16x4096x14336": {"bytes": 58_927_360 + 114_432,
                             "source": "bit_quantized_gemm_dequant_gb300/csrc/wo_skinny.cu",
-                            "sha256": "782b4d22380f29824cf0b8febcbddfb232741c93387b53907e997ce0646d54da",
+                            "sha256": "1758241bb134654b3f81671a4bed0da256ebfd0f71ddba0b9d766b3a696c696c",
                             "profile": "profiles/wo_skinny_w8a16_16x4096x14336.md"},
 }
 

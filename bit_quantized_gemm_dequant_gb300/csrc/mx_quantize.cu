@@ -18,12 +18,21 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 4;  // blocks in flight per thread quad
 
 __device__ __forceinline__ uint32_t e2m1_code(float x, float inv_scale) {
-  // v = x * 2^-e is exact (a power-of-two scaling); the comparisons below
-  // count the grid midpoints strictly below |v|, so a value exactly on a
-  // midpoint takes the smaller grid point — the first index of the argmin.
-  const float a = fabsf(x * inv_scale);
-  uint32_t j = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) +
-               (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
+  // v = x * 2^-e is exact (a power-of-two scaling) and |v| <= 6.  The index
+  // of the nearest grid point, the smaller one on a tie (the first index of
+  // the argmin), is the number of grid midpoints strictly below |v|:
+  //   |v| >= 1: the grid is every float with one mantissa bit from 1 to 6.
+  //             Adding just under half a unit of that bit (2^21 - 1) and
+  //             truncating rounds to nearest with ties to the smaller
+  //             magnitude; the index is 2 * (unbiased exponent + 1) plus the
+  //             kept mantissa bit, i.e. (bits >> 22) - 252.
+  //   |v| < 1:  the grid is 0, 0.5, 1, with midpoints 0.25 and 0.75.
+  // Non-negative float bits compare like the floats.  This equals counting
+  // the seven midpoints (0.25 .. 5) one by one for every float32 in [0, 6].
+  const uint32_t a = __float_as_uint(x * inv_scale) & 0x7FFFFFFFu;
+  const uint32_t big = ((a + 0x1FFFFFu) >> 22) - 252u;
+  const uint32_t small = (a > 0x3E800000u) + (a > 0x3F400000u);  // 0.25f, 0.75f
+  const uint32_t j = a >= 0x3F800000u ? big : small;              // 1.0f
   return (x < 0.0f ? 8u : 0u) | j;
 }
 
@@ -83,11 +92,15 @@ mx_quantize_kernel(MxQuantArgs p, uint32_t n_items) {
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       amax = fmaxf(amax, 1e-8f);
-      // q = amax / 6 rounded to FP32; ceil(log2 q) read off its bits: the
-      // unbiased exponent, plus one unless q is an exact power of two.  q is
-      // normal because amax >= 1e-8.
-      const uint32_t qb = __float_as_uint(__fdiv_rn(amax, 6.0f));
-      const int e = static_cast<int>((qb >> 23) & 0xFF) - 127 + ((qb & 0x7FFFFFu) != 0u);
+      // e = ceil(log2 q) with q = amax / 6 rounded to FP32, read off amax's
+      // own bits.  With amax = m 2^E (1 <= m < 2): amax / 6 = (m / 1.5) 2^(E-2),
+      // and m / 1.5 lies in (1, 4/3) when m > 1.5 (e = E - 1) and in [2/3, 1]
+      // otherwise (e = E - 2).  Rounding m / 1.5 to FP32 never lands on 1 from
+      // either side except at m = 1.5 itself, so e = E - 2 + [m > 1.5].  amax
+      // and q are normal because amax >= 1e-8.  (Equal to the rounded
+      // quotient's ceil(log2) for every mantissa, checked exhaustively.)
+      const uint32_t ab = __float_as_uint(amax);
+      const int e = static_cast<int>(ab >> 23) - 129 + ((ab & 0x7FFFFFu) > 0x400000u);
       const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
       uint32_t word = 0;
 #pragma unroll
@@ -110,10 +123,18 @@ cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s) {
   if (n_items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t blocks_per_cta = kThreads / 4;  // one 32-element block per thread quad
   int64_t ctas = (n_items + blocks_per_cta * kUnroll - 1) / (blocks_per_cta * kUnroll);
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 3;  // resident CTAs per SM (<= 85 registers)
-  if (ctas > cap) ctas = cap;
   const bool dense = a.ld_src == a.cols && a.ld_data == a.cols / 2 && a.ld_scales == a.cols / 32;
   auto kern = dense ? mx_quantize_kernel<true> : mx_quantize_kernel<false>;
+  // One wave of as many CTAs as the SMs hold at once (registers decide: at
+  // least 3 by the launch bounds).
+  static int per_sm[2] = {0, 0};
+  if (per_sm[dense] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess || n < 1) n = 3;
+    per_sm[dense] = n;
+  }
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm[dense];
+  if (ctas > cap) ctas = cap;
   kern<<<static_cast<unsigned>(ctas), kThreads, 0, s>>>(a, static_cast<uint32_t>(n_items));
   return cudaGetLastError();
 }

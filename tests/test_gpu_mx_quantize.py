@@ -75,6 +75,26 @@ def test_wide_dynamic_range_ties_and_zeros(wq):
     _assert_exact(_quant(wq, x), O.mx_quantize_fp4(x))
 
 
+def test_one_ulp_around_every_midpoint(wq):
+    """Blocks whose amax is exactly 6 * 2^e (so the block scale is 2^e) holding
+    each grid midpoint times 2^e and its float32 neighbours on both sides:
+    the code choice flips exactly at the midpoints, with ties to the smaller
+    magnitude."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    rows = []
+    for e in (-12, -1, 0, 3, 17):
+        scale = np.float32(2.0 ** e)
+        vals = np.concatenate([mids, np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0))])
+        block = np.zeros(32, np.float32)
+        block[0] = np.float32(6.0) * scale
+        block[1:22] = vals * scale
+        block[22:32] = -vals[:10] * scale
+        rows.append(block)
+        rows.append(-block)
+    x = np.stack(rows).repeat(2, axis=1).reshape(len(rows), 64)
+    _assert_exact(_quant(wq, x), O.mx_quantize_fp4(x))
+
+
 def test_large_operand_sampled_rows(wq):
     """The 8192 x 8192 weight operand, checked bit-exact on 256 sampled rows."""
     src = workloads.mx_source(8192, 8192, seed=0, stream=1)
