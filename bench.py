@@ -333,25 +333,36 @@ def time_calls_flushed(torch, wl, steps, warmup):
 
 # DRAM bytes (read + write) of one launch, from one ncu capture of the call's
 # kernel (the profile named beside it).  A figure is used only while the
-# kernel source it was taken on is unchanged (same SHA-256); else the roofline
-# reports traffic null.
+# kernel's code is the code it was taken on (same SHA-256 of the source with
+# comments removed, code_sha256); else the roofline reports traffic null.
 CAPTURED_TRAFFIC = {
     "w8a16_16x4096x14336": {"bytes": 58_927_360 + 114_432,
                             "source": "bit_quantized_gemm_dequant_gb300/csrc/wo_skinny.cu",
-                            "sha256": "1758241bb134654b3f81671a4bed0da256ebfd0f71ddba0b9d766b3a696c696c",
+                            "sha256": "141122c32bf3c5553f00350cc2539576cef7390a02ab568060ba77eee6746bea",  # code_sha256
                             "profile": "profiles/wo_skinny_w8a16_16x4096x14336.md"},
 }
 
 
-def captured_traffic(call_name):
+def code_sha256(text):
+    """SHA-256 of a C++/CUDA source with its comments and blank lines removed,
+    so that a comment edit does not invalidate a capture of unchanged code."""
     import hashlib
+    import re
 
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
+def captured_traffic(call_name):
+    """DRAM bytes of one launch from an ncu capture, while the kernel's code
+    (comments aside) is still the code that was captured; else None."""
     t = CAPTURED_TRAFFIC.get(call_name)
     if t is None:
         return None
     try:
-        with open(os.path.join(ROOT, t["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != t["sha256"]:
+        with open(os.path.join(ROOT, t["source"]), encoding="utf-8") as f:
+            if code_sha256(f.read()) != t["sha256"]:
                 return None
     except OSError:
         return None

@@ -40,14 +40,24 @@
 //     fragments use the same one.  Each fragment slot pair is mapped to the
 //     weight rows a thread loads (see the per-mode comments), and the
 //     activation fragment is gathered from shared memory in that order.
-//   * Stream-K split: the grid is the SM count and the (M tile, 128-column
-//     tile, chunk) units are dealt out as equal contiguous runs, so every SM
-//     streams the same number of bytes in a single wave.  The warps' partial
-//     sums of a tile meet in shared memory (lane-native float4
-//     layout, conflict free, fixed order); when a tile is split between
-//     CTAs, each writes its partial tile to the caller's workspace and the
-//     last one to arrive (per-tile counter) adds them in CTA order, so the
-//     result is deterministic, and resets the counter.
+//   * Work split, one of three plans per shape (make_plan):
+//       - one CTA per tile when the tiles fill at least half the SMs: no
+//         split of K, no hand-shake;
+//       - otherwise a cluster of S CTAs per tile, each streaming a slice of
+//         K; the partial tiles meet in distributed shared memory, each CTA
+//         pushing the other CTAs' slices into their receive areas with
+//         st.async (no CTA reads another's shared memory);
+//       - otherwise stream-K: the grid is the SM count and the (M tile,
+//         128-column tile, chunk) units are dealt out as equal contiguous
+//         runs; a tile split between CTAs meets in the caller's workspace,
+//         where the last CTA to arrive (per-tile counter) adds the parts in
+//         CTA order and resets the counter.
+//     In every plan the warps' partial sums of a tile meet in shared memory
+//     (lane-native float4 layout, conflict free) and every sum runs in a
+//     fixed order, so results are deterministic.
+//   * Column-grouped scales and zero points ("Triton 量化算子：W8A16 权重量化
+//     融合矩阵乘法", 扩展说明) are a separate compile-time instance: the zero
+//     point enters through the activation row sums, once per tile.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
