@@ -338,19 +338,20 @@ def time_calls_flushed(torch, wl, steps, warmup):
 CAPTURED_TRAFFIC = {
     "w8a16_16x4096x14336": {"bytes": 58_927_360 + 114_432,
                             "source": "bit_quantized_gemm_dequant_gb300/csrc/wo_skinny.cu",
-                            "sha256": "141122c32bf3c5553f00350cc2539576cef7390a02ab568060ba77eee6746bea",  # code_sha256
+                            "sha256": "f939ffb55552f7cb17112bd021a5f104681bd9177ec65473698c9b1de0a08e2e",  # code_sha256
                             "profile": "profiles/wo_skinny_w8a16_16x4096x14336.md"},
 }
 
 
 def code_sha256(text):
-    """SHA-256 of a C++/CUDA source with its comments and blank lines removed,
-    so that a comment edit does not invalidate a capture of unchanged code."""
+    """SHA-256 of a C++/CUDA source with its comments, indentation and blank
+    lines removed, so that such edits do not invalidate a capture of
+    unchanged code."""
     import hashlib
     import re
 
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    lines = [re.sub(r"//.*$", "", ln).strip() for ln in text.splitlines()]
     return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
 
 
