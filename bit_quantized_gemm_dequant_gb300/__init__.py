@@ -87,6 +87,51 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _require(cond, where, what):
+    if not cond:
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: {what}")
+
+
+def _on_gpu(where, *tensors):
+    """Every given tensor lives in the memory of one CUDA device: the C ABI takes
+    device pointers, and a host pointer handed to a kernel would fault."""
+    devs = {t.device for t in tensors if t is not None}
+    _require(all(d.type == "cuda" for d in devs), where, "tensors must be CUDA tensors")
+    _require(len(devs) <= 1, where, "tensors must be on one device")
+
+
+def _kind(where, t, name, *, size=None, dtypes=None):
+    """Element size or dtype of one argument."""
+    import torch
+
+    if t is None:
+        return
+    if dtypes is not None:
+        _require(t.dtype in tuple(getattr(torch, d) for d in dtypes if hasattr(torch, d)), where,
+                 f"{name} must be {' or '.join(dtypes)}, got {t.dtype}")
+    if size is not None:
+        _require(t.element_size() == size, where, f"{name} must have {size}-byte elements, got {t.dtype}")
+
+
+def _weight_only_checks(where, bits, x, w, scales, y, zeros=None, group_n=1):
+    _on_gpu(where, x, w, scales, y, zeros)
+    _kind(where, x, "x", dtypes=("float16",))
+    _kind(where, w, "w", size=1)
+    _kind(where, scales, "scales", dtypes=("float16",))
+    _kind(where, y, "y", dtypes=("float16",))
+    _kind(where, zeros, "zeros", size=1)
+    _require(x.dim() == 2 and w.dim() == 2, where, "x and w must be 2-D")
+    M, K = x.shape
+    N = w.shape[1]
+    _require(w.shape[0] * (2 if bits == 4 else 1) == K, where,
+             f"w has {w.shape[0]} rows; K = {K} needs {K // 2 if bits == 4 else K}")
+    _require(group_n >= 1, where, "group_n must be >= 1")
+    groups = -(-N // group_n)
+    _require(scales.numel() >= groups, where, f"scales has {scales.numel()} entries, needs {groups}")
+    _require(zeros is None or zeros.numel() >= groups, where, f"zeros needs {groups} entries")
+    _require(y is None or tuple(y.shape) == (M, N), where, f"y must be [{M}, {N}]")
+
+
 def _ld(t):
     if t.dim() != 2 or t.stride(1) != 1:
         raise WqError(WQ_ERR_UNSUPPORTED, "matrices must be 2-D with unit inner stride")
@@ -123,6 +168,8 @@ def wq_gemm_w4a16(x, wq, scales, y=None, workspace=None, stream=None):
     """Y fp16 [M, N] = X fp16 [M, K] * ((unpack(wq [K/2, N]) - 8) * scales[N])."""
     import torch
 
+    _weight_only_checks("wq_gemm_w4a16", 4, x, wq, scales, y)
+    _on_gpu("wq_gemm_w4a16", x, workspace)
     M, K = x.shape
     N = wq.shape[1]
     if y is None:
@@ -139,6 +186,8 @@ def wq_gemm_w8a16(x, w, scales, y=None, workspace=None, stream=None):
     """Y fp16 [M, N] = X fp16 [M, K] * (w int8 [K, N] * scales[N])."""
     import torch
 
+    _weight_only_checks("wq_gemm_w8a16", 8, x, w, scales, y)
+    _on_gpu("wq_gemm_w8a16", x, workspace)
     M, K = x.shape
     N = w.shape[1]
     if y is None:
@@ -156,6 +205,7 @@ def wq_gemm_w8a16_noalloc(x, w, scales, y=None, stream=None):
     (for callers that cannot allocate device memory at call time)."""
     import torch
 
+    _weight_only_checks("wq_gemm_w8a16_noalloc", 8, x, w, scales, y)
     M, K = x.shape
     N = w.shape[1]
     if y is None:
@@ -168,6 +218,8 @@ def wq_gemm_w8a16_noalloc(x, w, scales, y=None, stream=None):
 def _grouped(name, op, x, w, scales, zeros, group_n, y, workspace, stream):
     import torch
 
+    _weight_only_checks(name, 4 if op == WQ_OP_W4A16 else 8, x, w, scales, y, zeros, int(group_n))
+    _on_gpu(name, x, workspace)
     M, K = x.shape
     N = w.shape[1]
     if y is None:
@@ -196,7 +248,15 @@ def mx_quantize_fp4(src, data=None, scales=None, stream=None):
     """fp32 [R, C] -> (uint8 data [R, C/2], uint8 E8M0 scales [R, C/32])."""
     import torch
 
+    where = "mx_quantize_fp4"
+    _on_gpu(where, src, data, scales)
+    _kind(where, src, "src", dtypes=("float32",))
+    _kind(where, data, "data", size=1)
+    _kind(where, scales, "scales", size=1)
+    _require(src.dim() == 2, where, "src must be 2-D")
     R, C = src.shape
+    _require(data is None or tuple(data.shape) == (R, C // 2), where, f"data must be [{R}, {C // 2}]")
+    _require(scales is None or tuple(scales.shape) == (R, C // 32), where, f"scales must be [{R}, {C // 32}]")
     if data is None:
         data = torch.empty((R, C // 2), dtype=torch.uint8, device=src.device)
     if scales is None:
@@ -210,7 +270,17 @@ def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
     """C fp32 [M, N] = A * W^T for MXFP4 operands (data [rows, K/2] + scales [rows, K/32])."""
     import torch
 
+    where = "mx_gemm_fp4"
+    _on_gpu(where, a, sa, w, sw, c, workspace)
+    for t, n in ((a, "a"), (sa, "sa"), (w, "w"), (sw, "sw")):
+        _kind(where, t, n, size=1)
+        _require(t.dim() == 2, where, f"{n} must be 2-D")
+    _kind(where, c, "c", dtypes=("float32",))
     M, N, K = a.shape[0], w.shape[0], a.shape[1] * 2
+    _require(w.shape[1] * 2 == K, where, "a and w must have the same K")
+    _require(tuple(sa.shape) == (M, K // 32) and tuple(sw.shape) == (N, K // 32), where,
+             f"scales must be [{M}, {K // 32}] and [{N}, {K // 32}]")
+    _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
     if c is None:
         c = torch.empty((M, N), dtype=torch.float32, device=a.device)
     wsp, wsb = _ws(workspace)
@@ -223,8 +293,15 @@ def fp8_gemm(a, b, scale_a, scale_b, c=None, workspace=None, stream=None):
     """C bf16 [M, N] = (A e4m3 [M, K] * B e4m3 [K, N]) * scale_a * scale_b."""
     import torch
 
+    where = "fp8_gemm"
+    _on_gpu(where, a, b, c, workspace)
+    _kind(where, a, "a", size=1)
+    _kind(where, b, "b", size=1)
+    _kind(where, c, "c", dtypes=("bfloat16",))
+    _require(a.dim() == 2 and b.dim() == 2 and b.shape[0] == a.shape[1], where, "a [M, K] and b [K, N] needed")
     M, K = a.shape
     N = b.shape[1]
+    _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
     if c is None:
         c = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     if workspace is None:

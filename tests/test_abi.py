@@ -110,3 +110,51 @@ def test_product_does_not_import_oracle():
                 with open(os.path.join(dirpath, f)) as fh:
                     text = fh.read()
                 assert not re.search(r"(^|\s)(import|from)\s+oracle", text), f
+
+
+def test_binding_refuses_host_tensors(wq):
+    """The C ABI takes device pointers; the binding refuses CPU tensors before
+    any call (a host pointer in a kernel would fault)."""
+    import torch
+
+    x = torch.zeros((4, 64), dtype=torch.float16)
+    s = torch.zeros(64, dtype=torch.float16)
+    calls = [
+        lambda: wq.wq_gemm_w4a16(x, torch.zeros((32, 64), dtype=torch.uint8), s),
+        lambda: wq.wq_gemm_w8a16(x, torch.zeros((64, 64), dtype=torch.int8), s),
+        lambda: wq.wq_gemm_w8a16_grouped(x, torch.zeros((64, 64), dtype=torch.int8), s, None, 4),
+        lambda: wq.mx_quantize_fp4(torch.zeros((4, 64))),
+        lambda: wq.fp8_gemm(torch.zeros((4, 8), dtype=torch.uint8), torch.zeros((8, 16), dtype=torch.uint8), 1.0, 1.0),
+    ]
+    for call in calls:
+        with pytest.raises(wq.WqError) as ei:
+            call()
+        assert ei.value.status == wq.WQ_ERR_INVALID_ARG
+
+
+def test_binding_shape_and_dtype_checks(wq, monkeypatch):
+    """Shapes and element types are checked against each other before any call
+    (a short scales or zeros array would be read past its end)."""
+    import torch
+
+    monkeypatch.setattr(wq, "_on_gpu", lambda where, *t: None)
+    x = torch.zeros((4, 64), dtype=torch.float16)
+    w4 = torch.zeros((32, 80), dtype=torch.uint8)
+    w8 = torch.zeros((64, 80), dtype=torch.int8)
+    s = torch.zeros(80, dtype=torch.float16)
+    ok = [(4, x, w4, s, None, None, 1), (8, x, w8, s, None, None, 1),
+          (8, x, w8, torch.zeros(3, dtype=torch.float16), None, torch.zeros(3, dtype=torch.int8), 32)]
+    for bits, xx, w, sc, y, z, g in ok:
+        wq._weight_only_checks("t", bits, xx, w, sc, y, z, g)
+    bad = [
+        (4, x, w8, s, None, None, 1),                                  # INT8-shaped weights for INT4
+        (8, x.float(), w8, s, None, None, 1),                          # fp32 activations
+        (8, x, w8, torch.zeros(79, dtype=torch.float16), None, None, 1),  # one scale short
+        (8, x, w8, torch.zeros(2, dtype=torch.float16), None, None, 32),  # 80 columns need 3 groups
+        (8, x, w8, torch.zeros(3, dtype=torch.float16), None, torch.zeros(2, dtype=torch.int8), 32),
+        (8, x, w8, s, torch.zeros((4, 64), dtype=torch.float16), None, 1),  # y of the wrong shape
+        (8, x, w8, s, None, None, 0),                                  # empty groups
+    ]
+    for bits, xx, w, sc, y, z, g in bad:
+        with pytest.raises(wq.WqError):
+            wq._weight_only_checks("t", bits, xx, w, sc, y, z, g)
