@@ -95,41 +95,61 @@ def _require(cond, where, what):
 def _on_gpu(where, *tensors):
     """Every given tensor lives in the memory of one CUDA device: the C ABI takes
     device pointers, and a host pointer handed to a kernel would fault."""
-    devs = {t.device for t in tensors if t is not None}
-    _require(all(d.type == "cuda" for d in devs), where, "tensors must be CUDA tensors")
-    _require(len(devs) <= 1, where, "tensors must be on one device")
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise WqError(WQ_ERR_INVALID_ARG, f"{where}: tensors must be CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise WqError(WQ_ERR_INVALID_ARG, f"{where}: tensors must be on one device")
 
 
-def _kind(where, t, name, *, size=None, dtypes=None):
+_DTYPES: dict = {}
+
+
+def _dtype(name):
+    d = _DTYPES.get(name)
+    if d is None:
+        import torch
+
+        d = _DTYPES[name] = getattr(torch, name)
+    return d
+
+
+def _kind(where, t, name, *, size=None, dtype=None):
     """Element size or dtype of one argument."""
-    import torch
-
     if t is None:
         return
-    if dtypes is not None:
-        _require(t.dtype in tuple(getattr(torch, d) for d in dtypes if hasattr(torch, d)), where,
-                 f"{name} must be {' or '.join(dtypes)}, got {t.dtype}")
-    if size is not None:
-        _require(t.element_size() == size, where, f"{name} must have {size}-byte elements, got {t.dtype}")
+    if dtype is not None and t.dtype is not _dtype(dtype):
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: {name} must be {dtype}, got {t.dtype}")
+    if size is not None and t.element_size() != size:
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: {name} must have {size}-byte elements, got {t.dtype}")
 
 
 def _weight_only_checks(where, bits, x, w, scales, y, zeros=None, group_n=1):
     _on_gpu(where, x, w, scales, y, zeros)
-    _kind(where, x, "x", dtypes=("float16",))
+    _kind(where, x, "x", dtype="float16")
     _kind(where, w, "w", size=1)
-    _kind(where, scales, "scales", dtypes=("float16",))
-    _kind(where, y, "y", dtypes=("float16",))
+    _kind(where, scales, "scales", dtype="float16")
+    _kind(where, y, "y", dtype="float16")
     _kind(where, zeros, "zeros", size=1)
-    _require(x.dim() == 2 and w.dim() == 2, where, "x and w must be 2-D")
+    if x.dim() != 2 or w.dim() != 2:
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: x and w must be 2-D")
     M, K = x.shape
     N = w.shape[1]
-    _require(w.shape[0] * (2 if bits == 4 else 1) == K, where,
-             f"w has {w.shape[0]} rows; K = {K} needs {K // 2 if bits == 4 else K}")
-    _require(group_n >= 1, where, "group_n must be >= 1")
+    if w.shape[0] * (2 if bits == 4 else 1) != K:
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: w has {w.shape[0]} rows; K = {K} needs "
+                                          f"{K // 2 if bits == 4 else K}")
+    if group_n < 1:
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: group_n must be >= 1")
     groups = -(-N // group_n)
-    _require(scales.numel() >= groups, where, f"scales has {scales.numel()} entries, needs {groups}")
-    _require(zeros is None or zeros.numel() >= groups, where, f"zeros needs {groups} entries")
-    _require(y is None or tuple(y.shape) == (M, N), where, f"y must be [{M}, {N}]")
+    if scales.numel() < groups or (zeros is not None and zeros.numel() < groups):
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: scales and zeros need {groups} entries")
+    if y is not None and (y.shape[0] != M or y.shape[1] != N):
+        raise WqError(WQ_ERR_INVALID_ARG, f"{where}: y must be [{M}, {N}]")
 
 
 def _ld(t):
@@ -250,7 +270,7 @@ def mx_quantize_fp4(src, data=None, scales=None, stream=None):
 
     where = "mx_quantize_fp4"
     _on_gpu(where, src, data, scales)
-    _kind(where, src, "src", dtypes=("float32",))
+    _kind(where, src, "src", dtype="float32")
     _kind(where, data, "data", size=1)
     _kind(where, scales, "scales", size=1)
     _require(src.dim() == 2, where, "src must be 2-D")
@@ -275,7 +295,7 @@ def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
     for t, n in ((a, "a"), (sa, "sa"), (w, "w"), (sw, "sw")):
         _kind(where, t, n, size=1)
         _require(t.dim() == 2, where, f"{n} must be 2-D")
-    _kind(where, c, "c", dtypes=("float32",))
+    _kind(where, c, "c", dtype="float32")
     M, N, K = a.shape[0], w.shape[0], a.shape[1] * 2
     _require(w.shape[1] * 2 == K, where, "a and w must have the same K")
     _require(tuple(sa.shape) == (M, K // 32) and tuple(sw.shape) == (N, K // 32), where,
@@ -297,7 +317,7 @@ def fp8_gemm(a, b, scale_a, scale_b, c=None, workspace=None, stream=None):
     _on_gpu(where, a, b, c, workspace)
     _kind(where, a, "a", size=1)
     _kind(where, b, "b", size=1)
-    _kind(where, c, "c", dtypes=("bfloat16",))
+    _kind(where, c, "c", dtype="bfloat16")
     _require(a.dim() == 2 and b.dim() == 2 and b.shape[0] == a.shape[1], where, "a [M, K] and b [K, N] needed")
     M, K = a.shape
     N = b.shape[1]

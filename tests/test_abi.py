@@ -158,3 +158,57 @@ def test_binding_shape_and_dtype_checks(wq, monkeypatch):
     for bits, xx, w, sc, y, z, g in bad:
         with pytest.raises(wq.WqError):
             wq._weight_only_checks("t", bits, xx, w, sc, y, z, g)
+
+
+class _FakeLib:
+    """Records the C calls a binding function makes (no CUDA needed)."""
+
+    def __init__(self):
+        self.calls = []
+
+    def __getattr__(self, name):
+        if name == "wq_status_string":
+            return lambda status: b"WQ_STATUS"
+
+        def call(*args):
+            self.calls.append((name, args))
+            return 0
+        return call
+
+
+def test_binding_functions_marshal_without_cuda(wq, monkeypatch):
+    """Every binding function runs its checks and marshals its call: a fake
+    library stands in for libwq.so and host tensors stand in for device ones."""
+    import ctypes
+
+    import torch
+
+    fake = _FakeLib()
+    monkeypatch.setattr(wq, "lib", fake)
+    monkeypatch.setattr(wq, "_on_gpu", lambda where, *t: None)
+    monkeypatch.setattr(wq, "_stream", lambda stream: ctypes.c_void_p(0))
+    monkeypatch.setattr(wq, "auto_workspace", lambda *a, **k: None)
+    x = torch.zeros((4, 64), dtype=torch.float16)
+    s = torch.zeros(96, dtype=torch.float16)
+    w4 = torch.zeros((32, 96), dtype=torch.uint8)
+    w8 = torch.zeros((64, 96), dtype=torch.int8)
+    assert wq.wq_gemm_w4a16(x, w4, s).shape == (4, 96)
+    assert wq.wq_gemm_w8a16(x, w8, s).shape == (4, 96)
+    assert wq.wq_gemm_w8a16_noalloc(x, w8, s).shape == (4, 96)
+    assert wq.wq_gemm_w4a16_grouped(x, w4, s[:3], torch.zeros(3, dtype=torch.uint8), 32).shape == (4, 96)
+    assert wq.wq_gemm_w8a16_grouped(x, w8, s[:3], None, 32).shape == (4, 96)
+    d, e = wq.mx_quantize_fp4(torch.zeros((4, 64)))
+    assert d.shape == (4, 32) and e.shape == (4, 2)
+    c = wq.mx_gemm_fp4(d, e, torch.zeros((8, 32), dtype=torch.uint8), torch.zeros((8, 2), dtype=torch.uint8))
+    assert c.shape == (4, 8) and c.dtype == torch.float32
+    c8 = wq.fp8_gemm(torch.zeros((4, 64), dtype=torch.uint8), torch.zeros((64, 16), dtype=torch.uint8), 1.0, 2.0)
+    assert c8.shape == (4, 16) and c8.dtype == torch.bfloat16
+    names = [n for n, _ in fake.calls]
+    assert names == ["wq_gemm_w4a16", "wq_gemm_w8a16", "wq_gemm_w8a16_noalloc", "wq_gemm_w4a16_grouped",
+                     "wq_gemm_w8a16_grouped", "mx_quantize_fp4", "mx_gemm_fp4", "fp8_gemm"]
+    argc = {n: len(a) for n, a in fake.calls}
+    for n, sig in wq._SIGS.items():
+        if n in argc:
+            assert argc[n] == len(sig), n
+    with pytest.raises(wq.WqError):
+        wq.mx_gemm_fp4(d, e, torch.zeros((8, 30), dtype=torch.uint8), torch.zeros((8, 2), dtype=torch.uint8))
