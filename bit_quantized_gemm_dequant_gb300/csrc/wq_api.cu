@@ -67,6 +67,10 @@ static int check_weight_only(int M, int N, int K, const void* X, int64_t ldx, co
 // tiled tensor-memory GEMM.
 constexpr int kSkinnyMaxM = 64;
 
+// The tiled GEMMs put 128-row M tiles on the grid's y dimension (at most
+// 65535 blocks); larger M is refused on the host instead of failing to launch.
+constexpr int64_t kMaxTiledM = int64_t(65535) * 128;
+
 static size_t weight_only_workspace(int bits, int M, int N, int K) {
   return (M > 0 && M <= kSkinnyMaxM) ? wo_skinny_workspace(M, N, K, bits) : 0;
 }
@@ -75,6 +79,7 @@ static int run_weight_only(int bits, int M, int N, int K, const void* X, int64_t
                            const void* scales, void* Y, int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s,
                            const void* zeros = nullptr, int group_n = 1) {
   if (M == 0 || N == 0) return WQ_OK;
+  if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
   const size_t need = weight_only_workspace(bits, M, N, K);
   if (ws_bytes < need || (need > 0 && (!ws || !aligned(ws, 16)))) return WQ_ERR_WORKSPACE;
   WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy, ws, ws_bytes, zeros, group_n};
@@ -157,6 +162,7 @@ int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_
   if (!src || !data || !scales) return WQ_ERR_INVALID_ARG;
   if (ld_src < cols || ld_data < cols / 2 || ld_scales < cols / 32) return WQ_ERR_INVALID_ARG;
   if (!aligned(src, 16) || ld_src % 4 || !aligned(data, 4) || ld_data % 4) return WQ_ERR_MISALIGNED;
+  if (static_cast<int64_t>(rows) * (cols / 32) >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;  // 32-bit block ids
   MxQuantArgs a{rows, cols, src, ld_src, data, ld_data, scales, ld_scales};
   return launch_status(launch_mx_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -171,6 +177,7 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_
   if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2 || ldsa < K / 32 || ldsw < K / 32))) return WQ_ERR_INVALID_ARG;
   if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
   if (K > 0 && (!aligned(A, 16) || !aligned(W, 16) || lda % 16 || ldw % 16)) return WQ_ERR_MISALIGNED;
+  if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
   if (ws_bytes < wq_workspace_size(WQ_OP_MX_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
   MxGemmArgs a{M, N, K, A, lda, SA, ldsa, W, ldw, SW, ldsw, C, ldc};
   return launch_status(launch_mx_gemm(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -30,6 +30,9 @@
  *     WQ_OK is returned (for K == 0 with M, N > 0 the GEMMs write zeros).
  *   - Inputs must be finite; NaN/Inf inputs give unspecified (but in-bounds)
  *     results.
+ *   - Shapes beyond the kernels' grid limits return WQ_ERR_UNSUPPORTED without
+ *     launching: M > 8,388,480 (65535 tiles of 128 rows) for the weight-only
+ *     and MXFP4 GEMMs, and 2^31 or more 32-element blocks for mx_quantize_fp4.
  */
 #ifndef WQ_H_
 #define WQ_H_

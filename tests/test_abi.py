@@ -212,3 +212,15 @@ def test_binding_functions_marshal_without_cuda(wq, monkeypatch):
             assert argc[n] == len(sig), n
     with pytest.raises(wq.WqError):
         wq.mx_gemm_fp4(d, e, torch.zeros((8, 30), dtype=torch.uint8), torch.zeros((8, 2), dtype=torch.uint8))
+
+
+def test_shapes_beyond_the_grid_limits_are_refused(wq):
+    """Validation returns before any CUDA call, so fake pointers are never used."""
+    L = wq.lib
+    big_m = 65535 * 128 + 1
+    assert _w4(wq, M=big_m, ldy=64) == wq.WQ_ERR_UNSUPPORTED
+    assert L.wq_gemm_w8a16(big_m, 64, 64, FAKE, 64, FAKE, 64, FAKE, FAKE, 64, None, 0, None) == wq.WQ_ERR_UNSUPPORTED
+    assert L.mx_gemm_fp4(big_m, 64, 64, FAKE, 32, FAKE, 2, FAKE, 32, FAKE, 2, FAKE, 64, None, 0, None) \
+        == wq.WQ_ERR_UNSUPPORTED
+    rows, cols = 1 << 21, 1 << 15  # 2^31 blocks of 32
+    assert L.mx_quantize_fp4(rows, cols, FAKE, cols, FAKE, cols // 2, FAKE, cols // 32, None) == wq.WQ_ERR_UNSUPPORTED
