@@ -191,6 +191,8 @@ int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* 
   if (ldc < N || (K > 0 && (lda < K || ldb < N))) return WQ_ERR_INVALID_ARG;
   if (!aligned(C, 16) || ldc % 8) return WQ_ERR_MISALIGNED;
   if (K > 0 && (!aligned(A, 16) || !aligned(B, 16) || lda % 16 || ldb % 16)) return WQ_ERR_MISALIGNED;
+  // The tiled path counts its 128 x 256 tiles in 32 bits.
+  if (M > kFp8SkinnyMaxM && (M > kMaxTiledM || N > kMaxTiledM)) return WQ_ERR_UNSUPPORTED;
   const size_t need = wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K);
   if (ws_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 16)))) return WQ_ERR_WORKSPACE;
   Fp8GemmArgs a{M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, workspace, ws_bytes};

@@ -32,7 +32,8 @@
  *     results.
  *   - Shapes beyond the kernels' grid limits return WQ_ERR_UNSUPPORTED without
  *     launching: M > 8,388,480 (65535 tiles of 128 rows) for the weight-only
- *     and MXFP4 GEMMs, and 2^31 or more 32-element blocks for mx_quantize_fp4.
+ *     and MXFP4 GEMMs and for the FP8 GEMM at M > 16 (there also
+ *     N > 8,388,480), and 2^31 or more 32-element blocks for mx_quantize_fp4.
  */
 #ifndef WQ_H_
 #define WQ_H_

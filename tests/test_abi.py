@@ -222,5 +222,8 @@ def test_shapes_beyond_the_grid_limits_are_refused(wq):
     assert L.wq_gemm_w8a16(big_m, 64, 64, FAKE, 64, FAKE, 64, FAKE, FAKE, 64, None, 0, None) == wq.WQ_ERR_UNSUPPORTED
     assert L.mx_gemm_fp4(big_m, 64, 64, FAKE, 32, FAKE, 2, FAKE, 32, FAKE, 2, FAKE, 64, None, 0, None) \
         == wq.WQ_ERR_UNSUPPORTED
+    assert L.fp8_gemm(big_m, 64, 64, FAKE, 64, FAKE, 64, 1.0, 1.0, FAKE, 64, None, 0, None) == wq.WQ_ERR_UNSUPPORTED
+    assert L.fp8_gemm(64, big_m, 64, FAKE, 64, FAKE, big_m + 15, 1.0, 1.0, FAKE, big_m + 7, None, 0, None) \
+        == wq.WQ_ERR_UNSUPPORTED
     rows, cols = 1 << 21, 1 << 15  # 2^31 blocks of 32
     assert L.mx_quantize_fp4(rows, cols, FAKE, cols, FAKE, cols // 2, FAKE, cols // 32, None) == wq.WQ_ERR_UNSUPPORTED
