@@ -199,12 +199,14 @@ cudaError_t launch_variant(const Fp8GemmArgs& a, cudaStream_t s) {
   e = make_tmap_2d(&tB, a.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K, a.ldb, 128, BK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   auto kern = fp8_gemm_kernel<HALVES>;
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDevice<bool> configured;
+  bool done = false;
+  if (!configured.get(done, [&](bool& v) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        v = true;
+        return e == cudaSuccess;
+      }))
+    return e;
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
   kern<<<grid, kThreads, Cfg::kSmemBytes, s>>>(tA, tB, a, device_error_word());

@@ -339,12 +339,14 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
     tSW = tW;
   }
   auto kern = sf_tma ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
-  static bool configured[2] = {false, false};
-  if (!configured[sf_tma]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[sf_tma] = true;
-  }
+  static PerDevice<bool> configured[2];
+  bool done = false;
+  if (!configured[sf_tma].get(done, [&](bool& v) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        v = true;
+        return e == cudaSuccess;
+      }))
+    return e;
   const int splits = mx_splits(a.M, a.N, a.K);
   if (splits > 1) {  // the splits add into C
     e = cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);

@@ -127,13 +127,12 @@ cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s) {
   auto kern = dense ? mx_quantize_kernel<true> : mx_quantize_kernel<false>;
   // One wave of as many CTAs as the SMs hold at once (registers decide: at
   // least 3 by the launch bounds).
-  static int per_sm[2] = {0, 0};
-  if (per_sm[dense] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess || n < 1) n = 3;
-    per_sm[dense] = n;
-  }
-  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm[dense];
+  static PerDevice<int> per_sm[2];
+  int n = 3;  // the launch bounds' minimum, if the query fails
+  per_sm[dense].get(n, [&](int& v) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, 0) == cudaSuccess && v >= 1;
+  });
+  const int64_t cap = static_cast<int64_t>(sm_count()) * n;
   if (ctas > cap) ctas = cap;
   kern<<<static_cast<unsigned>(ctas), kThreads, 0, s>>>(a, static_cast<uint32_t>(n_items));
   return cudaGetLastError();

@@ -246,12 +246,14 @@ cudaError_t launch_tc(const WoArgs& a, cudaStream_t s) {
                    CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   auto kern = wo_gemm_kernel<BITS, BM>;
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDevice<bool> configured;
+  bool done = false;
+  if (!configured.get(done, [&](bool& v) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        v = true;
+        return e == cudaSuccess;
+      }))
+    return e;
   dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
   kern<<<grid, kThreads, Cfg::kSmemBytes, s>>>(tX, tW, a, device_error_word());
   return cudaGetLastError();

@@ -763,33 +763,38 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 // must precede both the occupancy query and the first launch.
 template <int BITS, int MT, bool kZp = false>
 cudaError_t configure_kernel() {
-  static cudaError_t status = cudaFuncSetAttribute(wo_skinny_kernel<BITS, MT, kZp>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(Cfg<BITS, MT>::kSmemBytes));
-  return status;
+  static PerDevice<cudaError_t> status;
+  cudaError_t e = cudaSuccess;
+  status.get(e, [&e](cudaError_t& v) {
+    v = e = cudaFuncSetAttribute(wo_skinny_kernel<BITS, MT, kZp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg<BITS, MT>::kSmemBytes));
+    return v == cudaSuccess;
+  });
+  return e;
 }
 
 template <int BITS, int MT>
 int ctas_per_sm() {
-  static int cached = 0;
-  if (cached == 0) {
-    int n = 0;
-    if (configure_kernel<BITS, MT>() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wo_skinny_kernel<BITS, MT, false>, kThreads,
-                                                      Cfg<BITS, MT>::kSmemBytes) != cudaSuccess || n < 1)
-      return 1;  // not cached: a later call may succeed
-    cached = n;
-  }
-  return cached;
+  static PerDevice<int> cached;
+  int n = 1;
+  if (!cached.get(n, [](int& v) {
+        return configure_kernel<BITS, MT>() == cudaSuccess &&
+               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, wo_skinny_kernel<BITS, MT, false>, kThreads,
+                                                             Cfg<BITS, MT>::kSmemBytes) == cudaSuccess &&
+               v >= 1;
+      }))
+    return 1;  // not cached: a later call may succeed
+  return n;
 }
 
 // Clusters of S of these CTAs that the GPU holds at once (0 when it holds
 // none or the query fails; not cached then).
 template <int BITS, int MT>
 int max_clusters(int S) {
-  static int cached[9] = {0};
+  static PerDevice<int> cached[9];
   if (S < 2 || S > 8) return 0;
-  if (cached[S] == 0) {
+  int n = 0;
+  cached[S].get(n, [S](int& v) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S);
     cfg.blockDim = dim3(kThreads);
@@ -801,13 +806,10 @@ int max_clusters(int S) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (configure_kernel<BITS, MT>() != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, wo_skinny_kernel<BITS, MT, false>, &cfg) != cudaSuccess || n < 1)
-      return 0;
-    cached[S] = n;
-  }
-  return cached[S];
+    return configure_kernel<BITS, MT>() == cudaSuccess &&
+           cudaOccupancyMaxActiveClusters(&v, wo_skinny_kernel<BITS, MT, false>, &cfg) == cudaSuccess && v >= 1;
+  });
+  return n;  // 0 when the query failed (not cached: a later call may succeed)
 }
 
 template <int BITS, int MT>

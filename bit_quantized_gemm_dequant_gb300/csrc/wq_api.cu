@@ -23,31 +23,32 @@ int launch_status(cudaError_t e) {
 }
 }  // namespace
 
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) d = 0;
+  return d;
+}
+
 int* device_error_word() {
-  static int* ptr = nullptr;
-  static int dev = -1;
-  int cur = 0;
-  cudaGetDevice(&cur);
-  if (ptr == nullptr || cur != dev) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptr = static_cast<int*>(p);
-    dev = cur;
-  }
-  return ptr;
+  static PerDevice<int*> words;
+  int* ptr = nullptr;
+  words.get(ptr, [](int*& p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return false;
+    p = static_cast<int*>(a);
+    return true;
+  });
+  return ptr;  // nullptr if the lookup failed: kernels then record nothing
 }
 
 int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 148;
-  }
-  return cached[dev];
+  static PerDevice<int> counts;
+  int n = 0;
+  if (!counts.get(n, [](int& v) {
+        return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, current_device()) == cudaSuccess && v > 0;
+      }))
+    n = 148;  // the query failed (the launch that follows reports the error)
+  return n;
 }
 
 // Shared validation of the weight-only GEMMs.

@@ -2,12 +2,50 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/wq.h"
 
 namespace wq {
+
+// Host-side one-time setup per device (a kernel's shared-memory attribute, an
+// occupancy count), safe to call from several host threads: get(init) runs
+// init(value) for the current device until it succeeds once, and returns the
+// stored value afterwards (lock-free once set).  A failed init is not stored,
+// so a later call tries again.
+constexpr int kMaxDevices = 64;
+int current_device();  // cudaGetDevice, clamped to [0, kMaxDevices)
+
+template <typename T>
+class PerDevice {
+ public:
+  template <typename F>
+  bool get(T& out, F&& init) {
+    const int d = current_device();
+    if (ready_[d].load(std::memory_order_acquire)) {
+      out = value_[d];
+      return true;
+    }
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!ready_[d].load(std::memory_order_relaxed)) {
+      T v{};
+      if (!init(v)) return false;
+      value_[d] = v;
+      ready_[d].store(true, std::memory_order_release);
+    }
+    out = value_[d];
+    return true;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> ready_[kMaxDevices] = {};
+  T value_[kMaxDevices] = {};
+};
 
 // Device error word written by kernels whose bounded waits give up.  Lives in
 // wq_api.cu; kernels receive its device address as a parameter.
