@@ -235,6 +235,6 @@ int wq_get_device_error(wq_stream_t stream, int* site) {
   return host ? WQ_ERR_DEVICE : WQ_OK;
 }
 
-int wq_version(void) { return 100; }
+int wq_version(void) { return 200; }  // 0.2.0: grouped weight-only entry points
 
 }  // extern "C"

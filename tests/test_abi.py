@@ -41,7 +41,7 @@ def test_status_strings(wq):
     for code in range(7):
         assert wq.wq_status_string(code).startswith("WQ_")
     assert wq.wq_status_string(99) == "WQ_ERR_UNKNOWN"
-    assert wq.wq_version() >= 100
+    assert wq.wq_version() >= 200
 
 
 FAKE = 0x10000  # never dereferenced: validation returns first
