@@ -78,8 +78,8 @@ class WeightOnly:
     """Weight-only GEMMs; with ``group_n`` the column-grouped entry points
     (one scale, and with ``asym`` one zero point, per group of columns)."""
 
-    def __init__(self, torch, wq, bits, shapes, replicas, seed=0, group_n=None, asym=False):
-        self.torch, self.bits, self.group_n, self.asym = torch, bits, group_n, asym
+    def __init__(self, torch, wq, bits, shapes, replicas, seed=0, group_n=None, asym=False, batched=False):
+        self.torch, self.bits, self.group_n, self.asym, self.batched = torch, bits, group_n, asym, batched
         if group_n:
             self.cases = [workloads.grouped_case(bits, M, K, N, group_n, asym, seed) for (M, K, N) in shapes]
             self.fn = wq.wq_gemm_w4a16_grouped if bits == 4 else wq.wq_gemm_w8a16_grouped
@@ -101,13 +101,24 @@ class WeightOnly:
         # other on one stream and each leaves it zero-filled.
         op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
         need = max(wq.wq_workspace_size(op, M, N, K) for (M, K, N) in shapes)
-        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
         tag = _wo_tag(bits, group_n, asym)
         self.calls = []
-        for i, (M, K, N) in enumerate(shapes):
-            self.calls.append({"call": f"{tag}_{M}x{K}x{N}", "index": i,
-                               "bytes": _wo_bytes(bits, M, K, N, group_n or 1, asym),
-                               "flops": 2 * M * N * K, "bound": "hbm" if M <= 64 else "tensor", "dtype": "fp16"})
+        if batched:
+            self.batch_fn = wq.wq_gemm_w4a16_batched if bits == 4 else wq.wq_gemm_w8a16_batched
+            probs = (wq.WqProblem * len(shapes))(*[
+                wq.WqProblem(M, N, K, 16, K, 16, N, 16, 1, 16, N) for (M, K, N) in shapes])
+            need = max(need, int(wq.lib.wq_batched_workspace_size(op, len(shapes), probs)))
+            self.calls.append({"call": f"{tag}_batched_" + "+".join(f"{M}x{K}x{N}" for (M, K, N) in shapes),
+                               "index": -1, "bytes": sum(_wo_bytes(bits, M, K, N) for (M, K, N) in shapes),
+                               "flops": sum(2 * M * N * K for (M, K, N) in shapes), "bound": "hbm",
+                               "dtype": "fp16", "problems": len(shapes)})
+        else:
+            for i, (M, K, N) in enumerate(shapes):
+                self.calls.append({"call": f"{tag}_{M}x{K}x{N}", "index": i,
+                                   "bytes": _wo_bytes(bits, M, K, N, group_n or 1, asym),
+                                   "flops": 2 * M * N * K, "bound": "hbm" if M <= 64 else "tensor",
+                                   "dtype": "fp16"})
+        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
 
     def _call(self, x, w, s, z, y=None):
         if self.group_n:
@@ -115,6 +126,11 @@ class WeightOnly:
         return self.fn(x, w, s, y=y, workspace=self.ws)
 
     def run(self, r, i):
+        if i < 0:  # the whole batch in one call
+            reps = self.dev[r]
+            self.batch_fn([d[0] for d in reps], [d[1] for d in reps], [d[2] for d in reps],
+                          ys=[d[3] for d in reps], workspace=self.ws)
+            return
         x, w, s, y, z = self.dev[r][i]
         self._call(x, w, s, z, y)
 
@@ -126,6 +142,13 @@ class WeightOnly:
         return out
 
     def e2e_call(self, host, i):
+        if i < 0:  # the whole batch: every problem's inputs in, every output out
+            devs = [[a.to("cuda", non_blocking=True) for a in h] for h in host]
+            ys = self.batch_fn([d[0] for d in devs], [d[1] for d in devs], [d[2] for d in devs], workspace=self.ws)
+            for y in ys:
+                y.to("cpu", non_blocking=True)
+            return (sum(a.numel() * a.element_size() for h in host for a in h),
+                    sum(y.numel() * y.element_size() for y in ys))
         dev = [a.to("cuda", non_blocking=True) for a in host[i]]
         y = self._call(dev[0], dev[1], dev[2], dev[3] if len(dev) > 3 else None)
         y.to("cpu", non_blocking=True)
@@ -134,6 +157,10 @@ class WeightOnly:
     def oracle_call(self, i):
         from oracle import wq_oracle as O
 
+        if i < 0:  # the whole batch
+            for j in range(len(self.cases)):
+                self.oracle_call(j)
+            return self.calls[0]["bytes"], self.calls[0]["flops"]
         c = self.cases[i]
         if self.group_n:
             (O.gemm_w4a16_grouped if self.bits == 4 else O.gemm_w8a16_grouped)(c.x, c.w, c.scales, c.zeros,
@@ -209,7 +236,8 @@ def make_workload(torch, wq, name, replicas, only=None):
     shapes = spec["shapes"]
     if spec["op"] in ("w4a16", "w8a16"):
         wl = WeightOnly(torch, wq, 4 if spec["op"] == "w4a16" else 8, shapes, replicas,
-                        group_n=spec.get("group_n"), asym=spec.get("asym", False))
+                        group_n=spec.get("group_n"), asym=spec.get("asym", False),
+                        batched=spec.get("batched", False))
     elif spec["op"] == "mxfp4":
         wl = MxFp4(torch, wq, shapes, replicas)
     else:

@@ -50,11 +50,24 @@ _SIGS = {
     "wq_get_device_error": [_p, ctypes.POINTER(_i)],
     "wq_version": [],
 }
+
+
+class WqProblem(ctypes.Structure):
+    """The C ABI's wq_problem: one weight-only GEMM of a batched call."""
+    _fields_ = [("M", _i), ("N", _i), ("K", _i), ("X", _p), ("ldx", _i64), ("W", _p), ("ldw", _i64),
+                ("scales", _p), ("group_n", _i), ("Y", _p), ("ldy", _i64)]
+
+
+WQ_MAX_BATCH = 8
+_SIGS["wq_gemm_w4a16_batched"] = [_i, ctypes.POINTER(WqProblem), _p, _sz, _p]
+_SIGS["wq_gemm_w8a16_batched"] = [_i, ctypes.POINTER(WqProblem), _p, _sz, _p]
+_SIGS["wq_batched_workspace_size"] = [_i, _i, ctypes.POINTER(WqProblem)]
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
     _fn.argtypes = _args
     _fn.restype = _i
 lib.wq_workspace_size.restype = _sz
+lib.wq_batched_workspace_size.restype = _sz
 lib.wq_status_string.restype = ctypes.c_char_p
 
 
@@ -173,7 +186,12 @@ def auto_workspace(op: int, M: int, N: int, K: int, device):
     (one cache entry per stream)."""
     import torch
 
-    need = wq_workspace_size(op, M, N, K)
+    return _cached_workspace(wq_workspace_size(op, M, N, K), device)
+
+
+def _cached_workspace(need: int, device):
+    import torch
+
     if need == 0:
         return None
     key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
@@ -262,6 +280,52 @@ def wq_gemm_w8a16_grouped(x, w, scales, zeros=None, group_n=1, y=None, workspace
     """Y = X * ((w - z[n // group_n]) * scales[n // group_n]); zeros int8
     [ceil(N / group_n)] or None (symmetric)."""
     return _grouped("wq_gemm_w8a16_grouped", WQ_OP_W8A16, x, w, scales, zeros, group_n, y, workspace, stream)
+
+
+def _batched(name, bits, xs, ws, scales, ys, group_n, workspace, stream):
+    import torch
+
+    count = len(xs)
+    if not (len(ws) == len(scales) == count) or (ys is not None and len(ys) != count):
+        raise WqError(WQ_ERR_INVALID_ARG, f"{name}: xs, ws, scales (and ys) must have the same length")
+    if not 1 <= count <= WQ_MAX_BATCH:
+        raise WqError(WQ_ERR_INVALID_ARG, f"{name}: 1..{WQ_MAX_BATCH} problems per call")
+    groups = list(group_n) if isinstance(group_n, (list, tuple)) else [group_n] * count
+    _require(len(groups) == count, name, "one group_n per problem")
+    probs = (WqProblem * count)()
+    outs = []
+    for i in range(count):
+        x, w, sc = xs[i], ws[i], scales[i]
+        y = ys[i] if ys is not None else None
+        _weight_only_checks(name, bits, x, w, sc, y, None, int(groups[i]))
+        _on_gpu(name, x, w, sc, y, xs[0], workspace)
+        M, K = x.shape
+        N = w.shape[1]
+        if y is None:
+            y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+        outs.append(y)
+        probs[i] = WqProblem(M, N, K, x.data_ptr(), _ld(x), w.data_ptr(), _ld(w), sc.data_ptr(), int(groups[i]),
+                             y.data_ptr(), _ld(y))
+    op = WQ_OP_W4A16 if bits == 4 else WQ_OP_W8A16
+    if workspace is None:
+        workspace = _cached_workspace(int(lib.wq_batched_workspace_size(op, count, probs)), xs[0].device)
+    wsp, wsb = _ws(workspace)
+    _check(getattr(lib, name)(count, probs, wsp, wsb, _stream(stream)), name)
+    return outs
+
+
+def wq_gemm_w4a16_batched(xs, wqs, scales, ys=None, group_n=1, workspace=None, stream=None):
+    """Several INT4 weight-only GEMMs (M <= 64 each) in one launch: for every
+    i, ys[i] = xs[i] * ((unpack(wqs[i]) - 8) * scales[i][n // group_n]).
+    Returns the list of outputs."""
+    return _batched("wq_gemm_w4a16_batched", 4, xs, wqs, scales, ys, group_n, workspace, stream)
+
+
+def wq_gemm_w8a16_batched(xs, ws, scales, ys=None, group_n=1, workspace=None, stream=None):
+    """Several INT8 weight-only GEMMs (M <= 64 each) in one launch: for every
+    i, ys[i] = xs[i] * (ws[i] * scales[i][n // group_n]).  Returns the list of
+    outputs."""
+    return _batched("wq_gemm_w8a16_batched", 8, xs, ws, scales, ys, group_n, workspace, stream)
 
 
 def mx_quantize_fp4(src, data=None, scales=None, stream=None):

@@ -73,19 +73,21 @@ constexpr int kSkinnyMaxM = 64;
 constexpr int64_t kMaxTiledM = int64_t(65535) * 128;
 
 static size_t weight_only_workspace(int bits, int M, int N, int K) {
-  return (M > 0 && M <= kSkinnyMaxM) ? wo_skinny_workspace(M, N, K, bits) : 0;
+  return (M > 0 && M <= kSkinnyMaxM) ? plan_skinny(M, N, K, bits).ws_bytes : 0;
 }
 
+// The skinny path's plan is made once here: the workspace is checked against
+// this plan's need and the same plan is launched.
 static int run_weight_only(int bits, int M, int N, int K, const void* X, int64_t ldx, const void* W, int64_t ldw,
                            const void* scales, void* Y, int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s,
                            const void* zeros = nullptr, int group_n = 1) {
   if (M == 0 || N == 0) return WQ_OK;
   if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
-  const size_t need = weight_only_workspace(bits, M, N, K);
-  if (ws_bytes < need || (need > 0 && (!ws || !aligned(ws, 16)))) return WQ_ERR_WORKSPACE;
   WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy, ws, ws_bytes, zeros, group_n};
-  if (M <= kSkinnyMaxM) return launch_status(launch_wo_skinny(a, bits, s));
-  return launch_status(launch_wo_gemm(a, bits, s));
+  if (M > kSkinnyMaxM) return launch_status(launch_wo_gemm(a, bits, s));
+  const SkinnyPlan pl = plan_skinny(M, N, K, bits);
+  if (ws_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!ws || !aligned(ws, 16)))) return WQ_ERR_WORKSPACE;
+  return launch_status(launch_wo_skinny(a, bits, pl, s));
 }
 
 }  // namespace wq
@@ -144,16 +146,50 @@ int wq_gemm_w8a16_noalloc(int M, int N, int K, const void* X, int64_t ldx, const
   int st = check_weight_only(M, N, K, X, ldx, W, ldw, scales, Y, ldy);
   if (st != WQ_OK || M == 0 || N == 0) return st;
   if (K > 0 && ldw < N) return WQ_ERR_INVALID_ARG;
-  const size_t need = weight_only_workspace(8, M, N, K);
-  if (need > kNoAllocScratchBytes) return WQ_ERR_WORKSPACE;  // beyond the built-in scratch
+  if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  void* scratch = nullptr;
-  if (need > 0) {
+  WoArgs a{M, N, K, X, ldx, W, ldw, scales, Y, ldy, nullptr, 0, nullptr, 1};
+  if (M > kSkinnyMaxM) return launch_status(launch_wo_gemm(a, 8, s));
+  // One plan for the size check and the launch.
+  const SkinnyPlan pl = plan_skinny(M, N, K, 8);
+  if (pl.ws_bytes > kNoAllocScratchBytes) return WQ_ERR_WORKSPACE;  // beyond the built-in scratch
+  if (pl.ws_bytes > 0) {
+    void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return launch_status(cudaErrorInvalidValue);
     // The array keeps the previous call's bytes: the tile counters must start at zero.
     if (cudaMemsetAsync(scratch, 0, skinny_counter_bytes(), s) != cudaSuccess) return launch_status(cudaErrorInvalidValue);
+    a.ws = scratch;
+    a.ws_bytes = kNoAllocScratchBytes;
   }
-  return run_weight_only(8, M, N, K, X, ldx, W, ldw, scales, Y, ldy, scratch, need > 0 ? kNoAllocScratchBytes : 0, s);
+  return launch_status(launch_wo_skinny(a, 8, pl, s));
+}
+
+// Batched weight-only GEMMs: every problem is checked like a single call and
+// the batch is planned once; the same plan serves the workspace check and the
+// launch.
+static int prepare_batched(int bits, int count, const wq_problem* problems, WoArgs (&a)[kMaxBatch], BatchPlan& pl) {
+  if (count < 1 || count > kMaxBatch || !problems) return WQ_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    const wq_problem& q = problems[i];
+    if (q.group_n < 1) return WQ_ERR_INVALID_ARG;
+    if (bits == 8 && q.K % 2 && q.K > 0 && q.M >= 0 && q.N >= 0) return WQ_ERR_UNSUPPORTED;
+    const int st = check_weight_only(q.M, q.N, q.K, q.X, q.ldx, q.W, q.ldw, q.scales, q.Y, q.ldy);
+    if (st != WQ_OK) return st;
+    if (q.M > 0 && q.N > 0 && q.K > 0 && q.ldw < q.N) return WQ_ERR_INVALID_ARG;
+    if (q.M > kSkinnyMaxM) return WQ_ERR_UNSUPPORTED;
+    a[i] = WoArgs{q.M, q.N, q.K, q.X, q.ldx, q.W, q.ldw, q.scales, q.Y, q.ldy, nullptr, 0, nullptr, q.group_n};
+  }
+  pl = plan_batched(a, count, bits);
+  return pl.unsupported ? WQ_ERR_UNSUPPORTED : WQ_OK;
+}
+
+static int run_batched(int bits, int count, const wq_problem* problems, void* ws, size_t ws_bytes, cudaStream_t s) {
+  WoArgs a[kMaxBatch];
+  BatchPlan pl = {};
+  const int st = prepare_batched(bits, count, problems, a, pl);
+  if (st != WQ_OK) return st;
+  if (ws_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!ws || !aligned(ws, 16)))) return WQ_ERR_WORKSPACE;
+  return launch_status(launch_wo_batched(a, count, bits, pl, ws, s));
 }
 
 int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_t* data, int64_t ld_data,
@@ -194,19 +230,37 @@ int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* 
   if (K > 0 && (!aligned(A, 16) || !aligned(B, 16) || lda % 16 || ldb % 16)) return WQ_ERR_MISALIGNED;
   // The tiled path counts its 128 x 256 tiles in 32 bits.
   if (M > kFp8SkinnyMaxM && (M > kMaxTiledM || N > kMaxTiledM)) return WQ_ERR_UNSUPPORTED;
-  const size_t need = wq_workspace_size(WQ_OP_FP8_GEMM, M, N, K);
-  if (ws_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 16)))) return WQ_ERR_WORKSPACE;
   Fp8GemmArgs a{M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, workspace, ws_bytes};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (M <= kFp8SkinnyMaxM) return launch_status(launch_fp8_skinny(a, workspace, s));
-  return launch_status(launch_fp8_gemm(a, s));
+  if (M > kFp8SkinnyMaxM) return launch_status(launch_fp8_gemm(a, s));
+  // One plan for the workspace check and the launch.
+  const SkinnyPlan pl = plan_skinny(M, N, K, 9);
+  if (ws_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!workspace || !aligned(workspace, 16)))) return WQ_ERR_WORKSPACE;
+  return launch_status(launch_fp8_skinny(a, pl, s));
+}
+
+int wq_gemm_w4a16_batched(int count, const wq_problem* problems, void* workspace, size_t ws_bytes,
+                          wq_stream_t stream) {
+  return run_batched(4, count, problems, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wq_gemm_w8a16_batched(int count, const wq_problem* problems, void* workspace, size_t ws_bytes,
+                          wq_stream_t stream) {
+  return run_batched(8, count, problems, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t wq_batched_workspace_size(int op, int count, const wq_problem* problems) {
+  if (op != WQ_OP_W4A16 && op != WQ_OP_W8A16) return 0;
+  WoArgs a[kMaxBatch];
+  BatchPlan pl = {};
+  return prepare_batched(op == WQ_OP_W4A16 ? 4 : 8, count, problems, a, pl) == WQ_OK ? pl.ws_bytes : 0;
 }
 
 size_t wq_workspace_size(int op, int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (op == WQ_OP_W4A16 && K % 2 == 0) return weight_only_workspace(4, M, N, K);
   if (op == WQ_OP_W8A16 && K % 2 == 0) return weight_only_workspace(8, M, N, K);
-  if (op == WQ_OP_FP8_GEMM && M <= kFp8SkinnyMaxM) return fp8_skinny_workspace(M, N, K);
+  if (op == WQ_OP_FP8_GEMM && M <= kFp8SkinnyMaxM) return plan_skinny(M, N, K, 9).ws_bytes;
   return 0;
 }
 
@@ -235,6 +289,6 @@ int wq_get_device_error(wq_stream_t stream, int* site) {
   return host ? WQ_ERR_DEVICE : WQ_OK;
 }
 
-int wq_version(void) { return 200; }  // 0.2.0: grouped weight-only entry points
+int wq_version(void) { return 300; }  // 0.3.0: batched weight-only entry points
 
 }  // extern "C"

@@ -59,6 +59,7 @@ enum ErrorSite : int {
   kSiteGemmEpilogue = 3,   // epilogue waited too long for the accumulator
   kSiteGemmTmemFree = 4,   // MMA issuer waited too long for the epilogue
   kSiteClusterRecv = 5,    // a CTA waited too long for its cluster peers' partial sums
+  kSiteBatchRecv = 6,      // a batched-call CTA waited too long for its neighbours' published parts
 };
 
 struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
@@ -99,23 +100,52 @@ struct Fp8GemmArgs {
   void* ws; size_t ws_bytes;  // caller scratch of the small-M path
 };
 
+// Work split of one call of the skinny weight-stream kernel, computed once
+// per call (plan_skinny) so that the workspace check and the launch see the
+// same plan.  U = tiles * chunks units over `grid` CTAs; CTA b owns units
+// [b*U/G, (b+1)*U/G).  cluster > 1: the grid is tiles * cluster CTAs in
+// clusters of that size; CTA b's run is then chunks [r ch / S, (r + 1) ch / S)
+// of tile b / S (r its rank), and the cluster adds its partial tiles through
+// distributed shared memory instead of the workspace.
+struct SkinnyPlan {
+  int n_tiles, tiles, chunks, grid, slots, cluster;
+  int64_t units;
+  int mt;           // 8-row activation groups per M tile (1 or 2): the kernel instance
+  size_t ws_bytes;  // workspace this plan needs (0: every tile finished by one CTA or one cluster)
+};
+// mode: 4 (INT4), 8 (INT8) or 9 (e4m3 B operand of the small-M FP8 GEMM).
+// An empty problem gives a zero plan.
+SkinnyPlan plan_skinny(int M, int N, int K, int mode);
+
 // Launchers (one per kernel family).  Each returns a cudaError_t from the
 // launch; argument validation happened in wq_api.cu.
-cudaError_t launch_wo_skinny(const WoArgs& a, int bits, cudaStream_t s);
+cudaError_t launch_wo_skinny(const WoArgs& a, int bits, const SkinnyPlan& pl, cudaStream_t s);
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s);
 cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_gemm(const Fp8GemmArgs& a, cudaStream_t s);
 
-// Scratch bytes the skinny path needs for this shape (0 when every tile is
-// finished by a single CTA).
-size_t wo_skinny_workspace(int M, int N, int K, int bits);
+
+
+// Batched skinny weight-only GEMMs (wo_batched.cu): up to kMaxBatch problems
+// of one weight kind in one launch.  Problems with M, N or K = 0 take no
+// units (K = 0 ones get Y = 0 from the launcher).
+constexpr int kMaxBatch = 8;
+struct BatchPlan {
+  int units;         // units of all problems
+  int grid;          // CTAs (one per SM, at most one per unit)
+  int mt;            // 8-row activation groups per M tile: 2 if any problem has M > 8
+  size_t ws_bytes;   // workspace: the tile counters and two published parts per CTA
+  bool unsupported;  // too many tiles or units for one launch
+};
+BatchPlan plan_batched(const WoArgs* probs, int count, int bits);
+cudaError_t launch_wo_batched(const WoArgs* probs, int count, int bits, const BatchPlan& pl, void* ws,
+                              cudaStream_t s);
 
 // Small-M FP8 (M <= kFp8SkinnyMaxM) runs on the skinny path as an e4m3
-// weight stream; its scratch bytes for this shape.
+// weight stream.
 constexpr int kFp8SkinnyMaxM = 16;
-size_t fp8_skinny_workspace(int M, int N, int K);
-cudaError_t launch_fp8_skinny(const Fp8GemmArgs& a, void* ws, cudaStream_t s);
+cudaError_t launch_fp8_skinny(const Fp8GemmArgs& a, const SkinnyPlan& pl, cudaStream_t s);
 
 int sm_count();
 

@@ -182,6 +182,69 @@ int wq_gemm_w8a16_grouped(int M, int N, int K, const void* X, int64_t ldx,
                           wq_stream_t stream);
 
 /*
+ * Batched weight-only GEMMs for decode-sized M: up to WQ_MAX_BATCH
+ * independent problems of one weight kind in one launch.
+ *
+ * Every problem computes what wq_gemm_w4a16 / wq_gemm_w8a16 compute ([W4A16]
+ * §二; [W8A16] Step 1 and Step 3), with group_n columns sharing one scale as
+ * for the _grouped calls (group_n = 1: per-column scales, the pages'
+ * layout); the symmetric zero points (8 for INT4, 0 for INT8) apply.  The
+ * pages have no batched call: each of their kernels computes one product.
+ * The batch exists because at M <= 16 a product moves only a few
+ * microseconds' worth of HBM traffic and every launch pays a fixed ramp and
+ * tail of the same order; one launch streams all the problems' weights
+ * back to back and pays it once.  The results equal the single calls' within
+ * the usual rounding (the K sums are split differently), and are
+ * deterministic.
+ *
+ *   count     number of problems, 1..WQ_MAX_BATCH.
+ *   problems  host array of `count` descriptors (read during the call only):
+ *               M, N, K   sizes; 0 <= M <= 64 (larger M: WQ_ERR_UNSUPPORTED);
+ *                         K even; a problem with M or N = 0 is skipped, one
+ *                         with K = 0 gets Y = 0;
+ *               X, ldx    fp16 [M, K] activations;
+ *               W, ldw    packed INT4 uint8 [K/2, N] (wq_gemm_w4a16_batched)
+ *                         or int8 [K, N] (wq_gemm_w8a16_batched);
+ *               scales    fp16 [ceil(N / group_n)];
+ *               group_n   columns per scale, >= 1;
+ *               Y, ldy    fp16 [M, N] output.
+ *             Alignment and leading-dimension rules are those of the single
+ *             calls.  No output may overlap another problem's output or any
+ *             input.
+ *   workspace, ws_bytes  device scratch of at least
+ *             wq_batched_workspace_size(op, count, problems) bytes, 16-byte
+ *             aligned: a counter area (zero-fill once before first use;
+ *             every call that returns WQ_OK leaves it zero) and the partial
+ *             tiles that neighbouring CTAs hand to each other.  Two calls in
+ *             flight at the same time must not share a workspace; after
+ *             WQ_ERR_DEVICE zero it again.  Too small: WQ_ERR_WORKSPACE.
+ * Errors: count outside 1..WQ_MAX_BATCH or problems == NULL give
+ * WQ_ERR_INVALID_ARG; each problem is checked as its single call would be.
+ */
+#define WQ_MAX_BATCH 8
+
+typedef struct wq_problem {
+  int M, N, K;
+  const void* X;
+  int64_t ldx;
+  const void* W;
+  int64_t ldw;
+  const void* scales;
+  int group_n;
+  void* Y;
+  int64_t ldy;
+} wq_problem;
+
+int wq_gemm_w4a16_batched(int count, const wq_problem* problems, void* workspace, size_t ws_bytes,
+                          wq_stream_t stream);
+int wq_gemm_w8a16_batched(int count, const wq_problem* problems, void* workspace, size_t ws_bytes,
+                          wq_stream_t stream);
+
+/* Workspace bytes a batched call needs (op = WQ_OP_W4A16 or WQ_OP_W8A16) on
+ * the current device; 0 when the batch is invalid or needs none. */
+size_t wq_batched_workspace_size(int op, int count, const wq_problem* problems);
+
+/*
  * mx_quantize_fp4 — quantize FP32 rows to MXFP4 (E2M1 elements, E8M0 scales).
  *
  * [MXFP4] §三 simulator, per 32-element block of each row:

@@ -97,6 +97,49 @@ def test_mx_and_fp8_validation(wq):
     assert L.fp8_gemm(0, 8, 32, 0, 32, 0, 16, ctypes.c_float(1), ctypes.c_float(1), 0, 8, None, 0, None) == wq.WQ_OK
 
 
+def test_problem_struct_matches_header(wq, tmp_path):
+    """The binding's wq_problem has the C layout of include/wq.h (checked with
+    the host C compiler)."""
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "wq.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu", sizeof(wq_problem), offsetof(wq_problem, X), '
+                   'offsetof(wq_problem, scales), offsetof(wq_problem, group_n), offsetof(wq_problem, ldy)); '
+                   'return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = wq.WqProblem
+    assert got == [ctypes.sizeof(P), P.X.offset, P.scales.offset, P.group_n.offset, P.ldy.offset]
+
+
+def _prob(wq, M=4, N=64, K=64, X=FAKE, ldx=64, W=FAKE, ldw=64, S=FAKE, G=1, Y=FAKE, ldy=64):
+    return wq.WqProblem(M, N, K, X, ldx, W, ldw, S, G, Y, ldy)
+
+
+def test_batched_validation(wq):
+    L = wq.lib
+    for fn in (L.wq_gemm_w4a16_batched, L.wq_gemm_w8a16_batched):
+        one = (wq.WqProblem * 1)(_prob(wq))
+        assert fn(0, one, None, 0, None) == wq.WQ_ERR_INVALID_ARG          # no problems
+        nine = (wq.WqProblem * 9)(*[_prob(wq)] * 9)
+        assert fn(9, nine, None, 0, None) == wq.WQ_ERR_INVALID_ARG         # beyond WQ_MAX_BATCH
+        assert fn(1, None, None, 0, None) == wq.WQ_ERR_INVALID_ARG
+        for bad, code in ((dict(M=65), wq.WQ_ERR_UNSUPPORTED),             # the skinny path ends at M = 64
+                          (dict(G=0), wq.WQ_ERR_INVALID_ARG),
+                          (dict(X=0), wq.WQ_ERR_INVALID_ARG),
+                          (dict(ldw=32), wq.WQ_ERR_INVALID_ARG),
+                          (dict(X=FAKE + 2), wq.WQ_ERR_MISALIGNED),
+                          (dict(ldy=68), wq.WQ_ERR_MISALIGNED)):
+            two = (wq.WqProblem * 2)(_prob(wq), _prob(wq, **bad))
+            assert fn(2, two, None, 0, None) == code, bad
+        empty = (wq.WqProblem * 2)(_prob(wq, M=0), _prob(wq, N=0))
+        assert fn(2, empty, None, 0, None) == wq.WQ_OK                       # nothing to launch
+    odd = (wq.WqProblem * 1)(_prob(wq, K=63))
+    assert L.wq_gemm_w4a16_batched(1, odd, None, 0, None) == wq.WQ_ERR_INVALID_ARG
+    assert L.wq_gemm_w8a16_batched(1, odd, None, 0, None) == wq.WQ_ERR_UNSUPPORTED
+    assert L.wq_batched_workspace_size(wq.WQ_OP_W8A16, 1, odd) == 0
+
+
 def test_workspace_query(wq):
     for op in range(5):
         assert wq.wq_workspace_size(op, 16, 4096, 4096) >= 0

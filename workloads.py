@@ -152,6 +152,16 @@ WORKLOADS = {
     # The decode sweep with one scale and one zero point per 128 columns.
     "w8a16_grouped_decode": {"op": "w8a16", "group_n": 128, "asym": True,
                              "shapes": [(m, 4096, n) for n in (4096, 14336) for m in (1, 16)]},
+    # The decode (M <= 16) calls of the Llama-7B-shaped INT4 linears.
+    "w4a16_decode": {"op": "w4a16", "shapes": [(m, k, n) for (k, n) in ((4096, 4096), (4096, 11008), (11008, 4096))
+                                               for m in (1, 8)]},
+    # The same two decode sweeps as one batched call per step (all problems of
+    # the sweep in one launch).
+    "w8a16_decode_batched": {"op": "w8a16", "batched": True,
+                             "shapes": [(m, 4096, n) for n in (4096, 14336) for m in (1, 4, 16)]},
+    "w4a16_decode_batched": {"op": "w4a16", "batched": True,
+                             "shapes": [(m, k, n) for (k, n) in ((4096, 4096), (4096, 11008), (11008, 4096))
+                                        for m in (1, 8)]},
     "w4a16_llama7b": {"op": "w4a16", "shapes": [(m, k, n) for (k, n) in ((4096, 4096), (4096, 11008), (11008, 4096))
                                                 for m in (1, 8, 64, 512, 4096)]},
     "mxfp4": {"op": "mxfp4", "shapes": [(m, 8192, 8192) for m in (128, 2048, 8192)]},
