@@ -176,7 +176,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             *reinterpret_cast<uint4*>(dst + 8 * v) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         } else {
-          for (int u = 0; u < 32 && col0 + u < p.N; ++u) dst[u] = __float2bfloat16_rn(__uint_as_float(r[u]) * scale);
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            if (col0 + u < p.N) dst[u] = __float2bfloat16_rn(__uint_as_float(r[u]) * scale);
         }
       }
     }

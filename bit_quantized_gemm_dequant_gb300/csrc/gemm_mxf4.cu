@@ -289,7 +289,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int v = 0; v < 8; ++v) red_add_v4(dst + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
         } else {
-          for (int t = 0; col0 + t < p.N; ++t) atomicAdd(dst + t, __uint_as_float(r[t]));
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (col0 + t < p.N) atomicAdd(dst + t, __uint_as_float(r[t]));
         }
         continue;
       }
@@ -301,8 +303,267 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int v = 0; v < 8; ++v)
           *reinterpret_cast<uint4*>(dst + 4 * v) = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
       } else {
-        for (int t = 0; t < 32 && col0 + t < p.N; ++t) dst[t] = __uint_as_float(r[t]);
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (col0 + t < p.N) dst[t] = __uint_as_float(r[t]);
       }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Transpose a 32 x 32 block held one row per lane (lane i: v[j] = B[i][j])
+// into one column per lane (lane j: v[i] = B[i][j]), with five butterfly
+// stages of register exchanges between lanes.
+__device__ __forceinline__ void warp_transpose32(uint32_t (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j & m) continue;
+      const uint32_t send = upper ? v[j] : v[j + m];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+      if (upper) v[j] = recv;
+      else v[j + m] = recv;
+    }
+  }
+}
+
+// Persistent variant (one CTA per SM, output tiles handed out round-robin,
+// walking down M so that the CTAs running at the same time share W tiles in
+// L2).  The ring runs continuously across a CTA's tiles.  There is one
+// accumulator (two 128 x 256 FP32 tiles and the staged scale columns do not
+// fit in TMEM together), so the epilogue hands it back as soon as it has read
+// it into registers and stores C while the next tile's MMAs run: eight
+// epilogue warps, each holding 32 rows x 128 columns.  TMEM hands each lane
+// one row; each 32 x 32 block is transposed across the warp first, so that
+// every store instruction writes one whole 128-byte row of C.  (Writing rows
+// per thread, 32 rows per instruction, either held the accumulator for a
+// third of each tile or, done after the hand-back, flooded the SM's memory
+// path and starved the next tile's TMA loads.)
+//   warp 0      TMA producer (gather mode: also the scale-chunk writer)
+//   warp 1      TMEM allocator and MMA issuer
+//   warp 2      scale-layout warp (TMA mode)
+//   warps 3-10  epilogue: warp w reads TMEM lanes 32 (w % 4) .. (the lane
+//               quarter it may access) and columns 128 ((w - 3) / 4) ..
+constexpr int kPThreads = 352;
+constexpr int kEpiWarps = 8;
+
+// Wait for an accumulator hand-off that is normally microseconds away: poll
+// with a short sleep between tries, so that the waiting warps leave the
+// shared-memory barrier unit to the roles on the critical path.  Bounded like
+// mbar_wait.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                                  int site, uint64_t limit_ns = 2000000000ull) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::globaltimer_ns();
+  for (;;) {
+    __nanosleep(256);
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (tc::globaltimer_ns() - t0 > limit_ns) {
+      if (err) atomicCAS(err, 0, site);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+template <bool kSfTma>
+__global__ void __launch_bounds__(kPThreads, 1)
+mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW,
+                   MxGemmArgs p, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* sf_ready = empty + kStages;
+  uint64_t* acc_full = sf_ready + kStages;  // MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 1;       // epilogue (4 warps) -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = p.K / 32;
+  const int KT = (p.K / 2 + BKB - 1) / BKB;
+  const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
+  const int tiles = m_tiles * n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], kSfTma ? 1 : 2);
+      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&sf_ready[s], 1);
+    }
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_empty, kEpiWarps);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tmA);
+      tc::tma_prefetch_desc(&tmW);
+      if (kSfTma) {
+        tc::tma_prefetch_desc(&tmSA);
+        tc::tma_prefetch_desc(&tmSW);
+      }
+    }
+    const bool a4 = ((reinterpret_cast<uintptr_t>(p.SA) | static_cast<uintptr_t>(p.ldsa)) & 3) == 0;
+    const bool w4 = ((reinterpret_cast<uintptr_t>(p.SW) | static_cast<uintptr_t>(p.ldsw)) & 3) == 0;
+    int it = 0, issued = 0;
+    bool go = true;
+    for (int t = blockIdx.x; t < tiles && go; t += gridDim.x) {
+      const int m0 = (t % m_tiles) * BM, n0 = (t / m_tiles) * BN;
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        const int s = it % kStages;
+        const bool free_slot = tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
+        if (!__all_sync(0xffffffffu, free_slot)) {
+          go = false;
+          break;
+        }
+        uint8_t* st = smem + s * kStageBytes;
+        uint8_t* sf = st + kABytes + kBBytes;
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + (kSfTma ? kSfBytes : 0));
+          tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
+          tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
+          if (kSfTma) {
+            const int x = kSfRowBytes * (kt / 2);
+            tc::tma_load_2d(sf, &tmSA, x, m0, &full[s]);
+            tc::tma_load_2d(sf + BM * kSfRowBytes, &tmSW, x, n0, &full[s]);
+          }
+        }
+        if (!kSfTma) {
+          const int kb0 = kt * kBlocksPerStage;
+#pragma unroll
+          for (int side = 0; side < 3; ++side) {
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = lane + 32 * i;
+              if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0, nkb, a4, lo[i], hi[i]);
+              else load_sf8(p.SW, p.ldsw, n0 + 128 * (side - 1) + r, p.N, kb0, nkb, w4, lo[i], hi[i]);
+            }
+            uint8_t* c0 = sf + side * 2 * kSfChunk;
+            *reinterpret_cast<uint4*>(c0 + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(c0 + kSfChunk + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&full[s]);
+        }
+        issued = it + 1;
+      }
+    }
+    if (*abort && lane == 0) {
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        tc::mbar_wait_drain(&full[i % kStages], (i / kStages) & 1);
+    }
+  } else if (warp == 1 && lane == 0) {
+    int it = 0, local = 0;
+    for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x, ++local) {
+      if (!tc::mbar_wait(acc_empty, (local & 1) ^ 1, abort, err, kSiteGemmTmemFree)) break;
+      tc::tc_fence_after();
+      bool ok = true;
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        const int s = it % kStages;
+        uint64_t* ready = kSfTma ? &sf_ready[s] : &full[s];
+        if (!tc::mbar_wait(ready, (it / kStages) & 1, abort, err, kSiteGemmMma)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
+        const uint32_t b = a + kABytes;
+        const uint32_t sf = b + kBBytes;
+        const uint32_t sf_col = tmem + kAccCols + s * kSfColsPerStage;
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          const int pos = (c == 3 || c == 4) ? 7 - c : c;  // chunk order 0, 1, 2, 4, 3, 5 (see mx_gemm_kernel)
+          tc::tmem_cp_32x128b_warpx4(sf_col + 4 * pos, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
+          const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
+          const uint32_t id = 2 * (j & 1);
+          const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
+          tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), (kt | j) != 0);
+        }
+        tc::tc_commit(&empty[s]);
+      }
+      if (!ok) break;
+      tc::tc_commit(acc_full);  // arrives once every MMA of the tile has completed
+    }
+  } else if (warp == 2) {
+    if (kSfTma) {
+      int it = 0;
+      bool go = true;
+      for (int t = blockIdx.x; t < tiles && go; t += gridDim.x) {
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % kStages;
+          const bool ok = tc::mbar_wait(&full[s], (it / kStages) & 1, abort, err, kSiteGemmMma);
+          if (!__all_sync(0xffffffffu, ok)) {
+            go = false;
+            break;
+          }
+          sf_to_chunks(smem + s * kStageBytes + kABytes + kBBytes, kt & 1, lane);
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sf_ready[s]);
+        }
+      }
+    }
+  } else if (warp >= 3) {
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int h = (warp - 3) >> 2;   // column half: 128 h .. 128 h + 127
+    int local = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
+      const bool ok = mbar_wait_backoff(acc_full, local & 1, abort, err, kSiteGemmEpilogue);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::tc_fence_after();
+      const int m0 = (t % m_tiles) * BM, n0 = (t / m_tiles) * BN + 128 * h;
+      const int row = m0 + 32 * q + lane;
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * h + 32 * c, r[c]);
+      tc::tmem_ld_wait();
+      // The accumulator is in registers: hand it back to the MMA warp.
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty);
+      // After the transpose lane l holds column col0 + l of rows
+      // m0 + 32 q .. m0 + 32 q + 31.
+      const int row0 = m0 + 32 * q;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = n0 + 32 * c + lane;
+        warp_transpose32(r[c], lane);
+        if (col >= p.N) continue;
+        float* dst = p.C + static_cast<int64_t>(row0) * p.ldc + col;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (row0 + i < p.M) dst[static_cast<int64_t>(i) * p.ldc] = __uint_as_float(r[c][i]);
+      }
+      (void)row;
     }
   }
   tc::tc_fence_before();
@@ -338,6 +599,22 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
     tSA = tA;  // unused by the gather variant
     tSW = tW;
   }
+  const int splits = mx_splits(a.M, a.N, a.K);
+  if (splits == 1) {  // persistent: one CTA per SM
+    auto pk = sf_tma ? mx_gemm_persistent<true> : mx_gemm_persistent<false>;
+    static PerDevice<bool> pconfigured[2];
+    bool pdone = false;
+    if (!pconfigured[sf_tma].get(pdone, [&](bool& v) {
+          e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+          v = true;
+          return e == cudaSuccess;
+        }))
+      return e;
+    const int tiles = ((a.N + BN - 1) / BN) * ((a.M + BM - 1) / BM);
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    pk<<<grid, kPThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
+    return cudaGetLastError();
+  }
   auto kern = sf_tma ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
   static PerDevice<bool> configured[2];
   bool done = false;
@@ -347,7 +624,6 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
         return e == cudaSuccess;
       }))
     return e;
-  const int splits = mx_splits(a.M, a.N, a.K);
   if (splits > 1) {  // the splits add into C
     e = cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
     if (e != cudaSuccess) return e;
