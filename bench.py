@@ -80,15 +80,16 @@ class WeightOnly:
 
     def __init__(self, torch, wq, bits, shapes, replicas, seed=0, group_n=None, asym=False, batched=False):
         self.torch, self.bits, self.group_n, self.asym, self.batched = torch, bits, group_n, asym, batched
+        self.shapes = shapes
         if group_n:
             self.cases = [workloads.grouped_case(bits, M, K, N, group_n, asym, seed) for (M, K, N) in shapes]
-            self.fn = wq.wq_gemm_w4a16_grouped if bits == 4 else wq.wq_gemm_w8a16_grouped
+            self.fn = None if wq is None else (wq.wq_gemm_w4a16_grouped if bits == 4 else wq.wq_gemm_w8a16_grouped)
         else:
             self.cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, seed)
                           for (M, K, N) in shapes]
-            self.fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+            self.fn = None if wq is None else (wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16)
         self.dev = []
-        for _ in range(replicas):
+        for _ in range(replicas if wq is not None else 0):  # wq None: host-side cases only (oracle arm)
             reps = []
             for c in self.cases:
                 z = getattr(c, "zeros", None)
@@ -99,15 +100,18 @@ class WeightOnly:
             self.dev.append(reps)
         # One zero-filled workspace serves every call: they run one after the
         # other on one stream and each leaves it zero-filled.
-        op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
-        need = max(wq.wq_workspace_size(op, M, N, K) for (M, K, N) in shapes)
         tag = _wo_tag(bits, group_n, asym)
         self.calls = []
+        need = 0
+        if wq is not None:
+            op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
+            need = max(wq.wq_workspace_size(op, M, N, K) for (M, K, N) in shapes)
         if batched:
-            self.batch_fn = wq.wq_gemm_w4a16_batched if bits == 4 else wq.wq_gemm_w8a16_batched
-            probs = (wq.WqProblem * len(shapes))(*[
-                wq.WqProblem(M, N, K, 16, K, 16, N, 16, 1, 16, N) for (M, K, N) in shapes])
-            need = max(need, int(wq.lib.wq_batched_workspace_size(op, len(shapes), probs)))
+            if wq is not None:
+                self.batch_fn = wq.wq_gemm_w4a16_batched if bits == 4 else wq.wq_gemm_w8a16_batched
+                probs = (wq.WqProblem * len(shapes))(*[
+                    wq.WqProblem(M, N, K, 16, K, 16, N, 16, 1, 16, N) for (M, K, N) in shapes])
+                need = max(need, int(wq.lib.wq_batched_workspace_size(op, len(shapes), probs)))
             self.calls.append({"call": f"{tag}_batched_" + "+".join(f"{M}x{K}x{N}" for (M, K, N) in shapes),
                                "index": -1, "bytes": sum(_wo_bytes(bits, M, K, N) for (M, K, N) in shapes),
                                "flops": sum(2 * M * N * K for (M, K, N) in shapes), "bound": "hbm",
@@ -118,7 +122,8 @@ class WeightOnly:
                                    "bytes": _wo_bytes(bits, M, K, N, group_n or 1, asym),
                                    "flops": 2 * M * N * K, "bound": "hbm" if M <= 64 else "tensor",
                                    "dtype": "fp16"})
-        self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
+        if wq is not None:
+            self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
 
     def _call(self, x, w, s, z, y=None):
         if self.group_n:
@@ -154,20 +159,30 @@ class WeightOnly:
         y.to("cpu", non_blocking=True)
         return sum(a.numel() * a.element_size() for a in host[i]), y.numel() * y.element_size()
 
-    def oracle_call(self, i):
+    def oracle_call(self, i, cols=None):
+        """Run the oracle on call i (or, i < 0, on every problem of the batch);
+        with `cols`, on the first `cols` output columns of each call only.
+        Returns the bytes and flops of the work done and what the sample was."""
         from oracle import wq_oracle as O
 
         if i < 0:  # the whole batch
+            b = f = 0
             for j in range(len(self.cases)):
-                self.oracle_call(j)
-            return self.calls[0]["bytes"], self.calls[0]["flops"]
+                bj, fj, _ = self.oracle_call(j, cols)
+                b, f = b + bj, f + fj
+            return b, f, "every problem of the batch" + (f", first {cols} columns of each" if cols else "")
         c = self.cases[i]
+        M, K, N = self.shapes[i]
+        n = N if cols is None else min(cols, N)
+        w = c.w[:, :n]
         if self.group_n:
-            (O.gemm_w4a16_grouped if self.bits == 4 else O.gemm_w8a16_grouped)(c.x, c.w, c.scales, c.zeros,
-                                                                               c.group_n)
+            g = -(-n // c.group_n)
+            z = c.zeros[:g] if c.zeros is not None else None
+            (O.gemm_w4a16_grouped if self.bits == 4 else O.gemm_w8a16_grouped)(c.x, w, c.scales[:g], z, c.group_n)
         else:
-            (O.gemm_w4a16 if self.bits == 4 else O.gemm_w8a16)(c.x, c.w, c.scales)
-        return self.calls[i]["bytes"], self.calls[i]["flops"]
+            (O.gemm_w4a16 if self.bits == 4 else O.gemm_w8a16)(c.x, w, c.scales[:n])
+        desc = "whole call" if n == N else f"first {n} of {N} columns (extrapolated)"
+        return _wo_bytes(self.bits, M, K, n, self.group_n or 1, self.asym), 2 * M * n * K, desc
 
 
 class MxFp4:
@@ -176,10 +191,12 @@ class MxFp4:
     def __init__(self, torch, wq, shapes, replicas, seed=0):
         self.torch, self.wq = torch, wq
         K, N = shapes[0][1], shapes[0][2]
+        self.K, self.N = K, N
         self.w_src = workloads.mx_source(N, K, seed=seed, stream=1)
         self.a_srcs = [workloads.mx_source(M, K, seed=seed, stream=0) for (M, _, _) in shapes]
+        self._oracle_ops = None
         self.dev = []
-        for _ in range(replicas):
+        for _ in range(replicas if wq is not None else 0):  # wq None: host-side sources only (oracle arm)
             w = torch.from_numpy(self.w_src).cuda()
             wd, wsc = wq.mx_quantize_fp4(w)
             reps = {"w": (w, wd, wsc), "a": []}
@@ -199,6 +216,30 @@ class MxFp4:
                                "bytes": (M + N) * (K // 2 + K // 32) + 4 * M * N, "flops": 2 * M * N * K,
                                "bound": "hbm" if M <= 128 else "tensor", "dtype": "fp4"})
 
+    # Oracle samples: quantize 64 rows; GEMM 4 rows of A against 256 rows of W.
+    Q_ROWS, G_ROWS_A, G_ROWS_W = 64, 4, 256
+
+    def oracle_call(self, idx):
+        from oracle import wq_oracle as O
+
+        kind, i = idx
+        K, N = self.K, self.N
+        if kind in ("qw", "qa"):
+            src = self.w_src if kind == "qw" else self.a_srcs[i]
+            r = min(self.Q_ROWS, src.shape[0])
+            O.mx_quantize_fp4(src[:r])
+            return r * K * 4 + r * K // 2 + r * K // 32, 0, f"first {r} of {src.shape[0]} rows (extrapolated)"
+        if self._oracle_ops is None:  # quantized row subsets, made once (outside the timed sample)
+            self._oracle_ops = (O.mx_quantize_fp4(self.w_src[:self.G_ROWS_W]),
+                                [O.mx_quantize_fp4(a[:self.G_ROWS_A]) for a in self.a_srcs])
+        (wd, ws), a_ops = self._oracle_ops
+        ad, asc = a_ops[i]
+        O.mx_gemm_fp4(ad, asc, wd, ws)
+        m, n = ad.shape[0], wd.shape[0]
+        M = self.a_srcs[i].shape[0]
+        return ((m + n) * (K // 2 + K // 32) + 4 * m * n, 2 * m * n * K,
+                f"{m} of {M} rows of A x {n} of {N} rows of W (extrapolated)")
+
     def run(self, r, idx):
         kind, i = idx
         d = self.dev[r]
@@ -217,14 +258,27 @@ class Fp8:
     def __init__(self, torch, wq, shapes, replicas, seed=0):
         self.torch, self.wq = torch, wq
         self.cases = [workloads.fp8_case(M, K, N, seed) for (M, K, N) in shapes]
+        self.shapes = shapes
         self.dev = []
-        for _ in range(replicas):
+        for _ in range(replicas if wq is not None else 0):  # wq None: host-side cases only (oracle arm)
             self.dev.append([(torch.from_numpy(c.a8).cuda(), torch.from_numpy(c.b8).cuda(),
                               torch.empty((c.a8.shape[0], c.b8.shape[1]), dtype=torch.bfloat16, device="cuda"))
                              for c in self.cases])
         self.calls = [{"call": f"fp8_{M}x{K}x{N}", "index": i, "bytes": M * K + K * N + 2 * M * N,
                        "flops": 2 * M * N * K, "bound": "hbm" if M <= 16 else "tensor", "dtype": "fp8"}
                       for i, (M, K, N) in enumerate(shapes)]
+
+    # Oracle sample: 8 rows of A against the first 1024 columns of B.
+    ROWS, COLS = 8, 1024
+
+    def oracle_call(self, i):
+        from oracle import wq_oracle as O
+
+        c = self.cases[i]
+        M, K, N = self.shapes[i]
+        m, n = min(self.ROWS, M), min(self.COLS, N)
+        O.fp8_gemm(c.a8[:m], c.b8[:, :n], c.scale_a, c.scale_b)
+        return m * K + K * n + 2 * m * n, 2 * m * n * K, f"{m} of {M} rows x {n} of {N} columns (extrapolated)"
 
     def run(self, r, i):
         a, b, c = self.dev[r][i]
@@ -247,6 +301,11 @@ def make_workload(torch, wq, name, replicas, only=None):
         if not wl.calls:
             raise SystemExit(f"--only {only!r} matches no call of {name}")
     return wl
+
+
+# Workloads reported in `breakdown` besides the headline one.
+BREAKDOWN = ("w8a16_decode_batched", "w4a16_decode", "w4a16_decode_batched", "w4a16_llama7b",
+             "w8a16_grouped_decode", "mxfp4", "fp8")
 
 
 def replicas_for(step_bytes):
@@ -605,12 +664,33 @@ def run_ours(args):
 
     breakdown = []
     if not args.no_breakdown and rank == 0:
-        for name in ("w4a16_llama7b", "w8a16_grouped_decode", "mxfp4", "fp8"):
+        for name in BREAKDOWN:
             if name == args.workload:
                 continue
-            other = make_workload(torch, wq, name, 1)
-            for c in time_calls_flushed(torch, other, 5, 3):
-                breakdown.append({"workload": name, **c, "roofline": roofline_for(c, peaks)})
+            decode = workloads.WORKLOADS[name].get("batched") or name.endswith("_decode")
+            reps = 1
+            if decode:  # inputs rotate over replicas, as for the headline
+                reps = replicas_for(sum(_wo_bytes(4 if workloads.WORKLOADS[name]["op"] == "w4a16" else 8, *sh)
+                                        for sh in workloads.WORKLOADS[name]["shapes"]))
+            other = make_workload(torch, wq, name, reps)
+            if decode:
+                # decode sweeps: back to back, as the headline is measured
+                steps_ms = time_steps(torch, other, 20, 5, reps, 1)
+                unit_o = _unit_of(other.calls)
+                row = {"workload": name, "call": "back-to-back step of " + ", ".join(c["call"] for c in other.calls),
+                       "bytes": sum(c["bytes"] for c in other.calls), "flops": sum(c["flops"] for c in other.calls),
+                       "bound": "hbm", "dtype": "fp16", "ms": steps_ms / 20}
+                row["roofline"] = roofline_for(row, peaks)
+                if args.cpu_budget > 0:
+                    row["cpu_baseline"] = oracle_rate(other, other.calls, unit_o, 1.5)
+                breakdown.append(row)
+            else:
+                for c in time_calls_flushed(torch, other, 5, 3):
+                    row = {"workload": name, **c, "roofline": roofline_for(c, peaks)}
+                    if args.cpu_budget > 0:
+                        row["cpu_baseline"] = oracle_rate(other, [next(x for x in other.calls if x["call"] == c["call"])],
+                                                          row["roofline"]["unit"], 0.7)
+                    breakdown.append(row)
             del other
             torch.cuda.empty_cache()
 
@@ -648,17 +728,44 @@ def cpu_baseline(wl, unit, budget_s):
         return None
     t0 = time.perf_counter()
     nbytes = nflops = ncalls = 0
+    desc = set()
     while time.perf_counter() - t0 < budget_s and ncalls < 200:
         c = wl.calls[ncalls % len(wl.calls)]
-        b, f = wl.oracle_call(c["index"])
+        b, f, d = wl.oracle_call(c["index"])
         nbytes += b
         nflops += f
         ncalls += 1
+        desc.add(d)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9 if unit == "GB/s" else nflops / dt / 1e12
     return {"value": round(value, 5), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{ncalls} oracle call(s) of the workload in order ({dt:.1f} s; numpy float64, "
-                      f"BLAS threads = cores)"}
+            "sample": f"{ncalls} oracle call(s) of the workload in order ({dt:.1f} s; {'; '.join(sorted(desc))}; "
+                      f"numpy float64, BLAS threads = cores)"}
+
+
+def oracle_rate(wl, calls, unit, budget_s):
+    """The oracle's throughput on the given calls, in `unit`, from a bounded
+    sample (each call's own oracle sample, repeated for about budget_s)."""
+    nbytes = nflops = n = 0
+    desc = set()
+    t0 = time.perf_counter()
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        for c in calls:
+            b, f, d = wl.oracle_call(c["index"])
+            nbytes, nflops = nbytes + b, nflops + f
+            desc.add(d)
+        n += 1
+        if n >= 50:
+            break
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9 if unit == "GB/s" else nflops / dt / 1e12
+    return {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} pass(es), {dt:.2f} s: " + "; ".join(sorted(desc))}
+
+
+# Column subset per weight-only call in the reference arm (the oracle's cost
+# is dequantizing W in float64, proportional to the columns).
+REF_COLS = 2048
 
 
 def run_reference(args):
@@ -666,50 +773,43 @@ def run_reference(args):
     if rank != 0:
         return
     spec = workloads.WORKLOADS[args.workload]
-    if spec["op"] not in ("w4a16", "w8a16"):
-        print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the weight-only workloads"}))
-        return
-    from oracle import wq_oracle as O
+    wl = make_workload(None, None, args.workload, 0, args.only)  # host-side inputs only
+    unit = _unit_of(wl.calls)
+    op = spec["op"]
 
-    bits = 4 if spec["op"] == "w4a16" else 8
-    shapes = spec["shapes"]
-    group_n, asym = spec.get("group_n"), spec.get("asym", False)
-    if group_n:
-        cases = [workloads.grouped_case(bits, M, K, N, group_n, asym, 0) for (M, K, N) in shapes]
-        gfn = O.gemm_w4a16_grouped if bits == 4 else O.gemm_w8a16_grouped
+    def one_step():
+        b = f = 0
+        desc = set()
+        for c in wl.calls:
+            if op in ("w4a16", "w8a16"):
+                bi, fi, d = wl.oracle_call(c["index"], cols=REF_COLS)
+            else:
+                bi, fi, d = wl.oracle_call(c["index"])
+            b, f = b + bi, f + fi
+            desc.add(d)
+        return b, f, desc
 
-        def fn(c):
-            return gfn(c.x, c.w, c.scales, c.zeros, c.group_n)
-    else:
-        cases = [(workloads.w4a16_case if bits == 4 else workloads.w8a16_case)(M, K, N, 0) for (M, K, N) in shapes]
-        pfn = O.gemm_w4a16 if bits == 4 else O.gemm_w8a16
-
-        def fn(c):
-            return pfn(c.x, c.w, c.scales)
-    # A bounded sample of the workload per step: the first `per_step` calls.
-    per_step = len(cases) if args.steps + args.warmup <= 4 else 2
-    sample_bytes = sum(_wo_bytes(bits, *shapes[i], group_n or 1, asym) for i in range(per_step))
     for _ in range(args.warmup):
-        for c in cases[:per_step]:
-            fn(c)
+        one_step()
     t0 = time.perf_counter()
+    nbytes = nflops = 0
+    desc = set()
     for _ in range(args.steps):
-        for c in cases[:per_step]:
-            fn(c)
+        b, f, d = one_step()
+        nbytes, nflops = nbytes + b, nflops + f
+        desc |= d
     dt = time.perf_counter() - t0
-    value = sample_bytes * args.steps / dt / 1e9
-    sample = f"first {per_step} call(s) of the workload per step: " + ", ".join(
-        f"{m}x{k}x{n}" for (m, k, n) in shapes[:per_step])
+    value = nbytes / dt / 1e9 if unit == "GB/s" else nflops / dt / 1e12
+    sample = "every call of the workload per step, each on the oracle's sample: " + "; ".join(sorted(desc))
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: " + ", ".join(f"{_wo_tag(bits, group_n, asym)}_{m}x{k}x{n}"
-                                                                for (m, k, n) in shapes),
+        "config": {"workload": f"{args.workload}: " + ", ".join(c["call"] for c in wl.calls),
                    "seed": 0, "parallelism": "host cores"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
@@ -728,6 +828,20 @@ def main():
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture of this build")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        # No launcher around this process: start one rank per GPU under the
+        # torch launcher (127.0.0.1 rendezvous) and pass its status on.
+        import socket
+
+        with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(args.gpus),
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+    if world is not None and int(world) != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but the launcher started {world} rank(s)")
     if args.impl == "reference":
         run_reference(args)
     else:

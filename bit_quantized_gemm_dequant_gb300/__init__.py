@@ -49,6 +49,7 @@ _SIGS = {
     "wq_status_string": [_i],
     "wq_get_device_error": [_p, ctypes.POINTER(_i)],
     "wq_version": [],
+    "wq_debug_set_wait_limit": [_i64],
 }
 
 
@@ -408,6 +409,12 @@ def wq_get_device_error(stream=None) -> tuple[int, int]:
     site = _i(0)
     st = lib.wq_get_device_error(_stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def wq_debug_set_wait_limit(ns: int) -> None:
+    """Testing hook: shorten (ns > 0) or restore (ns <= 0) the limit of the
+    skinny kernels' bounded waits."""
+    _check(lib.wq_debug_set_wait_limit(int(ns)), "wq_debug_set_wait_limit")
 
 
 def wq_version() -> int:

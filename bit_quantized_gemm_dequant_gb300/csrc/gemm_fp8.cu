@@ -56,7 +56,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;   // [2] MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;     // [2] epilogue -> MMA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* drain = acc_empty + 2;        // MMAs in flight after a give-up
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,6 +75,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc::mbar_init(&acc_full[b], 1);
       tc::mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
+    tc::mbar_init(drain, 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -137,6 +139,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
       if (!ok) break;
       tc::tc_commit(&acc_full[buf]);  // arrives once every MMA of the tile has completed
+    }
+    // After a give-up: wait (bounded) until every MMA issued so far has
+    // completed, so that none still writes TMEM when it is freed.
+    if (*abort) {
+      tc::tc_commit(drain);
+      tc::mbar_wait_drain(drain, 0);
     }
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter this warp may access

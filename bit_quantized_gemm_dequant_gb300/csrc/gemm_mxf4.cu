@@ -138,7 +138,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* empty = full + kStages;
   uint64_t* sf_ready = empty + kStages;
   uint64_t* accum = sf_ready + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* drain = accum + 1;  // MMAs in flight after a give-up
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,6 +160,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc::mbar_init(&sf_ready[s], 1);
     }
     tc::mbar_init(accum, 1);
+    tc::mbar_init(drain, 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -256,6 +258,12 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc::tc_commit(&empty[s]);
     }
     tc::tc_commit(accum);
+    // After a give-up: wait (bounded) until every MMA and scale copy issued
+    // so far has completed, so that none still uses TMEM when it is freed.
+    if (*abort) {
+      tc::tc_commit(drain);
+      tc::mbar_wait_drain(drain, 0);
+    }
   } else if (warp >= 2) {
     if (kSfTma && warp == 2) {
       // Scale-layout duty during the main loop.
@@ -386,8 +394,9 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   uint64_t* empty = full + kStages;
   uint64_t* sf_ready = empty + kStages;
   uint64_t* acc_full = sf_ready + kStages;  // MMA -> epilogue
-  uint64_t* acc_empty = acc_full + 1;       // epilogue (4 warps) -> MMA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* acc_empty = acc_full + 1;       // epilogue warps -> MMA
+  uint64_t* drain = acc_empty + 1;          // MMAs in flight after a give-up
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -404,6 +413,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
     tc::mbar_init(acc_full, 1);
     tc::mbar_init(acc_empty, kEpiWarps);
+    tc::mbar_init(drain, 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -511,6 +521,12 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       }
       if (!ok) break;
       tc::tc_commit(acc_full);  // arrives once every MMA of the tile has completed
+    }
+    // After a give-up: wait (bounded) until every MMA and scale copy issued
+    // so far has completed, so that none still uses TMEM when it is freed.
+    if (*abort) {
+      tc::tc_commit(drain);
+      tc::mbar_wait_drain(drain, 0);
     }
   } else if (warp == 2) {
     if (kSfTma) {

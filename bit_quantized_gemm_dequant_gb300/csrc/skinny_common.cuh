@@ -48,6 +48,7 @@ struct SkinnyArgs {
   void* ws;
   const void* zeros;  // weight-only: one zero point per column group, or nullptr
   int group_n;        // weight-only: columns per scale / zero-point group
+  uint64_t wait_ns = 2000000000ull;  // limit of a bounded wait before the kernel gives up
 };
 
 // The deepest per-warp ring (2..8 slots) whose slots, one 8-byte barrier

@@ -64,9 +64,37 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Bounded wait built on mbar_try_wait_sleep (same give-up rules as mbar_wait).
+// Non-blocking test of the phase with `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait built on mbar_try_wait_sleep (same give-up rules as mbar_wait):
+// each try may sleep up to 20 us.  Limits below 20 us (a testing mode) use
+// non-blocking tests instead, and a limit of 1 ns gives up at the first test
+// that finds the phase incomplete.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort, int* err_word,
                                                 int site, uint64_t limit_ns = 2000000000ull) {
+  if (limit_ns < 20000u) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (limit_ns <= 1 || globaltimer_ns() - t0 > limit_ns) {
+        if (err_word) atomicCAS(err_word, 0, site);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
   if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {

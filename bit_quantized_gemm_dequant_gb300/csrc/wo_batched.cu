@@ -53,6 +53,7 @@ struct BatchTable {
   BatchProb prob[kMaxBatch];
   int count;
   int units;
+  uint64_t wait_ns;  // limit of a bounded wait before the kernel gives up
 };
 
 struct TileRef {
@@ -238,7 +239,7 @@ wo_batched_kernel(const __grid_constant__ BatchTable tb, int* ws_count, float4* 
       }
       for (; ok && k < n_mine && warp + k * kWarps < i + seg; ++k) {
         const int s = warp * D + k % D;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait_sleep(&full[s], (k / D) & 1, abort, err, kSiteGemmMma));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait_sleep(&full[s], (k / D) & 1, abort, err, kSiteGemmMma, tb.wait_ns));
         if (!ok) break;
         const uint8_t* slot = ring + s * C::kSlotBytes;
         UnitRegs<BITS, MT> ur;
@@ -318,7 +319,7 @@ wo_batched_kernel(const __grid_constant__ BatchTable tb, int* ws_count, float4* 
           if (!got) {
             const uint64_t t0 = tc::globaltimer_ns();
             while (!(got = ld_acquire(cnt) >= bl - bf)) {
-              if (tc::globaltimer_ns() - t0 > 2000000000ull) {
+              if (tc::globaltimer_ns() - t0 > tb.wait_ns) {
                 if (err) atomicCAS(err, 0, kSiteBatchRecv);
                 *abort = 1;
                 break;
@@ -386,12 +387,14 @@ cudaError_t launch_batched_variant(const WoArgs* probs, int count, const BatchPl
   cudaError_t e = configure_batched<BITS, MT>();
   if (e != cudaSuccess) return e;
   BatchTable tb = {};
+  tb.wait_ns = skinny_wait_ns();
   int units = 0, tiles = 0, n = 0;
   for (int i = 0; i < count; ++i) {
     const WoArgs& a = probs[i];
     if (a.M == 0 || a.N == 0 || a.K == 0) continue;
     BatchProb& bp = tb.prob[n];
-    bp.a = SkinnyArgs{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, nullptr, nullptr, a.group_n};
+    bp.a = SkinnyArgs{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, nullptr, nullptr, a.group_n,
+                      tb.wait_ns};
     bp.n_tiles = (a.N + kTileN - 1) / kTileN;
     bp.tiles = bp.n_tiles * ((a.M + C::kRows - 1) / C::kRows);
     bp.chunks = (a.K + C::kChunkK - 1) / C::kChunkK;

@@ -96,7 +96,8 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   uint64_t* a_full = empty + kStages;     // 4 dequant warps wrote the TMEM A slice
   uint64_t* a_empty = a_full + kAStages;  // MMA done with the TMEM A slice (commit)
   uint64_t* accum = a_empty + kAStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* drain = accum + 1;            // MMAs in flight after a give-up
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -113,6 +114,7 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       tc::mbar_init(&a_empty[t], 1);
     }
     tc::mbar_init(accum, 1);
+    tc::mbar_init(drain, 1);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -162,6 +164,12 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         tc::tc_commit(&a_empty[t]);
       }
       tc::tc_commit(accum);
+      // After a give-up: wait (bounded) until every MMA issued so far has
+      // completed, so that none still reads or writes TMEM when it is freed.
+      if (*abort) {
+        tc::tc_commit(drain);
+        tc::mbar_wait_drain(drain, 0);
+      }
     }
   } else {
     // Dequant warps, then the epilogue.

@@ -246,7 +246,7 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 
     for (; ok && k < n_mine && warp + k * kWarps < i + seg; ++k) {
       const int s = warp * D + k % D;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait_sleep(&full[s], (k / D) & 1, abort, err, kSiteGemmMma));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait_sleep(&full[s], (k / D) & 1, abort, err, kSiteGemmMma, p.wait_ns));
       if (!ok) break;
       const uint8_t* slot = ring + s * C::kSlotBytes;
       UnitRegs<BITS, MT> ur;
@@ -569,14 +569,15 @@ SkinnyPlan plan_skinny(int M, int N, int K, int mode) {
 
 cudaError_t launch_wo_skinny(const WoArgs& a, int bits, const SkinnyPlan& pl, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
-  const SkinnyArgs sa{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, a.ws, a.zeros, a.group_n};
+  const SkinnyArgs sa{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, a.ws, a.zeros, a.group_n,
+                      skinny_wait_ns()};
   return bits == 4 ? launch_mode<kInt4>(sa, pl, s) : launch_mode<kInt8>(sa, pl, s);
 }
 
 cudaError_t launch_fp8_skinny(const Fp8GemmArgs& a, const SkinnyPlan& pl, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.C, a.ldc * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
   const SkinnyArgs sa{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, nullptr, a.scale_a * a.scale_b, a.C, a.ldc, a.ws,
-                      nullptr, 1};
+                      nullptr, 1, skinny_wait_ns()};
   return launch_mode<kE4m3>(sa, pl, s);
 }
 

@@ -3,6 +3,7 @@
 // status; no exception crosses the boundary.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -22,6 +23,12 @@ int launch_status(cudaError_t e) {
   return WQ_ERR_LAUNCH;
 }
 }  // namespace
+
+namespace {
+std::atomic<uint64_t> g_skinny_wait_ns{2000000000ull};
+}  // namespace
+
+uint64_t skinny_wait_ns() { return g_skinny_wait_ns.load(std::memory_order_relaxed); }
 
 int current_device() {
   int d = 0;
@@ -287,6 +294,11 @@ int wq_get_device_error(wq_stream_t stream, int* site) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return WQ_ERR_LAUNCH;
   if (site) *site = host;
   return host ? WQ_ERR_DEVICE : WQ_OK;
+}
+
+int wq_debug_set_wait_limit(int64_t ns) {
+  g_skinny_wait_ns.store(ns > 0 ? static_cast<uint64_t>(ns) : 2000000000ull, std::memory_order_relaxed);
+  return WQ_OK;
 }
 
 int wq_version(void) { return 300; }  // 0.3.0: batched weight-only entry points

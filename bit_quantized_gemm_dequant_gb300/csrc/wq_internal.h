@@ -47,6 +47,10 @@ class PerDevice {
   T value_[kMaxDevices] = {};
 };
 
+// Limit of the skinny kernels' bounded waits (2 s unless a test shortened it
+// with wq_debug_set_wait_limit).
+uint64_t skinny_wait_ns();
+
 // Device error word written by kernels whose bounded waits give up.  Lives in
 // wq_api.cu; kernels receive its device address as a parameter.
 int* device_error_word();

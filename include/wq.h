@@ -335,6 +335,21 @@ const char* wq_status_string(int status);
  */
 int wq_get_device_error(wq_stream_t stream, int* site);
 
+/*
+ * wq_debug_set_wait_limit — testing hook: the limit (in nanoseconds) after
+ * which the skinny weight-stream kernels (wq_gemm_w4a16, wq_gemm_w8a16, their
+ * _grouped, _noalloc and _batched forms, and fp8_gemm at M <= 16) give up a
+ * bounded wait, record the site in the device error word (see
+ * wq_get_device_error) and return, instead of waiting on.  ns <= 0 restores
+ * the default of 2 s.  Applies to calls launched afterwards, from any host
+ * thread.  With a very short limit a call gives up almost at once and its
+ * output is not computed; nothing is left in flight when it returns, and the
+ * next call with the default limit computes normally.  The pages have no
+ * counterpart: it exists so that tests can exercise the give-up path without
+ * faulting or hanging a GPU.  Always returns WQ_OK.
+ */
+int wq_debug_set_wait_limit(int64_t ns);
+
 /* Library version, as major * 10000 + minor * 100 + patch. */
 int wq_version(void);
 

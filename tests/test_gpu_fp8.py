@@ -50,13 +50,13 @@ def test_fp8_cases(wq, M, K, N, lda, ldb, ldc):
 
 
 @pytest.mark.parametrize("S", [4096, 8192])
-def test_fp8_square_sampled_rows(wq, S):
+def test_fp8_square_every_element(wq, S):
+    """The square FP8 workloads at full size, every output element against the
+    oracle (every 128 x 256 tile of the persistent kernel, both TMEM
+    accumulators)."""
     case = workloads.fp8_case(S, S, S, seed=0)
     c = _run(wq, case)
-    rows = np.random.default_rng(S).choice(S, 40, replace=False)
-    rows[:3] = [0, 127, S - 1]
-    ref = O.fp8_gemm(case.a8, case.b8, case.scale_a, case.scale_b, rows=rows)
-    assert_gemm_close(c[torch.from_numpy(rows).cuda()], ref, "bf16")
+    assert_gemm_close(c, O.fp8_gemm(case.a8, case.b8, case.scale_a, case.scale_b), "bf16")
 
 
 def test_fp8_identity_and_k_zero(wq):

@@ -75,13 +75,7 @@ def test_w8a16_decode_full_size(wq, M, K, N):
 def test_w4a16_llama_shapes(wq, M, K, N):
     case = workloads.w4a16_case(M, K, N, seed=0)
     y = _run(wq, 4, case)
-    if M <= 64:
-        assert_gemm_close(y, _ref(4, case), "fp16")
-    else:
-        rows = np.random.default_rng(M).choice(M, 48, replace=False)
-        rows[:2] = [0, M - 1]
-        # the bound's max|y_ref| term is taken over the sampled rows only
-        assert_gemm_close(y[torch.from_numpy(rows).cuda()], _ref(4, case, rows), "fp16")
+    assert_gemm_close(y, _ref(4, case), "fp16")  # every element, at every M
 
 
 @pytest.mark.parametrize("bits", [4, 8])
@@ -137,12 +131,36 @@ def test_large_m_cases(wq, bits, M, K, N, ldx, ldw, ldy):
 
 
 @pytest.mark.parametrize("M,K,N", [(4096, 4096, 4096), (4096, 4096, 14336)])
-def test_w8a16_large_m_sampled(wq, M, K, N):
+def test_w8a16_large_m_every_element(wq, M, K, N):
     case = workloads.w8a16_case(M, K, N, seed=1)
-    y = _run(wq, 8, case)
-    rows = np.random.default_rng(N).choice(M, 32, replace=False)
-    rows[:2] = [0, M - 1]
-    assert_gemm_close(y[torch.from_numpy(rows).cuda()], _ref(8, case, rows), "fp16")
+    assert_gemm_close(_run(wq, 8, case), _ref(8, case), "fp16")
+
+
+# Activations with a non-zero mean.  The INT8 skinny path feeds the tensor
+# cores 1152 + q and removes 1152 * sum(x) afterwards; that cancellation grows
+# with |sum(x)|, which zero-mean activations keep small.  Long K and shifted
+# activations check it against the tolerance (the tensor-memory path, M > 64,
+# subtracts before its MMAs and is checked too).
+SHIFTED = [(1, 14336, 4096), (16, 14336, 4096), (16, 11008, 1024), (100, 14336, 512)]
+
+
+@pytest.mark.parametrize("kind", ["normal_mean2", "uniform01"])
+@pytest.mark.parametrize("M,K,N", SHIFTED)
+def test_int8_shifted_activations_long_k(wq, kind, M, K, N):
+    base = workloads.w8a16_case(M, K, N, seed=13)
+    case = workloads.WeightOnlyCase(workloads.activations_fp16_shifted(M, K, kind, seed=13), base.w, base.scales, 8)
+    assert_gemm_close(_run(wq, 8, case), _ref(8, case), "fp16")
+
+
+@pytest.mark.parametrize("kind", ["normal_mean2", "uniform01"])
+@pytest.mark.parametrize("M,K,N", SHIFTED)
+def test_int8_shifted_activations_grouped_zero_points(wq, kind, M, K, N):
+    g = workloads.grouped_case(8, M, K, N, 128, True, seed=17)
+    x = workloads.activations_fp16_shifted(M, K, kind, seed=17)
+    y = wq.wq_gemm_w8a16_grouped(torch.from_numpy(x).cuda(), torch.from_numpy(g.w).cuda(),
+                                 torch.from_numpy(g.scales).cuda(), torch.from_numpy(g.zeros).cuda(), 128)
+    torch.cuda.synchronize()
+    assert_gemm_close(y, O.gemm_w8a16_grouped(x, g.w, g.scales, g.zeros, 128), "fp16")
 
 
 @pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 512), (4, 1, 11008, 512), (4, 64, 4096, 256)])

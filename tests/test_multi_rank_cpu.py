@@ -79,3 +79,26 @@ def test_reference_arm_under_launcher_prints_one_line():
     assert line["value"] > 0 and line["unit"] == "GB/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gpus_flag_without_launcher_starts_the_ranks():
+    """`bench.py --gpus 2` run bare (no launcher in the environment) starts
+    two ranks itself; rank 0 reports n_gpus = 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["OMP_NUM_THREADS"] = "1"
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "w4a16_tiny", "--steps", "1",
+           "--warmup", "3", "--gpus", "2"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "w4a16_tiny", "--steps", "1",
+           "--warmup", "3", "--gpus", "4"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "--gpus 4" in r.stderr

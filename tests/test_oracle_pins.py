@@ -450,6 +450,58 @@ def test_fp8_bruteforce_exact_rational():
 # ----------------------------------------------------------- tolerance helper
 
 
+def _tolerance_golden():
+    import json
+
+    with open(os.path.join(GOLDEN, "tolerance_worked.json")) as f:
+        return json.load(f)
+
+
+def check_tolerance_worked(tol_fn):
+    g = _tolerance_golden()
+    y = np.array(g["y_ref"], dtype=np.float64)
+    for dtype, want in g["tol"].items():
+        assert np.array_equal(tol_fn(y, dtype), np.array(want)), dtype
+    t = g["tiny_fp16"]
+    want = np.array(t["tol"]) + t["first_term"]
+    assert np.allclose(tol_fn(np.array(t["y_ref"]), "fp16"), want, rtol=1e-12, atol=0)
+
+
+def test_gemm_tolerance_worked_example():
+    """The comparison rule every GPU parity test rests on, against hand-worked
+    values (tests/golden/tolerance_worked.json)."""
+    check_tolerance_worked(O.gemm_tolerance)
+
+
+def _mutant_tol_per_element(y_ref, dtype, rel=5e-3):
+    y = np.asarray(y_ref, dtype=np.float64)
+    return rel * np.abs(y) + O.ulp(y, dtype)
+
+
+def _mutant_tol_row_max(y_ref, dtype, rel=5e-3):
+    y = np.asarray(y_ref, dtype=np.float64)
+    return rel * np.abs(y).max(axis=-1, keepdims=True) + O.ulp(y, dtype)
+
+
+def _mutant_tol_ulp_no_subnormal(y_ref, dtype, rel=5e-3):
+    y = np.asarray(y_ref, dtype=np.float64)
+    mant = {"fp16": 10, "bf16": 7, "fp32": 23}[dtype]
+    _, x = np.frexp(np.where(y != 0, np.abs(y), np.finfo(np.float64).tiny))
+    return rel * np.abs(y).max() + np.ldexp(1.0, (x - 1 - mant).astype(np.int64))
+
+
+def _mutant_tol_ulp_exponent_off(y_ref, dtype, rel=5e-3):
+    y = np.asarray(y_ref, dtype=np.float64)
+    return rel * np.abs(y).max() + 2.0 * O.ulp(y, dtype)
+
+
+@pytest.mark.parametrize("mutant", [_mutant_tol_per_element, _mutant_tol_row_max, _mutant_tol_ulp_no_subnormal,
+                                    _mutant_tol_ulp_exponent_off])
+def test_gemm_tolerance_pin_catches_planted_mistakes(mutant):
+    with pytest.raises(AssertionError):
+        check_tolerance_worked(mutant)
+
+
 def test_ulp_matches_numpy_spacing():
     for dt, name in ((np.float16, "fp16"), (np.float32, "fp32")):
         vals = np.array([1.0, 1.5, 1000.0, 3e-3, 0.0, -7.25], dt)

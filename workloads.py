@@ -34,6 +34,19 @@ def activations_fp16(m: int, k: int, seed: int = 0) -> np.ndarray:
     return _rng(seed, _X_STREAM, m, k).standard_normal((m, k), dtype=np.float32).astype(np.float16)
 
 
+def activations_fp16_shifted(m: int, k: int, kind: str, seed: int = 0) -> np.ndarray:
+    """X fp16 [m, k] with a non-zero mean: "normal_mean2" draws N(2, 1),
+    "uniform01" draws U(0, 1) (both in float32, rounded to fp16)."""
+    g = _rng(seed, _X_STREAM, 7, m, k)
+    if kind == "normal_mean2":
+        v = g.standard_normal((m, k), dtype=np.float32) + np.float32(2.0)
+    elif kind == "uniform01":
+        v = g.random((m, k), dtype=np.float32)
+    else:
+        raise ValueError(kind)
+    return v.astype(np.float16)
+
+
 def int4_codes_packed(k: int, n: int, seed: int = 0) -> np.ndarray:
     """Packed INT4 weights uint8 [k/2, n]: codes uniform on 0..15, the code for
     even k in the low nibble and odd k in the high nibble."""
