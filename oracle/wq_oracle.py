@@ -307,6 +307,116 @@ def fp8_gemm(a8: np.ndarray, b8: np.ndarray, scale_a: float, scale_b: float,
 
 
 # --------------------------------------------------------------------------
+# NVFP4 (W4A16 page, §三 "Blackwell 第五代 Tensor Core NVFP4 指令实操": E2M1
+# elements under a two-level block scaling, an FP8 local scale per block of
+# elements inside a tensor-wide scale, executed natively by the tensor cores).
+# The page gives no block size or scale encoding; the reading taken here is:
+# 16-element blocks along the contiguous dimension, an unsigned E4M3 scale per
+# block, and a float32 scale per tensor that maps the tensor's amax onto the
+# largest block scale times the largest element (448 x 6).  Elements are
+# chosen exactly as the MXFP4 page's simulator chooses them (nearest E2M1 grid
+# point, the smaller magnitude on a tie, sign bit = x < 0).
+# --------------------------------------------------------------------------
+
+NV_BLOCK = 16
+NV_SCALE_RANGE = np.float32(E2M1_MAX * E4M3_MAX)  # 6 * 448 = 2688
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """Non-negative values -> e4m3fn bytes: round to the nearest finite e4m3
+    value, ties to the even code, saturating at 448 (0x7E).
+
+    The 127 non-negative finite codes 0x00..0x7E decode to increasing values,
+    so the result is a search over that table (exact in float64)."""
+    v = np.asarray(values, dtype=np.float64)
+    if (v < 0).any() or np.isnan(v).any():
+        raise ValueError("e4m3_encode takes non-negative numbers")
+    table = e4m3_decode(np.arange(0x7F))
+    hi = np.clip(np.searchsorted(table, v, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_lo, d_hi = np.abs(v - table[lo]), np.abs(table[hi] - v)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    return np.where(v >= E4M3_MAX, 0x7E, code).astype(np.uint8)
+
+
+def nv_tensor_scale(src: np.ndarray) -> np.float32:
+    """The tensor-wide scale g = amax / (6 * 448) in float32 (1 for an all-zero
+    tensor): the largest block then gets the largest block scale, 448."""
+    amax = np.float32(np.abs(np.asarray(src, dtype=np.float32)).max()) if np.size(src) else np.float32(0)
+    return np.float32(1.0) if amax == 0 else np.float32(amax / NV_SCALE_RANGE)
+
+
+def nv_quantize_fp4(src: np.ndarray, g=None):
+    """Quantize float32 ``[R, C]`` (C % 16 == 0) to NVFP4, in float32 steps:
+
+    1. g = nv_tensor_scale(src) unless given;
+    2. per 16-element block: amax = max |x|; the block scale
+       s = e4m3(amax / (6 g)) (the division in float32, 6 g rounded to
+       float32 first; round to nearest even, saturating at 448);
+    3. d = s * g in float32; a block whose scale is 0 gets code 0 everywhere;
+    4. v = x / d in float32; code magnitude = the nearest E2M1 grid point to
+       |v|, the first (smaller) one on a tie; sign bit = x < 0.
+
+    Returns ``(data, scales, g)``: data uint8 ``[R, C/2]`` (element 2t in the
+    low nibble of byte t, as for MXFP4), e4m3 block scales uint8 ``[R, C/16]``
+    and g (float32)."""
+    x = np.asarray(src, dtype=np.float32)
+    rows, cols = x.shape
+    if cols % NV_BLOCK:
+        raise ValueError("cols must be a multiple of 16")
+    g = nv_tensor_scale(x) if g is None else np.float32(g)
+    blocks = x.reshape(rows, cols // NV_BLOCK, NV_BLOCK)
+    amax = np.abs(blocks).max(axis=-1) if cols else np.zeros((rows, 0), np.float32)
+    sb_f = (amax / np.float32(np.float32(6.0) * g)).astype(np.float32)
+    sb = e4m3_encode(sb_f)
+    d = (e4m3_decode(sb).astype(np.float32) * g).astype(np.float32)
+    safe = np.where(d > 0, d, np.float32(1.0)).astype(np.float32)
+    v = (blocks / safe[..., None]).astype(np.float32)
+    grid = np.asarray(E2M1_GRID, dtype=np.float32)
+    dist = np.abs(np.abs(v)[..., None] - grid).astype(np.float32)
+    j = np.argmin(dist, axis=-1).astype(np.uint8)
+    sign = (blocks < 0).astype(np.uint8)
+    codes = np.where((d > 0)[..., None], (sign << 3) | j, 0).astype(np.uint8).reshape(rows, cols)
+    data = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return data, sb, g
+
+
+def nv_dequantize(data: np.ndarray, scales: np.ndarray, g) -> np.ndarray:
+    """x_hat = e2m1(code) * e4m3(scale of its 16-element block) * g, float64."""
+    vals = e2m1_decode(mx_unpack_codes(data))
+    rows, cols = vals.shape
+    s = e4m3_decode(scales)[..., None]
+    return (vals.reshape(rows, cols // NV_BLOCK, NV_BLOCK) * s).reshape(rows, cols) * float(np.float32(g))
+
+
+def nv_gemm_fp4(a_data, a_scales, ga, w_data, w_scales, gw, rows=None) -> np.ndarray:
+    """C = A @ W^T for NVFP4 operands, float64: for every output (m, n) and
+    every 16-element K block b,
+
+        dC = e4m3(sA[m, b]) * e4m3(sW[n, b]) * sum_{i<16} a[m, b, i] * w[n, b, i],
+
+    C = ga * gw * sum_b dC (the block dot, then its two block scales, then
+    the running sum, then the two tensor scales).  A ``[M, K/2]`` +
+    ``[M, K/16]``, W ``[N, K/2]`` + ``[N, K/16]``, both K-contiguous; ``rows``
+    optionally restricts the output to a subset of A's rows."""
+    ca = e2m1_decode(mx_unpack_codes(a_data))
+    cw = e2m1_decode(mx_unpack_codes(w_data))
+    sa = e4m3_decode(a_scales)
+    sw = e4m3_decode(w_scales)
+    if rows is not None:
+        ca, sa = ca[rows], sa[rows]
+    m, k = ca.shape
+    n = cw.shape[0]
+    out = np.zeros((m, n), dtype=np.float64)
+    for b in range(k // NV_BLOCK):
+        sl = slice(b * NV_BLOCK, (b + 1) * NV_BLOCK)
+        block_dot = ca[:, sl] @ cw[:, sl].T  # exact: small dyadic rationals
+        out += block_dot * (sa[:, b][:, None] * sw[:, b][None, :])
+    return out * (float(np.float32(ga)) * float(np.float32(gw)))
+
+
+# --------------------------------------------------------------------------
 # Output rounding and the comparison rule
 # --------------------------------------------------------------------------
 

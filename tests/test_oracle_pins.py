@@ -11,6 +11,7 @@ from fractions import Fraction
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import wq_oracle as O
 
@@ -448,6 +449,223 @@ def test_fp8_bruteforce_exact_rational():
 
 
 # ----------------------------------------------------------- tolerance helper
+
+
+# ------------------------------------------------------------------- NVFP4
+
+
+def _nv_golden():
+    with open(os.path.join(GOLDEN, "nvfp4_worked.json")) as f:
+        return json.load(f)
+
+
+def test_e4m3_encode_round_trip_and_midpoints():
+    """Every finite non-negative e4m3 value encodes to its own code; a value
+    halfway between two neighbours goes to the even code; values from 448 up
+    saturate at 0x7E."""
+    codes = np.arange(0x7F)
+    vals = O.e4m3_decode(codes)
+    assert np.array_equal(O.e4m3_encode(vals), codes)
+    mids = (vals[:-1] + vals[1:]) / 2
+    want = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[1:])
+    assert np.array_equal(O.e4m3_encode(mids), want)
+    assert (O.e4m3_encode([448.0, 460.0, 1e6]) == 0x7E).all()
+
+
+def test_e4m3_encode_against_torch():
+    """The encoder against PyTorch's float8_e4m3fn cast (round to nearest even)
+    on random float32 values below the cast's overflow point."""
+    r = np.random.default_rng(5).uniform(0, 463.9, 100000).astype(np.float32)
+    r = np.concatenate([r, np.ldexp(np.float32(1), np.arange(-12, 9)).astype(np.float32)])
+    ref = torch.from_numpy(r).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(r), ref)
+
+
+def check_nv_quantize_golden(quant=None):
+    quant = quant or O.nv_quantize_fp4
+    q = _nv_golden()["quantize"]
+    src = np.array(q["src"], dtype=np.float32)
+    src[0, 21] = np.float32(-0.0)
+    d, s, g = quant(src)
+    assert float(g) == q["g"]
+    assert np.array_equal(d, np.array(q["data"], np.uint8))
+    assert np.array_equal(s, np.array(q["scales"], np.uint8))
+    assert np.array_equal(O.nv_dequantize(d, s, g)[0], np.array(q["dequantized_row0"]))
+
+
+def test_nv_quantize_worked_example():
+    check_nv_quantize_golden()
+
+
+def _nv_bruteforce(src):
+    """Exhaustive reference on a small tensor: for every element, search all 16
+    codes for the one whose value (times the block's decoded scale and g, in
+    exact rationals) is nearest to x / (s g) computed in float32, preferring
+    the smaller magnitude on ties."""
+    x = np.asarray(src, dtype=np.float32)
+    g = O.nv_tensor_scale(x)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), np.int64)
+    scales = np.zeros((rows, cols // 16), np.uint8)
+    for r in range(rows):
+        for b in range(cols // 16):
+            blk = x[r, 16 * b:16 * b + 16]
+            sb_f = np.float32(np.abs(blk).max() / np.float32(np.float32(6) * g))
+            sb = int(O.e4m3_encode([sb_f])[0])
+            scales[r, b] = sb
+            d = np.float32(np.float32(O.e4m3_decode(np.array([sb]))[0]) * g)
+            for i, xv in enumerate(blk):
+                if d == 0:
+                    continue
+                v = Fraction(float(np.float32(xv / d)))
+                best = None
+                for mag in range(8):
+                    dist = abs(abs(v) - Fraction(O.E2M1_GRID[mag]))
+                    if best is None or dist < best[0]:
+                        best = (dist, mag)
+                codes[r, 16 * b + i] = (8 if xv < 0 else 0) | best[1]
+    data = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return data, scales, g
+
+
+def check_nv_quantize_bruteforce(quant=None):
+    quant = quant or O.nv_quantize_fp4
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((3, 64)) * rng.choice([1e-3, 1.0, 300.0], size=(3, 1))).astype(np.float32)
+    x[0, :16] = np.float32([0.75, 1.75, 3.5, -0.25, 5.0, 2.5, 1.25, 6.0, 0, 0, 0, 0, 0, 0, 0, 0.1])
+    d, s, g = quant(x)
+    rd, rs, rg = _nv_bruteforce(x)
+    assert g == rg and np.array_equal(s, rs) and np.array_equal(d, rd)
+
+
+def test_nv_quantize_bruteforce_exact_rational():
+    check_nv_quantize_bruteforce()
+
+
+def test_nv_quantize_error_bound_invariant():
+    """|x - x_hat| <= half the local grid spacing at the block's scale, plus
+    the clamp when the rounded block scale fell below amax / 6."""
+    x = (np.random.default_rng(8).standard_normal((16, 256)) * 3).astype(np.float32)
+    d, s, g = O.nv_quantize_fp4(x)
+    xh = O.nv_dequantize(d, s, g)
+    scale = np.repeat(O.e4m3_decode(s), 16, axis=1) * float(g)
+    v = np.abs(x.astype(np.float64)) / scale
+    half_step = np.where(v < 2, 0.25, np.where(v < 4, 0.5, 1.0))
+    bound = (half_step + np.maximum(v - 6.0, 0)) * scale
+    assert (np.abs(xh - x) <= bound * (1 + 1e-6) + 1e-300).all()
+
+
+def check_nv_gemm_worked(gemm=None):
+    gemm = gemm or O.nv_gemm_fp4
+    q = _nv_golden()["gemm"]
+    c = gemm(np.array(q["a_data"], np.uint8), np.array(q["a_scales"], np.uint8), q["ga"],
+             np.array(q["w_data"], np.uint8), np.array(q["w_scales"], np.uint8), q["gw"])
+    assert np.array_equal(c, np.array(q["c"]))
+
+
+def test_nv_gemm_worked_example():
+    check_nv_gemm_worked()
+
+
+def check_nv_gemm_bruteforce(gemm=None):
+    """2 x 64 operands (the MXFP4 page's demo shape) in exact rationals."""
+    gemm = gemm or O.nv_gemm_fp4
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((2, 64)).astype(np.float32)
+    w = (rng.standard_normal((2, 64)) * 40).astype(np.float32)
+    ad, asc, ga = O.nv_quantize_fp4(a)
+    wd, wsc, gw = O.nv_quantize_fp4(w)
+    ca, cw = O.mx_unpack_codes(ad), O.mx_unpack_codes(wd)
+    out = np.zeros((2, 2))
+    for m in range(2):
+        for n in range(2):
+            tot = Fraction(0)
+            for k in range(64):
+                b = k // 16
+                tot += (Fraction(float(O.e2m1_decode(ca[m, k]))) * Fraction(float(O.e2m1_decode(cw[n, k])))
+                        * Fraction(float(O.e4m3_decode(asc[m, b]))) * Fraction(float(O.e4m3_decode(wsc[n, b]))))
+            out[m, n] = float(tot * Fraction(float(ga)) * Fraction(float(gw)))
+    assert np.array_equal(gemm(ad, asc, ga, wd, wsc, gw), out)
+
+
+def test_nv_gemm_bruteforce_exact_rational():
+    check_nv_gemm_bruteforce()
+
+
+def test_nv_gemm_equals_dequantize_then_matmul():
+    rng = np.random.default_rng(10)
+    a = rng.standard_normal((5, 256)).astype(np.float32)
+    w = rng.standard_normal((7, 256)).astype(np.float32)
+    ad, asc, ga = O.nv_quantize_fp4(a)
+    wd, wsc, gw = O.nv_quantize_fp4(w)
+    ref = O.nv_dequantize(ad, asc, ga) @ O.nv_dequantize(wd, wsc, gw).T
+    assert np.allclose(O.nv_gemm_fp4(ad, asc, ga, wd, wsc, gw), ref, rtol=1e-13, atol=0)
+
+
+def _mutant_nv_block32(src, g=None):
+    """Block scales from 32-element blocks (each shared by two 16-element halves)."""
+    x = np.asarray(src, np.float32)
+    g2 = O.nv_tensor_scale(x) if g is None else np.float32(g)
+    amax32 = np.repeat(np.abs(x.reshape(x.shape[0], -1, 32)).max(axis=-1), 2, axis=1)
+    sb = O.e4m3_encode((amax32 / np.float32(np.float32(6) * g2)).astype(np.float32))
+    d = (O.e4m3_decode(sb).astype(np.float32) * g2).astype(np.float32)
+    blocks = x.reshape(x.shape[0], -1, 16)
+    v = (blocks / np.where(d > 0, d, 1)[..., None]).astype(np.float32)
+    grid = np.asarray(O.E2M1_GRID, np.float32)
+    j = np.argmin(np.abs(np.abs(v)[..., None] - grid), axis=-1)
+    codes = np.where((d > 0)[..., None], ((blocks < 0) << 3) | j, 0).reshape(x.shape).astype(np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), sb, g2
+
+
+def _mutant_nv_ties_up(src, g=None):
+    x = np.asarray(src, np.float32)
+    d, s, g2 = O.nv_quantize_fp4(x, g)
+    return O.nv_quantize_fp4((x * np.float32(1.0000001)).astype(np.float32), g2)
+
+
+def _mutant_nv_no_tensor_scale(src, g=None):
+    return O.nv_quantize_fp4(src, np.float32(1.0))
+
+
+def _mutant_nv_scale_floor(src, g=None):
+    x = np.asarray(src, np.float32)
+    _, _, g2 = O.nv_quantize_fp4(x, g)
+    blocks = x.reshape(x.shape[0], -1, 16)
+    sb_f = (np.abs(blocks).max(axis=-1) / np.float32(np.float32(6) * g2)).astype(np.float32)
+    table = O.e4m3_decode(np.arange(0x7F))
+    sb = np.clip(np.searchsorted(table, sb_f, side="right") - 1, 0, 0x7E).astype(np.uint8)
+    d = (O.e4m3_decode(sb).astype(np.float32) * g2).astype(np.float32)
+    out = O.nv_quantize_fp4(x, g2)
+    return out[0] if (d == 0).all() else out[0], sb, g2
+
+
+def _mutant_nv_gemm_no_tensor_scales(ad, asc, ga, wd, wsc, gw, rows=None):
+    return O.nv_gemm_fp4(ad, asc, 1.0, wd, wsc, 1.0, rows)
+
+
+def _mutant_nv_gemm_w_nibbles_swapped(ad, asc, ga, wd, wsc, gw, rows=None):
+    """W's element pairs read in the wrong order (A's in the right one)."""
+    sw = ((np.asarray(wd, np.uint8) >> 4) | (np.asarray(wd, np.uint8) << 4)).astype(np.uint8)
+    return O.nv_gemm_fp4(ad, asc, ga, sw, wsc, gw, rows)
+
+
+@pytest.mark.parametrize("mutant,checks", [
+    (_mutant_nv_block32, [check_nv_quantize_golden, check_nv_quantize_bruteforce]),
+    (_mutant_nv_ties_up, [check_nv_quantize_golden]),
+    (_mutant_nv_no_tensor_scale, [check_nv_quantize_bruteforce]),
+    (_mutant_nv_scale_floor, [check_nv_quantize_golden, check_nv_quantize_bruteforce]),
+])
+def test_nv_quantize_pins_catch_planted_mistakes(mutant, checks):
+    for check in checks:
+        with pytest.raises(AssertionError):
+            check(mutant)
+
+
+@pytest.mark.parametrize("mutant", [_mutant_nv_gemm_no_tensor_scales, _mutant_nv_gemm_w_nibbles_swapped])
+def test_nv_gemm_pins_catch_planted_mistakes(mutant):
+    for check in (check_nv_gemm_worked, check_nv_gemm_bruteforce):
+        with pytest.raises(AssertionError):
+            check(mutant)
 
 
 def _tolerance_golden():
