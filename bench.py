@@ -254,6 +254,77 @@ class MxFp4:
             self.wq.mx_gemm_fp4(ad, asc, wd, wsc, c=c)
 
 
+class NvFp4:
+    """Per M: quantize A [M, K] and W [N, K] to NVFP4 on the device, then C = A W^T."""
+
+    def __init__(self, torch, wq, shapes, replicas, seed=0):
+        self.torch, self.wq = torch, wq
+        K, N = shapes[0][1], shapes[0][2]
+        self.K, self.N = K, N
+        self.w_src = workloads.mx_source(N, K, seed=seed, stream=1)
+        self.a_srcs = [workloads.mx_source(M, K, seed=seed, stream=0) for (M, _, _) in shapes]
+        self._oracle_ops = None
+        self.dev = []
+        for _ in range(replicas if wq is not None else 0):  # wq None: host-side sources only (oracle arm)
+            w = torch.from_numpy(self.w_src).cuda()
+            wd, wsc, gw = wq.nv_quantize_fp4(w)
+            reps = {"w": (w, wd, wsc, gw), "a": []}
+            for a_src in self.a_srcs:
+                a = torch.from_numpy(a_src).cuda()
+                ad, asc, ga = wq.nv_quantize_fp4(a)
+                c = torch.empty((a.shape[0], N), dtype=torch.float32, device="cuda")
+                reps["a"].append((a, ad, asc, ga, c))
+            self.dev.append(reps)
+
+        def qbytes(r):  # the source twice (amax, then codes), codes and E4M3 scales out
+            return r * K * 8 + r * K // 2 + r * K // 16
+
+        self.calls = [{"call": f"nv_quantize_{N}x{K}", "index": ("qw", 0), "bytes": qbytes(N), "flops": 0,
+                       "bound": "hbm", "dtype": "fp4"}]
+        for i, (M, _, _) in enumerate(shapes):
+            self.calls.append({"call": f"nv_quantize_{M}x{K}", "index": ("qa", i), "bytes": qbytes(M), "flops": 0,
+                               "bound": "hbm", "dtype": "fp4"})
+            self.calls.append({"call": f"nv_gemm_{M}x{K}x{N}", "index": ("g", i),
+                               "bytes": (M + N) * (K // 2 + K // 16) + 4 * M * N, "flops": 2 * M * N * K,
+                               "bound": "hbm" if M <= 128 else "tensor", "dtype": "fp4"})
+
+    Q_ROWS, G_ROWS_A, G_ROWS_W = 64, 4, 256
+
+    def oracle_call(self, idx):
+        from oracle import wq_oracle as O
+
+        kind, i = idx
+        K, N = self.K, self.N
+        if kind in ("qw", "qa"):
+            src = self.w_src if kind == "qw" else self.a_srcs[i]
+            r = min(self.Q_ROWS, src.shape[0])
+            O.nv_quantize_fp4(src[:r])
+            return r * K * 8 + r * K // 2 + r * K // 16, 0, f"first {r} of {src.shape[0]} rows (extrapolated)"
+        if self._oracle_ops is None:
+            self._oracle_ops = (O.nv_quantize_fp4(self.w_src[:self.G_ROWS_W]),
+                                [O.nv_quantize_fp4(a[:self.G_ROWS_A]) for a in self.a_srcs])
+        (wd, ws, gw), a_ops = self._oracle_ops
+        ad, asc, ga = a_ops[i]
+        O.nv_gemm_fp4(ad, asc, ga, wd, ws, gw)
+        m, n = ad.shape[0], wd.shape[0]
+        M = self.a_srcs[i].shape[0]
+        return ((m + n) * (K // 2 + K // 16) + 4 * m * n, 2 * m * n * K,
+                f"{m} of {M} rows of A x {n} of {N} rows of W (extrapolated)")
+
+    def run(self, r, idx):
+        kind, i = idx
+        d = self.dev[r]
+        w, wd, wsc, gw = d["w"]
+        if kind == "qw":
+            self.wq.nv_quantize_fp4(w, wd, wsc, gw)
+            return
+        a, ad, asc, ga, c = d["a"][i]
+        if kind == "qa":
+            self.wq.nv_quantize_fp4(a, ad, asc, ga)
+        else:
+            self.wq.nv_gemm_fp4(ad, asc, ga, wd, wsc, gw, c=c)
+
+
 class Fp8:
     def __init__(self, torch, wq, shapes, replicas, seed=0):
         self.torch, self.wq = torch, wq
@@ -294,6 +365,8 @@ def make_workload(torch, wq, name, replicas, only=None):
                         batched=spec.get("batched", False))
     elif spec["op"] == "mxfp4":
         wl = MxFp4(torch, wq, shapes, replicas)
+    elif spec["op"] == "nvfp4":
+        wl = NvFp4(torch, wq, shapes, replicas)
     else:
         wl = Fp8(torch, wq, shapes, replicas)
     if only:
@@ -305,7 +378,7 @@ def make_workload(torch, wq, name, replicas, only=None):
 
 # Workloads reported in `breakdown` besides the headline one.
 BREAKDOWN = ("w8a16_decode_batched", "w4a16_decode", "w4a16_decode_batched", "w4a16_llama7b",
-             "w8a16_grouped_decode", "mxfp4", "fp8")
+             "w8a16_grouped_decode", "mxfp4", "nvfp4", "fp8")
 
 
 def replicas_for(step_bytes):
@@ -607,6 +680,7 @@ def _throughput(calls, unit, seconds, factor=1):
 DTYPES = {"w8a16": "int8 weights x fp16 activations, fp32 accumulate",
           "w4a16": "int4 weights x fp16 activations, fp32 accumulate",
           "mxfp4": "e2m1 x e2m1 with e8m0 block scales, fp32 accumulate",
+          "nvfp4": "e2m1 x e2m1 with e4m3 block scales and fp32 tensor scales, fp32 accumulate",
           "fp8": "e4m3 x e4m3, fp32 accumulate, bf16 out"}
 
 

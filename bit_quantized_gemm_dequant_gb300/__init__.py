@@ -45,6 +45,8 @@ _SIGS = {
     "mx_quantize_fp4": [_i, _i, _p, _i64, _p, _i64, _p, _i64, _p],
     "mx_gemm_fp4": [_i, _i, _i, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _sz, _p],
     "fp8_gemm": [_i, _i, _i, _p, _i64, _p, _i64, _f, _f, _p, _i64, _p, _sz, _p],
+    "nv_quantize_fp4": [_i, _i, _p, _i64, _p, _i64, _p, _i64, _p, _p],
+    "nv_gemm_fp4": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
     "wq_workspace_size": [_i, _i, _i, _i],
     "wq_status_string": [_i],
     "wq_get_device_error": [_p, ctypes.POINTER(_i)],
@@ -371,6 +373,58 @@ def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
     wsp, wsb = _ws(workspace)
     _check(lib.mx_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
                            _ptr(c), _ld(c), wsp, wsb, _stream(stream)), "mx_gemm_fp4")
+    return c
+
+
+def nv_quantize_fp4(src, data=None, scales=None, tensor_scale=None, stream=None):
+    """fp32 [R, C] -> (uint8 data [R, C/2], uint8 E4M3 scales [R, C/16], fp32
+    tensor scale [1] on the device)."""
+    import torch
+
+    where = "nv_quantize_fp4"
+    _on_gpu(where, src, data, scales, tensor_scale)
+    _kind(where, src, "src", dtype="float32")
+    _kind(where, data, "data", size=1)
+    _kind(where, scales, "scales", size=1)
+    _kind(where, tensor_scale, "tensor_scale", dtype="float32")
+    _require(src.dim() == 2, where, "src must be 2-D")
+    R, C = src.shape
+    _require(data is None or tuple(data.shape) == (R, C // 2), where, f"data must be [{R}, {C // 2}]")
+    _require(scales is None or tuple(scales.shape) == (R, C // 16), where, f"scales must be [{R}, {C // 16}]")
+    _require(tensor_scale is None or tensor_scale.numel() >= 1, where, "tensor_scale needs one element")
+    if data is None:
+        data = torch.empty((R, C // 2), dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty((R, C // 16), dtype=torch.uint8, device=src.device)
+    if tensor_scale is None:
+        tensor_scale = torch.empty(1, dtype=torch.float32, device=src.device)
+    _check(lib.nv_quantize_fp4(R, C, _ptr(src), _ld(src), _ptr(data), _ld(data), _ptr(scales), _ld(scales),
+                               _ptr(tensor_scale), _stream(stream)), where)
+    return data, scales, tensor_scale
+
+
+def nv_gemm_fp4(a, sa, ga, w, sw, gw, c=None, stream=None):
+    """C fp32 [M, N] = A * W^T for NVFP4 operands (data [rows, K/2], E4M3
+    scales [rows, K/16], tensor scale [1] on the device)."""
+    import torch
+
+    where = "nv_gemm_fp4"
+    _on_gpu(where, a, sa, ga, w, sw, gw, c)
+    for t, n in ((a, "a"), (sa, "sa"), (w, "w"), (sw, "sw")):
+        _kind(where, t, n, size=1)
+        _require(t.dim() == 2, where, f"{n} must be 2-D")
+    for t, n in ((ga, "ga"), (gw, "gw")):
+        _kind(where, t, n, dtype="float32")
+    _kind(where, c, "c", dtype="float32")
+    M, N, K = a.shape[0], w.shape[0], a.shape[1] * 2
+    _require(w.shape[1] * 2 == K, where, "a and w must have the same K")
+    _require(tuple(sa.shape) == (M, K // 16) and tuple(sw.shape) == (N, K // 16), where,
+             f"scales must be [{M}, {K // 16}] and [{N}, {K // 16}]")
+    _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check(lib.nv_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(ga), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
+                           _ptr(gw), _ptr(c), _ld(c), _p(0), 0, _stream(stream)), where)
     return c
 
 

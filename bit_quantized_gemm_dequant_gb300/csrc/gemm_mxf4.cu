@@ -40,21 +40,37 @@ namespace {
 
 constexpr int BM = 128, BN = 256;
 constexpr int BKB = 128;                    // K bytes per stage (256 E2M1 elements)
-constexpr int kBlocksPerStage = BKB * 2 / 32;  // 8 scale blocks
 constexpr int kStages = 4;
 constexpr int kABytes = BM * BKB;           // 16 KB
 constexpr int kBBytes = BN * BKB;           // 32 KB
-constexpr int kSfChunk = 512;               // 128 rows x 4 blocks
-constexpr int kSfRowBytes = 16;             // scale bytes per row and TMA box (two stages)
-constexpr int kSfBytes = (BM + BN) * kSfRowBytes;  // 6 KB: raw boxes, rewritten into 6 chunks in place
+constexpr int kSfChunk = 512;               // 128 rows x 4 scale bytes
+constexpr int kSfRowBytes = 16;             // scale bytes per row and TMA box
+constexpr int kSfBytes = (BM + BN) * kSfRowBytes;  // 6 KB: raw boxes, rewritten into chunks in place
 constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // 54 KB (multiple of 1024)
 constexpr int kAccCols = BN;                // FP32 accumulator columns
-constexpr int kSfColsPerStage = 24;         // 6 chunks x 4 columns
-constexpr int kTmemCols = 512;              // accumulator + 4 x 24 scale columns, rounded up
+constexpr int kTmemCols = 512;              // accumulator + 4 stages of scale columns, rounded up
 constexpr int kThreads = 192;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 
-static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+// The two FP4 formats.  MXFP4: 32-element blocks with E8M0 scales, 8 scale
+// bytes per row per K step (the 16-byte scale box spans two steps), scales
+// in pairs per TMEM word (scale_vec::2X).  NVFP4: 16-element blocks with
+// E4M3 scales, 16 scale bytes per row per K step (one box per step), one
+// TMEM word of four scales per MMA (scale_vec::4X), and two FP32 tensor
+// scales applied in the epilogue.
+template <bool kNv>
+struct Fmt {
+  static constexpr int kBlock = kNv ? 16 : 32;          // elements per scale
+  static constexpr int kSfPerStep = BKB * 2 / kBlock;   // scale bytes per row per K step
+  static constexpr int kWords = kSfPerStep / 4;         // 4-byte chunk lines per row per K step
+  static constexpr int kChunks = 3 * kWords;            // 512-byte chunks per K step (A, W 0-127, W 128-255)
+  static constexpr int kSfCols = 4 * kChunks;           // TMEM columns per stage
+  // Scale bytes of rows or blocks outside the matrix (their data reads as
+  // zero, so any finite scale gives zero): 2^0 for E8M0, 0 for E4M3.
+  static constexpr uint32_t kFill = kNv ? 0u : 0x7F7F7F7Fu;
+};
+static_assert(kAccCols + kStages * Fmt<true>::kSfCols <= kTmemCols, "TMEM budget");
+static_assert(kAccCols + kStages * Fmt<false>::kSfCols <= kTmemCols, "TMEM budget");
 
 // K splits: when the output tiles cannot fill half the GPU (M = 128 at
 // N = 8192: 32 tiles), split K so that tiles x splits fill it, keeping at
@@ -74,16 +90,17 @@ int mx_splits(int M, int N, int K) {
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
 // Gather 8 scale bytes (blocks kb0 .. kb0+7) of one row; rows or blocks
-// outside the matrix read as 127 (2^0) so that zero-filled data stays zero.
+// outside the matrix read as `fill` (a finite scale, so that zero-filled
+// data stays zero).
 __device__ __forceinline__ void load_sf8(const uint8_t* S, int64_t ld, int row, int rows, int kb0, int nkb,
-                                         bool aligned4, uint32_t& lo, uint32_t& hi) {
+                                         bool aligned4, uint32_t fill, uint32_t& lo, uint32_t& hi) {
   if (row < rows && kb0 + 8 <= nkb && aligned4) {
     const uint32_t* p = reinterpret_cast<const uint32_t*>(S + static_cast<int64_t>(row) * ld + kb0);
     lo = __ldg(p);
     hi = __ldg(p + 1);
     return;
   }
-  uint32_t w[2] = {0x7F7F7F7Fu, 0x7F7F7F7Fu};
+  uint32_t w[2] = {fill, fill};
   if (row < rows) {
     const uint8_t* p = S + static_cast<int64_t>(row) * ld;
     for (int i = 0; i < 8; ++i)
@@ -97,26 +114,106 @@ __device__ __forceinline__ void load_sf8(const uint8_t* S, int64_t ld, int row, 
 }
 
 // Rewrite the stage's raw scale boxes (A: 128 rows, W: 256 rows, 16 bytes
-// each; the stage uses bytes 8h .. 8h+7) into six chunks at the start of the
-// same area: [A kb 0-3][A kb 4-7][W 0-127 kb 0-3][W 0-127 kb 4-7][W 128-255
-// kb 0-3][W 128-255 kb 4-7].  Lane l reads rows l + 32q of each 128-row
-// group and writes line l of each chunk, which lies in bytes it read.
-__device__ __forceinline__ void sf_to_chunks(uint8_t* sf, int h, int lane) {
-  uint32_t v[3][2][4];
+// each; the stage uses bytes off .. off + kSfPerStep - 1 of each row) into
+// 512-byte chunks at the start of the same area, group by group (A, W rows
+// 0-127, W rows 128-255) and 4-byte word by word: chunk grp * kWords + w,
+// line l = word w of rows l, l + 32, l + 64, l + 96 of the group (the layout
+// tcgen05.cp 32x128b.warpx4 copies into TMEM).  Lane l reads rows l + 32q of
+// each group and writes line l of each chunk, which lies in bytes it read.
+template <bool kNv>
+__device__ __forceinline__ void sf_to_chunks(uint8_t* sf, int off, int lane) {
+  constexpr int W = Fmt<kNv>::kWords;
+  uint32_t v[3][W][4];
 #pragma unroll
   for (int grp = 0; grp < 3; ++grp)
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint8_t* row = sf + (grp * 128 + lane + 32 * q) * kSfRowBytes + 8 * h;
-      v[grp][0][q] = *reinterpret_cast<const uint32_t*>(row);
-      v[grp][1][q] = *reinterpret_cast<const uint32_t*>(row + 4);
+      const uint8_t* row = sf + (grp * 128 + lane + 32 * q) * kSfRowBytes + off;
+#pragma unroll
+      for (int w = 0; w < W; ++w) v[grp][w][q] = *reinterpret_cast<const uint32_t*>(row + 4 * w);
     }
 #pragma unroll
   for (int grp = 0; grp < 3; ++grp)
 #pragma unroll
-    for (int half = 0; half < 2; ++half)
-      *reinterpret_cast<uint4*>(sf + (2 * grp + half) * kSfChunk + 16 * lane) =
-          make_uint4(v[grp][half][0], v[grp][half][1], v[grp][half][2], v[grp][half][3]);
+    for (int w = 0; w < W; ++w)
+      *reinterpret_cast<uint4*>(sf + (grp * W + w) * kSfChunk + 16 * lane) =
+          make_uint4(v[grp][w][0], v[grp][w][1], v[grp][w][2], v[grp][w][3]);
+}
+
+// Gather mode: the producer warp writes the same chunks from global memory.
+template <bool kNv>
+__device__ __forceinline__ void gather_sf_chunks(uint8_t* sf, const MxGemmArgs& p, int m0, int n0, int kt, int lane,
+                                                 bool a4, bool w4) {
+  constexpr int W = Fmt<kNv>::kWords;
+  const int nkb = p.K / Fmt<kNv>::kBlock;
+  const int kb0 = kt * Fmt<kNv>::kSfPerStep;
+#pragma unroll
+  for (int side = 0; side < 3; ++side) {
+    uint32_t v[W][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane + 32 * i;
+#pragma unroll
+      for (int h = 0; h < W / 2; ++h) {
+        if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0 + 8 * h, nkb, a4, Fmt<kNv>::kFill, v[2 * h][i], v[2 * h + 1][i]);
+        else load_sf8(p.SW, p.ldsw, n0 + 128 * (side - 1) + r, p.N, kb0 + 8 * h, nkb, w4, Fmt<kNv>::kFill,
+                      v[2 * h][i], v[2 * h + 1][i]);
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < W; ++w)
+      *reinterpret_cast<uint4*>(sf + (side * W + w) * kSfChunk + 16 * lane) = make_uint4(v[w][0], v[w][1], v[w][2], v[w][3]);
+  }
+}
+
+// One K step on the tensor cores: copy the stage's scale chunks into its TMEM
+// columns, then four 128 x 256 x 64 block-scaled MMAs.
+//   MXFP4: TMEM [A kb 0-3][A kb 4-7][W 0-127 kb 0-3][W 128-255 kb 0-3]
+//          [W 0-127 kb 4-7][W 128-255 kb 4-7], 4 columns each; MMA j takes
+//          the byte pair 2 (j % 2) of column 4 (j / 2) (A) and 8 + 8 (j / 2)
+//          (W: the N = 256 MMA reads W rows 128-255 four columns after rows
+//          0-127).
+//   NVFP4: TMEM [A j=0..3][W 0-127 j=0][W 128-255 j=0] .. [W 0-127 j=3][W 128-255 j=3];
+//          MMA j takes the whole word of column 4 j (A) and 16 + 8 j (W).
+template <bool kNv>
+__device__ __forceinline__ void mma_step(uint32_t tmem, uint32_t a, uint32_t b, uint32_t sf, uint32_t sf_col,
+                                         bool first) {
+  if constexpr (!kNv) {
+#pragma unroll
+    for (int c = 0; c < 6; ++c) {
+      const int pos = (c == 3 || c == 4) ? 7 - c : c;  // chunk order 0, 1, 2, 4, 3, 5
+      tc::tmem_cp_32x128b_warpx4(sf_col + 4 * pos, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // 64 elements = 32 bytes per MMA: 128 x 256 x 64
+      const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
+      const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
+      const uint32_t id = 2 * (j & 1);
+      const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
+      tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), !first || j != 0);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 12; ++c) {
+      const int grp = c / 4, j = c % 4;
+      const int col = grp == 0 ? 4 * j : 16 + 8 * j + (grp == 2 ? 4 : 0);
+      tc::tmem_cp_32x128b_warpx4(sf_col + col, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
+      const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
+      constexpr uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, 0, 0, /*UE4M3*/ 0);
+      tc::mma_mxf4nvf4_4x(tmem, adesc, bdesc, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j, !first || j != 0);
+    }
+  }
+}
+
+// Product of the two tensor scales (NVFP4), 1 for MXFP4.
+template <bool kNv>
+__device__ __forceinline__ float tensor_scale(const MxGemmArgs& p) {
+  if constexpr (kNv) return __fmul_rn(*p.ga, *p.gw);
+  return 1.0f;
 }
 
 // Add four floats to C (16-byte aligned) in one reduction, without reading
@@ -127,7 +224,7 @@ __device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, u
                : "memory");
 }
 
-template <bool kSfTma>
+template <bool kNv, bool kSfTma>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW, MxGemmArgs p,
@@ -144,7 +241,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int nkb = p.K / 32;
   // K steps [kt0, kt1) of this CTA: all of K, or split z of gridDim.z.
   const int KT_all = (p.K / 2 + BKB - 1) / BKB;
   const int kt0 = static_cast<int>(static_cast<int64_t>(blockIdx.z) * KT_all / gridDim.z);
@@ -196,27 +292,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
         tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
         if (kSfTma) {
-          const int x = kSfRowBytes * (kt / 2);  // 16-byte aligned column of the scale arrays
+          // the 16-byte aligned column of the scale arrays that holds this step's bytes
+          const int x = (kt * Fmt<kNv>::kSfPerStep) & ~(kSfRowBytes - 1);
           tc::tma_load_2d(sf, &tmSA, x, m0, &full[s]);
           tc::tma_load_2d(sf + BM * kSfRowBytes, &tmSW, x, n0, &full[s]);
         }
       }
       if (!kSfTma) {
-        // Gather: chunks [A 0-3][A 4-7][W 0-127: 0-3][4-7][W 128-255: 0-3][4-7].
-        const int kb0 = kt * kBlocksPerStage;
-#pragma unroll
-        for (int side = 0; side < 3; ++side) {
-          uint32_t lo[4], hi[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = lane + 32 * i;
-            if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0, nkb, a4, lo[i], hi[i]);
-            else load_sf8(p.SW, p.ldsw, n0 + 128 * (side - 1) + r, p.N, kb0, nkb, w4, lo[i], hi[i]);
-          }
-          uint8_t* c0 = sf + side * 2 * kSfChunk;
-          *reinterpret_cast<uint4*>(c0 + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          *reinterpret_cast<uint4*>(c0 + kSfChunk + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        }
+        gather_sf_chunks<kNv>(sf, p, m0, n0, kt, lane, a4, w4);
         tc::fence_proxy_async_smem();  // scale bytes -> visible to tcgen05.cp
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&full[s]);
@@ -236,25 +319,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
       const uint32_t b = a + kABytes;
       const uint32_t sf = b + kBBytes;
-      const uint32_t sf_col = tmem + kAccCols + s * kSfColsPerStage;
-      // Shared-memory chunk order: [A kb 0-3][A kb 4-7][W 0-127 kb 0-3]
-      // [W 0-127 kb 4-7][W 128-255 kb 0-3][W 128-255 kb 4-7].  In TMEM the two
-      // W halves of one block group sit side by side (columns +8, +12 for kb
-      // 0-3 and +16, +20 for kb 4-7): the N = 256 MMA reads the scale factors
-      // of W rows 128-255 four columns after those of rows 0-127.
-#pragma unroll
-      for (int c = 0; c < 6; ++c) {
-        const int pos = (c == 3 || c == 4) ? 7 - c : c;  // chunk order 0, 1, 2, 4, 3, 5
-        tc::tmem_cp_32x128b_warpx4(sf_col + 4 * pos, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {  // 64 elements = 32 bytes per MMA: 128 x 256 x 64
-        const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
-        const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
-        const uint32_t id = 2 * (j & 1);
-        const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
-        tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), (i | j) != 0);
-      }
+      const uint32_t sf_col = tmem + kAccCols + s * Fmt<kNv>::kSfCols;
+      mma_step<kNv>(tmem, a, b, sf, sf_col, i == 0);
       tc::tc_commit(&empty[s]);
     }
     tc::tc_commit(accum);
@@ -271,12 +337,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int kt = kt0 + i, s = i % kStages;
         const bool ok = tc::mbar_wait(&full[s], (i / kStages) & 1, abort, err, kSiteGemmMma);
         if (!__all_sync(0xffffffffu, ok)) break;
-        sf_to_chunks(smem + s * kStageBytes + kABytes + kBBytes, kt & 1, lane);
+        sf_to_chunks<kNv>(smem + s * kStageBytes + kABytes + kBBytes, (kt * Fmt<kNv>::kSfPerStep) & (kSfRowBytes - 1),
+                          lane);
         tc::fence_proxy_async_smem();  // chunk bytes -> visible to tcgen05.cp
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sf_ready[s]);
       }
     }
+    const float gs = tensor_scale<kNv>(p);
     const bool ok = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
     const int q = warp & 3;
@@ -289,6 +357,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
       tc::tmem_ld_wait();
       if (!ok) continue;
+      if constexpr (kNv) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gs);
+      }
       if (S > 1) {
         const int col0 = n0 + 32 * c;
         if (row >= p.M || col0 >= p.N) continue;
@@ -383,7 +455,7 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
   }
 }
 
-template <bool kSfTma>
+template <bool kNv, bool kSfTma>
 __global__ void __launch_bounds__(kPThreads, 1)
 mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW,
@@ -400,7 +472,6 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = p.K / 32;
   const int KT = (p.K / 2 + BKB - 1) / BKB;
   const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
@@ -455,26 +526,13 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
           tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
           if (kSfTma) {
-            const int x = kSfRowBytes * (kt / 2);
+            const int x = (kt * Fmt<kNv>::kSfPerStep) & ~(kSfRowBytes - 1);
             tc::tma_load_2d(sf, &tmSA, x, m0, &full[s]);
             tc::tma_load_2d(sf + BM * kSfRowBytes, &tmSW, x, n0, &full[s]);
           }
         }
         if (!kSfTma) {
-          const int kb0 = kt * kBlocksPerStage;
-#pragma unroll
-          for (int side = 0; side < 3; ++side) {
-            uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = lane + 32 * i;
-              if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0, nkb, a4, lo[i], hi[i]);
-              else load_sf8(p.SW, p.ldsw, n0 + 128 * (side - 1) + r, p.N, kb0, nkb, w4, lo[i], hi[i]);
-            }
-            uint8_t* c0 = sf + side * 2 * kSfChunk;
-            *reinterpret_cast<uint4*>(c0 + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<uint4*>(c0 + kSfChunk + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          }
+          gather_sf_chunks<kNv>(sf, p, m0, n0, kt, lane, a4, w4);
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&full[s]);
@@ -503,20 +561,8 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
         const uint32_t b = a + kABytes;
         const uint32_t sf = b + kBBytes;
-        const uint32_t sf_col = tmem + kAccCols + s * kSfColsPerStage;
-#pragma unroll
-        for (int c = 0; c < 6; ++c) {
-          const int pos = (c == 3 || c == 4) ? 7 - c : c;  // chunk order 0, 1, 2, 4, 3, 5 (see mx_gemm_kernel)
-          tc::tmem_cp_32x128b_warpx4(sf_col + 4 * pos, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
-          const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
-          const uint32_t id = 2 * (j & 1);
-          const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
-          tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), (kt | j) != 0);
-        }
+        const uint32_t sf_col = tmem + kAccCols + s * Fmt<kNv>::kSfCols;
+        mma_step<kNv>(tmem, a, b, sf, sf_col, kt == 0);
         tc::tc_commit(&empty[s]);
       }
       if (!ok) break;
@@ -540,7 +586,8 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             go = false;
             break;
           }
-          sf_to_chunks(smem + s * kStageBytes + kABytes + kBBytes, kt & 1, lane);
+          sf_to_chunks<kNv>(smem + s * kStageBytes + kABytes + kBBytes,
+                            (kt * Fmt<kNv>::kSfPerStep) & (kSfRowBytes - 1), lane);
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sf_ready[s]);
@@ -550,6 +597,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   } else if (warp >= 3) {
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int h = (warp - 3) >> 2;   // column half: 128 h .. 128 h + 127
+    const float gs = tensor_scale<kNv>(p);
     int local = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
       const bool ok = mbar_wait_backoff(acc_full, local & 1, abort, err, kSiteGemmEpilogue);
@@ -566,6 +614,12 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(acc_empty);
+      if constexpr (kNv) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int u = 0; u < 32; ++u) r[c][u] = __float_as_uint(__uint_as_float(r[c][u]) * gs);
+      }
       // After the transpose lane l holds column col0 + l of rows
       // m0 + 32 q .. m0 + 32 q + 31.
       const int row0 = m0 + 32 * q;
@@ -592,7 +646,10 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 }  // namespace
 
-cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
+namespace {
+
+template <bool kNv>
+cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
   if (a.K == 0)
     return cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
   CUtensorMap tA, tW, tSA, tSW;
@@ -604,11 +661,12 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
   // Scale arrays go through TMA when their rows start on 16-byte boundaries.
   const bool sf_tma = ((reinterpret_cast<uintptr_t>(a.SA) | reinterpret_cast<uintptr_t>(a.SW) |
                         static_cast<uintptr_t>(a.ldsa) | static_cast<uintptr_t>(a.ldsw)) & 15) == 0;
+  const uint64_t sf_cols = a.K / Fmt<kNv>::kBlock;
   if (sf_tma) {
-    e = make_tmap_2d(&tSA, a.SA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 32, a.M, a.ldsa, kSfRowBytes, BM,
+    e = make_tmap_2d(&tSA, a.SA, CU_TENSOR_MAP_DATA_TYPE_UINT8, sf_cols, a.M, a.ldsa, kSfRowBytes, BM,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
-    e = make_tmap_2d(&tSW, a.SW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 32, a.N, a.ldsw, kSfRowBytes, BN,
+    e = make_tmap_2d(&tSW, a.SW, CU_TENSOR_MAP_DATA_TYPE_UINT8, sf_cols, a.N, a.ldsw, kSfRowBytes, BN,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
   } else {
@@ -617,7 +675,7 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
   }
   const int splits = mx_splits(a.M, a.N, a.K);
   if (splits == 1) {  // persistent: one CTA per SM
-    auto pk = sf_tma ? mx_gemm_persistent<true> : mx_gemm_persistent<false>;
+    auto pk = sf_tma ? mx_gemm_persistent<kNv, true> : mx_gemm_persistent<kNv, false>;
     static PerDevice<bool> pconfigured[2];
     bool pdone = false;
     if (!pconfigured[sf_tma].get(pdone, [&](bool& v) {
@@ -631,7 +689,7 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
     pk<<<grid, kPThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
     return cudaGetLastError();
   }
-  auto kern = sf_tma ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
+  auto kern = sf_tma ? mx_gemm_kernel<kNv, true> : mx_gemm_kernel<kNv, false>;
   static PerDevice<bool> configured[2];
   bool done = false;
   if (!configured[sf_tma].get(done, [&](bool& v) {
@@ -648,5 +706,11 @@ cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) {
   kern<<<grid, kThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
   return cudaGetLastError();
 }
+
+}  // namespace
+
+cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) { return launch_fp4_gemm<false>(a, s); }
+
+cudaError_t launch_nv_gemm(const MxGemmArgs& a, cudaStream_t s) { return launch_fp4_gemm<true>(a, s); }
 
 }  // namespace wq

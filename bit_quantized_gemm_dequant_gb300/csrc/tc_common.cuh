@@ -290,6 +290,18 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// Block-scaled FP4 with 16-element blocks (E2M1 x E2M1, four scale factors
+// per row per K = 64 instruction, one 32-bit TMEM word per row).
+__device__ __forceinline__ void mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copy a 32-row x 128-bit shared-memory block into TMEM, replicated into the
 // four 32-lane quarters of the destination columns.
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
@@ -338,12 +350,13 @@ __host__ __device__ constexpr uint32_t idesc_dense(uint32_t a_fmt, uint32_t b_fm
 }
 
 // Instruction descriptor for the block-scaled kinds: formats at bits 7-9 /
-// 10-12, N >> 3 at 17-22, scale type (1 = UE8M0) at bit 23, M >> 4 at 24-28,
+// 10-12, N >> 3 at 17-22, scale type at bit 23 (1 = UE8M0, 0 = UE4M3),
+// M >> 4 at 24-28,
 // and the byte selectors of the scale factors inside their TMEM words:
 // B at bits 4-5, A at bits 29-30.
 __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N,
-                                                          uint32_t sfa_id, uint32_t sfb_id) {
-  return (sfb_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+                                                          uint32_t sfa_id, uint32_t sfb_id, uint32_t ue8m0 = 1) {
+  return (sfb_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (ue8m0 << 23) | ((M >> 4) << 24) |
          (sfa_id << 29);
 }
 

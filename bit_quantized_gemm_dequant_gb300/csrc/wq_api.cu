@@ -227,6 +227,38 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_
   return launch_status(launch_mx_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nv_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_t* data, int64_t ld_data,
+                    uint8_t* scales, int64_t ld_scales, float* tensor_scale, wq_stream_t stream) {
+  if (rows < 0 || cols < 0 || cols % 16 || !tensor_scale) return WQ_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0) {
+    if (!src || !data || !scales) return WQ_ERR_INVALID_ARG;
+    if (ld_src < cols || ld_data < cols / 2 || ld_scales < cols / 16) return WQ_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || ld_src % 4 || !aligned(data, 8) || ld_data % 8) return WQ_ERR_MISALIGNED;
+    if (static_cast<int64_t>(rows) * (cols / 16) >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  }
+  if (!aligned(tensor_scale, 4)) return WQ_ERR_MISALIGNED;
+  NvQuantArgs a{rows, cols, src, ld_src, data, ld_data, scales, ld_scales, tensor_scale};
+  return launch_status(launch_nv_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nv_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* SA, int64_t ldsa,
+                const float* scale_a, const uint8_t* W, int64_t ldw, const uint8_t* SW, int64_t ldsw,
+                const float* scale_w, float* C, int64_t ldc, void* workspace, size_t ws_bytes, wq_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  if (M < 0 || N < 0 || K < 0 || K % 16) return WQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQ_OK;
+  if (!C || (K > 0 && (!A || !SA || !W || !SW || !scale_a || !scale_w))) return WQ_ERR_INVALID_ARG;
+  if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2 || ldsa < K / 16 || ldsw < K / 16))) return WQ_ERR_INVALID_ARG;
+  if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(A, 16) || !aligned(W, 16) || lda % 16 || ldw % 16 || !aligned(scale_a, 4) ||
+                !aligned(scale_w, 4)))
+    return WQ_ERR_MISALIGNED;
+  if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
+  MxGemmArgs a{M, N, K, A, lda, SA, ldsa, W, ldw, SW, ldsw, C, ldc, scale_a, scale_w};
+  return launch_status(launch_nv_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb, float scale_a,
              float scale_b, void* C, int64_t ldc, void* workspace, size_t ws_bytes, wq_stream_t stream) {
   if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
@@ -301,6 +333,6 @@ int wq_debug_set_wait_limit(int64_t ns) {
   return WQ_OK;
 }
 
-int wq_version(void) { return 300; }  // 0.3.0: batched weight-only entry points
+int wq_version(void) { return 400; }  // 0.4.0: NVFP4 quantizer and GEMM
 
 }  // extern "C"

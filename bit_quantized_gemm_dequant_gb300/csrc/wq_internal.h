@@ -86,13 +86,23 @@ struct MxQuantArgs {
   uint8_t* scales; int64_t ld_scales;
 };
 
-struct MxGemmArgs {
+struct MxGemmArgs {  // MXFP4 and NVFP4 GEMMs
   int M, N, K;
   const uint8_t* A; int64_t lda;
   const uint8_t* SA; int64_t ldsa;
   const uint8_t* W; int64_t ldw;
   const uint8_t* SW; int64_t ldsw;
   float* C; int64_t ldc;
+  const float* ga = nullptr;  // NVFP4: the tensor scales of A and W (device memory)
+  const float* gw = nullptr;
+};
+
+struct NvQuantArgs {
+  int rows, cols;
+  const float* src; int64_t ld_src;
+  uint8_t* data; int64_t ld_data;
+  uint8_t* scales; int64_t ld_scales;
+  float* tensor_scale;  // device: receives the tensor scale
 };
 
 struct Fp8GemmArgs {
@@ -127,6 +137,8 @@ cudaError_t launch_wo_skinny(const WoArgs& a, int bits, const SkinnyPlan& pl, cu
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s);
 cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s);
+cudaError_t launch_nv_gemm(const MxGemmArgs& a, cudaStream_t s);
+cudaError_t launch_nv_quantize(const NvQuantArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_gemm(const Fp8GemmArgs& a, cudaStream_t s);
 
 

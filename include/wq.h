@@ -11,6 +11,7 @@
  *            Step 1 formula, Step 3 signature and layout, reference solution.
  *   [FP8]    "通过 CUTLASS 命名约定在 Triton 中实现 FP8 GEMM 内核", kernel
  *            listing and the 精度管理 (precision management) bullet.
+ *   [W4A16] §三 also names NVFP4, the format of nv_quantize_fp4 / nv_gemm_fp4.
  *
  * Conventions for every entry point below
  *   - Matrices are row-major.  A leading dimension ("ld*") is the distance in
@@ -295,6 +296,63 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
                 int64_t ldw, const uint8_t* SW, int64_t ldsw, float* C,
                 int64_t ldc, void* workspace, size_t ws_bytes,
                 wq_stream_t stream);
+
+/*
+ * nv_quantize_fp4 — quantize FP32 rows to NVFP4: E2M1 elements in 16-element
+ * blocks, one E4M3 scale per block, one FP32 scale per tensor.
+ *
+ * [W4A16] §三 names NVFP4 as E2M1 elements under a two-level block scaling
+ * with an FP8 local block scale, executed natively by the 5th-generation
+ * tensor cores, and gives no block size or encoding.  The reading: 16-element
+ * blocks along the row; with g = amax(|src|) / 2688 (6 x 448; g = 1 for an
+ * all-zero tensor), each block's scale is s = e4m3(amax_block / (6 g)), the
+ * nearest E4M3 value with ties to the even code, saturating at 448; each
+ * element's code is the nearest E2M1 grid point to x / (s g), the smaller one
+ * on a tie, with the sign bit set when x < 0 ([MXFP4] §三 chooses elements the
+ * same way); a block whose scale is 0 is all code 0.  Every step is one
+ * float32 operation rounded to nearest, so the bytes are exact.
+ *
+ *   rows, cols    source size; cols must be a multiple of 16.
+ *   src           fp32 [rows, cols], row stride ld_src (elements).
+ *   data          uint8 [rows, cols/2] output (element 2t in the low nibble
+ *                 of byte t), row stride ld_data (bytes).
+ *   scales        uint8 [rows, cols/16] output E4M3 bytes, row stride ld_scales.
+ *   tensor_scale  device pointer to one float that receives g (it also holds
+ *                 the running amax while the call runs).
+ * Alignment: src 16-byte aligned, ld_src a multiple of 4; data 8-byte aligned,
+ * ld_data a multiple of 8; tensor_scale 4-byte aligned.
+ * The source is read twice (amax, then the codes).
+ */
+int nv_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
+                    uint8_t* data, int64_t ld_data, uint8_t* scales,
+                    int64_t ld_scales, float* tensor_scale, wq_stream_t stream);
+
+/*
+ * nv_gemm_fp4 — C = A * W^T for NVFP4 operands, FP32 output.
+ *
+ * [W4A16] §三 (NVFP4 on the 5th-generation tensor cores; reading as for
+ * nv_quantize_fp4) and [MXFP4] §二.1 (the block dot product): for every output
+ * (m, n) and 16-element K block b,
+ *   dC = sA[m, b] * sW[n, b] * sum_{i<16} a[m, b, i] * w[n, b, i],
+ * C = gA * gW * sum_b dC, accumulated in FP32 by the block-scaled tensor
+ * cores (kind::mxf4nvf4, E4M3 scales).
+ *
+ *   M, N, K   problem size; K must be a multiple of 16.
+ *   A, SA     A's data uint8 [M, K/2] (row stride lda) and E4M3 scales uint8
+ *             [M, K/16] (row stride ldsa), as nv_quantize_fp4 writes them.
+ *   scale_a   device pointer to A's tensor scale gA (from nv_quantize_fp4).
+ *   W, SW, scale_w  the same for W [N, K].
+ *   C         fp32 [M, N] output, row stride ldc (elements).
+ *   workspace, ws_bytes  unused (0 bytes needed).
+ * Alignment: as for mx_gemm_fp4, plus scale_a and scale_w 4-byte aligned.
+ * Small M splits K across CTAs as mx_gemm_fp4 does (C is zeroed on `stream`
+ * and the splits add into it, in no fixed order).
+ */
+int nv_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
+                const uint8_t* SA, int64_t ldsa, const float* scale_a,
+                const uint8_t* W, int64_t ldw, const uint8_t* SW,
+                int64_t ldsw, const float* scale_w, float* C, int64_t ldc,
+                void* workspace, size_t ws_bytes, wq_stream_t stream);
 
 /*
  * fp8_gemm — C = bf16((A * B) * scale_a * scale_b) for e4m3 operands.
