@@ -84,7 +84,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -192,7 +192,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg::kTmemCols);

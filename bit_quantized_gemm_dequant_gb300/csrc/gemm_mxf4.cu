@@ -265,7 +265,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -390,7 +390,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -493,7 +493,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -637,7 +637,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);

@@ -369,8 +369,10 @@ __device__ __forceinline__ float4 f4add(float4 a, float4 b) {
 }
 
 // Barrier over the CTA's warps (all of them load and consume).
+// All kThreads threads of the CTA, on barrier 1 (barrier 0 is cta_barrier's).
+// Non-aligned: it counts threads, so lanes of a warp may arrive apart.
 __device__ __forceinline__ void cta_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  asm volatile("barrier.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
 }  // namespace

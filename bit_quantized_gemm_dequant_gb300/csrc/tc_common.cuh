@@ -163,14 +163,29 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 
 // ------------------------------------------------------------------ clusters
 
-// All threads of every CTA of the cluster: arrive (release) and wait (acquire).
+// All threads of every CTA of the cluster: arrive (release) and wait
+// (acquire).  The non-aligned forms: a warp's lanes may get here at different
+// times (roles where lane 0 runs a loop alone).
 __device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+
+// CTA-wide barrier over all threads.  The kernels give whole warps to roles
+// whose lane 0 alone runs a loop (TMA producer, MMA issuer) while the other
+// lanes go ahead; the aligned barrier behind __syncthreads() assumes a warp's
+// lanes arrive together and, measured on sm_103a, then lets threads through
+// before the other warps arrive.  The non-aligned barrier.sync counts threads.
+__device__ __forceinline__ void cta_barrier() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 
@@ -190,6 +205,23 @@ __device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
                ::"r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
                : "memory");
+}
+
+// Load a float from shared::cluster address `addr` (another CTA's shared
+// memory after a cluster barrier).
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // try_wait with cluster-scope acquire: data that other CTAs of the cluster

@@ -138,7 +138,7 @@ wo_batched_kernel(const __grid_constant__ BatchTable tb, int* ws_count, float4* 
     *abort = 0;
     tc::fence_mbar_init();
   }
-  __syncthreads();
+  tc::cta_barrier();
 
   // Issue cursor of this warp: piece cp, batch unit cu, and its problem,
   // tile and chunk (cb, ct, cc), advanced by kWarps units at a time.

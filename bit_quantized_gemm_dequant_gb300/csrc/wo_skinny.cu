@@ -127,7 +127,7 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     *abort = 0;
     tc::fence_mbar_init();
   }
-  __syncthreads();
+  tc::cta_barrier();
   if (pl.cluster > 1) {
     // The receive barrier expects the other CTAs' slices of this CTA's part of
     // the tile; every CTA's barrier is armed before any CTA sends.
