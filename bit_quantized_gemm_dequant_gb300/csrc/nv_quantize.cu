@@ -13,9 +13,9 @@
 // IEEE float32 operation rounded to nearest, so the bytes match a float32
 // restatement of those steps exactly.
 //
-// Three launches on the stream: the tensor amax (an atomic max over the
-// float bits, kept in the tensor-scale word), the quantization (which reads
-// it), and a one-thread step that turns the amax into g.  HBM-bound: the
+// Three launches on the stream after zeroing the tensor-scale word: the
+// tensor amax (kept in that word), the quantization (which reads it), and a
+// one-thread step that turns the amax into g.  HBM-bound: the
 // source is read twice (4 + 4 B per element) and 0.5 + 1/16 B written.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -34,19 +34,42 @@ __device__ __forceinline__ float amax4(float4 v) {
   return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 }
 
-// Tensor amax: the largest |x| over the rows [row0, row0 + gridDim.y); the
-// non-negative float bits order like the floats, so an integer atomic max
-// over them is a float max.
+// Tensor amax.  Each block takes one 1024-column slice of every gridDim.y-th
+// row (four rows in flight per thread), reduces in shared memory and makes
+// one atomic max on the tensor-scale word: non-negative float bits order like
+// the floats, so an integer max over them is a float max.  Plain cached loads,
+// so that an operand that fits in L2 is still there for the second pass.
+constexpr int kAmaxRowsInFlight = 4;
+
 __global__ void __launch_bounds__(kThreads)
-nv_amax_kernel(NvQuantArgs p, int row0) {
-  const int r = row0 + blockIdx.y;
+nv_amax_kernel(NvQuantArgs p) {
   const int c4 = blockIdx.x * kThreads + threadIdx.x;
   float m = 0.0f;
-  if (c4 < p.cols / 4) m = amax4(load4(p.src + static_cast<int64_t>(r) * p.ld_src + 4 * c4));
+  if (c4 < p.cols / 4) {
+    const float* col = p.src + 4 * static_cast<int64_t>(c4);
+    const int step = gridDim.y;
+    int r = blockIdx.y;
+    for (; r + (kAmaxRowsInFlight - 1) * step < p.rows; r += kAmaxRowsInFlight * step) {
+      float4 v[kAmaxRowsInFlight];
+#pragma unroll
+      for (int i = 0; i < kAmaxRowsInFlight; ++i)
+        v[i] = __ldg(reinterpret_cast<const float4*>(col + static_cast<int64_t>(r + i * step) * p.ld_src));
+#pragma unroll
+      for (int i = 0; i < kAmaxRowsInFlight; ++i) m = fmaxf(m, amax4(v[i]));
+    }
+    for (; r < p.rows; r += step)
+      m = fmaxf(m, amax4(__ldg(reinterpret_cast<const float4*>(col + static_cast<int64_t>(r) * p.ld_src))));
+  }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0 && m > 0.0f)
-    atomicMax(reinterpret_cast<unsigned int*>(p.tensor_scale), __float_as_uint(m));
+  __shared__ float warp_max[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
+    if (m > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(p.tensor_scale), __float_as_uint(m));
+  }
 }
 
 // g from the amax the first kernel left in the tensor-scale word.
@@ -63,17 +86,14 @@ __device__ __forceinline__ uint32_t e2m1_index(float v) {
   return (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) + (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
 }
 
-__global__ void __launch_bounds__(kThreads)
-nv_quantize_kernel(NvQuantArgs p, int row0) {
-  const int r = row0 + blockIdx.y;
-  const int c4 = blockIdx.x * kThreads + threadIdx.x;
-  const int lane = threadIdx.x & 31;
-  const bool live = c4 < p.cols / 4;  // cols is a multiple of 16: a block is live or dead as a whole
-  const float4 x = live ? load4(p.src + static_cast<int64_t>(r) * p.ld_src + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+// One 16-element block per four lanes: the block amax by two shuffles, the
+// E4M3 scale, then each lane's four codes.  Lane 4k gathers the block's four
+// 16-bit code groups into 8 bytes.
+__device__ __forceinline__ void quantize_row4(const NvQuantArgs& p, int r, int c4, bool live, float4 x, float g,
+                                              int lane) {
   float m = amax4(x);
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));  // the block's amax in all four lanes
-  const float g = tensor_scale_of(__uint_as_float(*reinterpret_cast<const unsigned int*>(p.tensor_scale)));
   const float sb_f = __fdiv_rn(m, __fmul_rn(6.0f, g));
   const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sb_f, __NV_SATFINITE, __NV_E4M3);
   const float d = __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3))), g);
@@ -84,12 +104,40 @@ nv_quantize_kernel(NvQuantArgs p, int row0) {
     for (int i = 0; i < 4; ++i)
       codes |= ((xs[i] < 0.0f ? 8u : 0u) | e2m1_index(__fdiv_rn(xs[i], d))) << (4 * i);
   }
-  // Lane 4k gathers the block's four 16-bit code groups into 8 bytes.
   const uint32_t pair = codes | (__shfl_down_sync(0xffffffffu, codes, 1) << 16);
   const uint32_t pair_hi = __shfl_down_sync(0xffffffffu, pair, 2);
   if (live && (lane & 3) == 0) {
     *reinterpret_cast<uint2*>(p.data + static_cast<int64_t>(r) * p.ld_data + 2 * c4) = make_uint2(pair, pair_hi);
     p.scales[static_cast<int64_t>(r) * p.ld_scales + c4 / 4] = sb;
+  }
+}
+
+// Each block takes one 1024-column slice of every gridDim.y-th row, loading
+// four rows before quantizing them.  The columns past the matrix are whole
+// dead blocks (cols is a multiple of 16): they quantize zeros and store
+// nothing, but still take part in the shuffles.
+constexpr int kQuantRowsInFlight = 4;
+
+__global__ void __launch_bounds__(kThreads)
+nv_quantize_kernel(NvQuantArgs p) {
+  const int c4 = blockIdx.x * kThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool live = c4 < p.cols / 4;
+  const float g = tensor_scale_of(__uint_as_float(*reinterpret_cast<const unsigned int*>(p.tensor_scale)));
+  const float* col = p.src + 4 * static_cast<int64_t>(c4);
+  const int step = gridDim.y;
+  int r = blockIdx.y;
+  for (; r + (kQuantRowsInFlight - 1) * step < p.rows; r += kQuantRowsInFlight * step) {
+    float4 x[kQuantRowsInFlight];
+#pragma unroll
+    for (int i = 0; i < kQuantRowsInFlight; ++i)
+      x[i] = live ? load4(col + static_cast<int64_t>(r + i * step) * p.ld_src) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kQuantRowsInFlight; ++i) quantize_row4(p, r + i * step, c4, live, x[i], g, lane);
+  }
+  for (; r < p.rows; r += step) {
+    const float4 x = live ? load4(col + static_cast<int64_t>(r) * p.ld_src) : make_float4(0.f, 0.f, 0.f, 0.f);
+    quantize_row4(p, r, c4, live, x, g, lane);
   }
 }
 
@@ -104,16 +152,13 @@ cudaError_t launch_nv_quantize(const NvQuantArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int cx = (a.cols / 4 + kThreads - 1) / kThreads;
   if (a.rows > 0 && a.cols > 0) {
-    for (int r0 = 0; r0 < a.rows; r0 += 65535) {  // grid y is at most 65535 rows per launch
-      const int n = a.rows - r0 < 65535 ? a.rows - r0 : 65535;
-      nv_amax_kernel<<<dim3(cx, n), kThreads, 0, s>>>(a, r0);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    for (int r0 = 0; r0 < a.rows; r0 += 65535) {
-      const int n = a.rows - r0 < 65535 ? a.rows - r0 : 65535;
-      nv_quantize_kernel<<<dim3(cx, n), kThreads, 0, s>>>(a, r0);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    // About 16 blocks per SM in each pass; each strides over the rows.
+    int ry = (sm_count() * 16 + cx - 1) / cx;
+    ry = ry < a.rows ? ry : a.rows;
+    nv_amax_kernel<<<dim3(cx, ry), kThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    nv_quantize_kernel<<<dim3(cx, ry), kThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   nv_tensor_scale_kernel<<<1, 1, 0, s>>>(a.tensor_scale);
   return cudaGetLastError();

@@ -11,8 +11,9 @@
 //   warp 0      TMA producer: X tile 256(m) x 64(k) fp16 (128-byte swizzle)
 //               and the packed weight tile (INT4 32 x 128 bytes, INT8 64 x 128
 //               bytes, no swizzle) into a shared-memory ring.
-//   warps 2-5   dequant: lane L of warp w owns weight column n = 32*(w%4) + L
-//               (its TMEM lane).  It reads its column of the packed tile
+//   warps 2-9   dequant, two warps per TMEM lane quarter taking alternate
+//               64-k steps (two steps in flight per CTA): lane L of warp w
+//               owns weight column n = 32*(w%4) + L (its TMEM lane).  It reads its column of the packed tile
 //               byte by byte, turns every byte into exact fp16 values (INT4:
 //               0x6400 | nibble = 1024 + q, minus 1032; INT8: byte ^ 0x80 |
 //               0x6400, minus 1152) and writes 32 fp16 pairs (one 64-k slice)
@@ -21,7 +22,8 @@
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma.kind::f16 with A
 //               from TMEM (128 n x 16 k) and B = the X tile from shared memory
 //               (K-major), 128 x 256 x 16, four per 64-k slice.
-//   warps 2-5   then the epilogue: tcgen05.ld of the 128 x 256 accumulator,
+//   warps 2-9   then the epilogue: tcgen05.ld of the 128 x 256 accumulator
+//               (the two warps of a lane quarter take alternate 32 columns),
 //               multiply by the per-column scale (exact to move out of the K
 //               sum: it is per column), round to fp16 and store; a warp writes
 //               32 consecutive columns of one row of Y per store.
@@ -29,6 +31,18 @@
 // 阵乘法", 扩展说明): the scale of column n is scales[n / group_n], and a
 // zero point z replaces the fixed 8 (INT4) or 0 (INT8) in the constant each
 // thread subtracts for its own column.
+//
+// Mid M (16 < M <= 64, the "tile per (M, N, K)" choice of the W4A16 page §二
+// at a shape between decode and prefill): one 64-row activation tile, so each
+// weight is dequantized exactly once, and the K loop of every 128-column tile
+// split among the S CTAs of a thread-block cluster so that tiles x S fills
+// the GPU (two CTAs per SM).  Each CTA parks its 128 x 64 FP32 partial in its
+// own shared memory; after a cluster barrier CTA r reads rows r*64/S ..
+// (r+1)*64/S - 1 of every peer's partial through distributed shared memory,
+// adds them in rank order (deterministic), scales, rounds and stores; a
+// second cluster barrier keeps each CTA's shared memory alive until its peers
+// are done reading it.  These launches use programmatic dependent launch, so
+// a call's prologue overlaps the previous kernel's tail.
 #include <cuda_fp16.h>
 
 #include "tc_common.cuh"
@@ -40,10 +54,14 @@ namespace {
 
 constexpr int BN = 128;            // weight columns per CTA (MMA M)
 constexpr int BK = 64;             // k per stage
-constexpr int kStages = 4;         // shared-memory ring
-constexpr int kAStages = 4;        // TMEM A ring
-constexpr int kThreads = 192;
+constexpr int kDequantWarps = 8;   // two per TMEM lane quarter
+constexpr int kThreads = (2 + kDequantWarps) * 32;
 constexpr int kAColsPerStage = BK / 2;  // fp16 pairs per TMEM lane
+constexpr int kMidRows = 64;       // activation rows of the mid-M (cluster K-split) instance
+constexpr int kMaxClusterK = 8;    // portable cluster size
+
+constexpr int kSmPerSmem = 228 * 1024;  // shared memory of one SM
+constexpr int kSmemPerCtaReserved = 1024;
 
 template <int BITS, int BM>
 struct WoGemmCfg {
@@ -52,9 +70,23 @@ struct WoGemmCfg {
   static constexpr int kWBytes = kWRows * BN;
   static constexpr int kStageBytes = ((kXBytes + kWBytes + 1023) / 1024) * 1024;
   static constexpr int kAccCols = BM;
-  static constexpr int kTmemCols = 512;
+  static constexpr int kTmemCols = BM == kMidRows ? 256 : 512;  // mid M: two CTAs per SM
+  static constexpr int kCtasPerSm = 512 / kTmemCols;
+  // TMEM A ring: the columns the accumulator leaves, at most 8 slices.
+  static constexpr int kAStagesFit = (kTmemCols - kAccCols) / kAColsPerStage;
+  static constexpr int kAStages = kAStagesFit > 8 ? 8 : kAStagesFit;
+  // Shared-memory ring: as deep as the SM's share for kCtasPerSm CTAs allows
+  // (at most 8 stages).  The ring also keeps a (kCtasPerSm + 1)-th CTA off
+  // the SM: it could not get tensor memory and would stall in its allocation
+  // until a neighbour left.
+  static constexpr int kStagesFit = (kSmPerSmem / kCtasPerSm - kSmemPerCtaReserved - 2048) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+  static_assert(kStages >= 2, "ring depth");
+  static_assert((kSmemBytes + kSmemPerCtaReserved) * (kCtasPerSm + 1) > kSmPerSmem, "one CTA too many per SM");
   static_assert(kAccCols + kAStages * kAColsPerStage <= kTmemCols, "TMEM budget");
+  // Mid M: the FP32 partial tile [BM rows][BN columns] reuses the idle ring.
+  static_assert(BM != kMidRows || BM * BN * 4 <= kStages * kStageBytes, "partial tile fits in the ring");
 };
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -79,16 +111,22 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+__device__ __forceinline__ uint32_t h2_bits2(__half lo, __half hi) {
+  return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-template <int BITS, int BM>
+template <int BITS, int BM, bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, WoArgs p,
                int* err) {
   using Cfg = WoGemmCfg<BITS, BM>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kAStages = Cfg::kAStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
@@ -101,8 +139,19 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
   const int KT = (p.K + BK - 1) / BK;
+  // This CTA's 128-column tile and its k-tiles [kt0, kt0 + nk): all of K, or
+  // (cluster K-split) the rank's share.
+  int n_tile = blockIdx.x, rank = 0, S = 1;
+  if constexpr (kCluster) {
+    rank = static_cast<int>(tc::cluster_ctarank());
+    S = static_cast<int>(tc::cluster_nctarank());
+    n_tile = blockIdx.x / S;
+    tc::griddep_launch_dependents();
+  }
+  const int n0 = n_tile * BN, m0 = blockIdx.y * BM;
+  const int kt0 = static_cast<int>(static_cast<int64_t>(rank) * KT / S);
+  const int nk = static_cast<int>(static_cast<int64_t>(rank + 1) * KT / S) - kt0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -123,42 +172,45 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t a_ring = tmem + Cfg::kAccCols;
+  // Programmatic dependent launch: everything above overlapped the previous
+  // kernel; no thread reads global memory before that kernel has finished.
+  if constexpr (kCluster) tc::griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmX);
       tc::tma_prefetch_desc(&tmW);
       int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kStages;
-        if (!tc::mbar_wait(&empty[s], ((kt / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer)) break;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages, kt = kt0 + i;
+        if (!tc::mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer)) break;
         uint8_t* st = smem + s * Cfg::kStageBytes;
         tc::mbar_arrive_expect_tx(&full[s], Cfg::kXBytes + Cfg::kWBytes);
         tc::tma_load_2d(st, &tmX, kt * BK, m0, &full[s]);
         tc::tma_load_2d(st + Cfg::kXBytes, &tmW, n0, kt * Cfg::kWRows, &full[s]);
-        issued = kt + 1;
+        issued = i + 1;
       }
       if (*abort)
-        for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
-          tc::mbar_wait_drain(&full[kt % kStages], (kt / kStages) & 1);
+        for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+          tc::mbar_wait_drain(&full[i % kStages], (i / kStages) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_dense(/*F16*/ 0, /*F16*/ 0, 0, 0, 128, BM);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kStages, t = kt % kAStages;
-        if (!tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmMma)) break;
-        if (!tc::mbar_wait(&a_full[t], (kt / kAStages) & 1, abort, err, kSiteGemmMma)) break;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages, t = i % kAStages;
+        if (!tc::mbar_wait(&full[s], (i / kStages) & 1, abort, err, kSiteGemmMma)) break;
+        if (!tc::mbar_wait(&a_full[t], (i / kAStages) & 1, abort, err, kSiteGemmMma)) break;
         tc::tc_fence_after();
         const uint32_t xs = tc::smem_u32(smem + s * Cfg::kStageBytes);
 #pragma unroll
         for (int j = 0; j < BK / 16; ++j) {
           const uint64_t bdesc = tc::smem_desc(xs + 32 * j, 1024, 1024, tc::kSwizzle128B);
-          mma_f16_tmem_a(tmem, a_ring + t * kAColsPerStage + 8 * j, bdesc, idesc, (kt | j) != 0);
+          mma_f16_tmem_a(tmem, a_ring + t * kAColsPerStage + 8 * j, bdesc, idesc, (i | j) != 0);
         }
         tc::tc_commit(&empty[s]);
         tc::tc_commit(&a_empty[t]);
@@ -172,8 +224,10 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       }
     }
   } else {
-    // Dequant warps, then the epilogue.
-    const int q = warp & 3;
+    // Dequant warps, then the epilogue.  Group dg (0 or 1) of the lane
+    // quarter q takes local steps dg, dg + 2, ... and accumulator chunks dg,
+    // dg + 2, ...
+    const int q = warp & 3, dg = (warp - 2) >> 2;
     const int nl = 32 * q + lane;  // this thread's weight column inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     const int gn = n0 + nl;
@@ -187,10 +241,10 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                                    : static_cast<uint32_t>(static_cast<int>(static_cast<const int8_t*>(p.zeros)[g]) + 128);
       sub = (0x6400u | z) * 0x10001u;
     }
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % kStages, t = kt % kAStages;
-      bool ok = tc::mbar_wait(&full[s], (kt / kStages) & 1, abort, err, kSiteGemmProducer);
-      ok = ok && tc::mbar_wait(&a_empty[t], ((kt / kAStages) & 1) ^ 1, abort, err, kSiteGemmTmemFree);
+    for (int i = dg; i < nk; i += 2) {
+      const int s = i % kStages, t = i % kAStages;
+      bool ok = tc::mbar_wait(&full[s], (i / kStages) & 1, abort, err, kSiteGemmProducer);
+      ok = ok && tc::mbar_wait(&a_empty[t], ((i / kAStages) & 1) ^ 1, abort, err, kSiteGemmTmemFree);
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint8_t* wt = smem + s * Cfg::kStageBytes + Cfg::kXBytes + nl;
       uint32_t r[32];
@@ -220,9 +274,22 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     const bool done = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
+    if constexpr (kCluster) {
+      // Park the partial tile, row-major [BM][BN], in the idle ring: every
+      // load has landed and every MMA has completed (accum).
+      float* part = reinterpret_cast<float*>(smem);
+#pragma unroll 1
+      for (int c = dg; c < BM / 32; c += 2) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_off + 32 * c, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part[(32 * c + i) * BN + nl] = __uint_as_float(v[i]);
+      }
+    }
     const float sc = (gn < p.N) ? __half2float(static_cast<const __half*>(p.scales)[gn / p.group_n]) : 0.0f;
     __half* Y = static_cast<__half*>(p.Y);
-    for (int c = 0; c < BM / 32; ++c) {
+    for (int c = dg; c < (kCluster ? 0 : BM / 32); c += 2) {
       uint32_t v[32];
       tc::tmem_ld_32x32b_x32(tmem + lane_off + 32 * c, v);
       tc::tmem_ld_wait();
@@ -235,11 +302,78 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
   }
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cta_barrier();
+  if constexpr (kCluster) {
+    // Every CTA of the cluster gets here (all its waits are bounded), so the
+    // two cluster barriers end.  First: all partial tiles are in place.
+    tc::cluster_sync_all();
+    if (warp >= 2) {
+      // Rows r0 .. r1 - 1 of the tile, four columns per item; all S peers'
+      // float4s of an item are loaded before they are added in rank order.
+      const int r0 = rank * BM / S;
+      const int r1 = min((rank + 1) * BM / S, p.M - m0);
+      const float4* part = reinterpret_cast<const float4*>(smem);
+      const __half* scales = static_cast<const __half*>(p.scales);
+      __half* Y = static_cast<__half*>(p.Y);
+      const bool live = !*abort;
+      for (int it = threadIdx.x - 64; it < (r1 - r0) * (BN / 4); it += kThreads - 64) {
+        const int r = r0 + it / (BN / 4), c4 = it % (BN / 4);
+        float4 v[kMaxClusterK];
+#pragma unroll
+        for (int q = 0; q < kMaxClusterK; ++q)
+          if (q < S) v[q] = tc::dsmem_ld_f4(tc::dsmem_addr(part + r * (BN / 4) + c4, q));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kMaxClusterK; ++q)
+          if (q < S) {
+            acc.x += v[q].x;
+            acc.y += v[q].y;
+            acc.z += v[q].z;
+            acc.w += v[q].w;
+          }
+        const int gn = n0 + 4 * c4;
+        if (!live || gn >= p.N) continue;
+        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        __half h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          h[j] = __float2half_rn(gn + j < p.N ? __half2float(scales[(gn + j) / p.group_n]) * a4[j] : 0.0f);
+        __half* dst = Y + static_cast<int64_t>(m0 + r) * p.ldy + gn;
+        if (gn + 4 <= p.N) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(h2_bits2(h[0], h[1]), h2_bits2(h[2], h[3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (gn + j < p.N) dst[j] = h[j];
+        }
+      }
+    }
+    // Second: no CTA leaves (releasing its shared memory) while a peer may
+    // still read its partial tile.
+    tc::cluster_sync_all();
+  }
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cfg::kTmemCols);
   }
+}
+
+template <int BITS, int BM, bool kCluster>
+cudaError_t configure_tc() {
+  static PerDevice<bool> configured;
+  bool done = false;
+  cudaError_t e = cudaSuccess;
+  if (!configured.get(done, [&](bool& v) {
+        e = cudaFuncSetAttribute(wo_gemm_kernel<BITS, BM, kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 WoGemmCfg<BITS, BM>::kSmemBytes);
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(wo_gemm_kernel<BITS, BM, kCluster>,
+                                   cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        v = true;
+        return e == cudaSuccess;
+      }))
+    return e == cudaSuccess ? cudaErrorUnknown : e;
+  return cudaSuccess;
 }
 
 template <int BITS, int BM>
@@ -253,17 +387,55 @@ cudaError_t launch_tc(const WoArgs& a, cudaStream_t s) {
   e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, w_rows, a.ldw, BN, Cfg::kWRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  auto kern = wo_gemm_kernel<BITS, BM>;
-  static PerDevice<bool> configured;
-  bool done = false;
-  if (!configured.get(done, [&](bool& v) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-        v = true;
-        return e == cudaSuccess;
-      }))
-    return e;
+  if ((e = configure_tc<BITS, BM, false>()) != cudaSuccess) return e;
   dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
-  kern<<<grid, kThreads, Cfg::kSmemBytes, s>>>(tX, tW, a, device_error_word());
+  wo_gemm_kernel<BITS, BM, false><<<grid, kThreads, Cfg::kSmemBytes, s>>>(tX, tW, a, device_error_word());
+  return cudaGetLastError();
+}
+
+// Mid M: the K-split size S of each 128-column tile's cluster.  As many CTAs
+// as the GPU holds at once (tiles x S, with the kCtasPerSm CTAs per SM that
+// the ring and tensor-memory sizes admit), S at most the portable cluster
+// size and at most the number of 64-k steps.
+template <int BITS>
+int mid_split(int N, int K) {
+  using Cfg = WoGemmCfg<BITS, kMidRows>;
+  const int64_t tiles = (N + BN - 1) / BN, kt = (K + BK - 1) / BK;
+  int64_t S = static_cast<int64_t>(sm_count()) * Cfg::kCtasPerSm / tiles;
+  if (S > kMaxClusterK) S = kMaxClusterK;
+  if (S > kt) S = kt;
+  return S < 1 ? 1 : static_cast<int>(S);
+}
+
+template <int BITS>
+cudaError_t launch_mid(const WoArgs& a, cudaStream_t s) {
+  using Cfg = WoGemmCfg<BITS, kMidRows>;
+  CUtensorMap tX, tW;
+  cudaError_t e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.K, a.M, a.ldx * 2, BK, kMidRows,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  const uint64_t w_rows = BITS == 4 ? a.K / 2 : a.K;
+  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, w_rows, a.ldw, BN, Cfg::kWRows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  if ((e = configure_tc<BITS, kMidRows, true>()) != cudaSuccess) return e;
+  const int S = mid_split<BITS>(a.N, a.K);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.N + BN - 1) / BN * S), 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, wo_gemm_kernel<BITS, kMidRows, true>, tX, tW, a, device_error_word());
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -281,6 +453,7 @@ int wo_gemm_rows(int M, int N) {
 
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
+  if (a.M <= kMidRows) return bits == 4 ? launch_mid<4>(a, s) : launch_mid<8>(a, s);
   if (wo_gemm_rows(a.M, a.N) == 128) return bits == 4 ? launch_tc<4, 128>(a, s) : launch_tc<8, 128>(a, s);
   return bits == 4 ? launch_tc<4, 256>(a, s) : launch_tc<8, 256>(a, s);
 }

@@ -72,8 +72,11 @@ static int check_weight_only(int M, int N, int K, const void* X, int64_t ldx, co
 }
 
 // M up to this bound runs the split-K skinny path (HBM-bound); larger M the
-// tiled tensor-memory GEMM.
-constexpr int kSkinnyMaxM = 64;
+// tensor-memory GEMM (up to 64 rows: one activation tile with K split over a
+// cluster; beyond: 128- or 256-row tiles).
+constexpr int kSkinnyMaxM = 16;
+// The batched call runs every problem on the skinny kernel.
+constexpr int kBatchedMaxM = 64;
 
 // The tiled GEMMs put 128-row M tiles on the grid's y dimension (at most
 // 65535 blocks); larger M is refused on the host instead of failing to launch.
@@ -183,7 +186,7 @@ static int prepare_batched(int bits, int count, const wq_problem* problems, WoAr
     const int st = check_weight_only(q.M, q.N, q.K, q.X, q.ldx, q.W, q.ldw, q.scales, q.Y, q.ldy);
     if (st != WQ_OK) return st;
     if (q.M > 0 && q.N > 0 && q.K > 0 && q.ldw < q.N) return WQ_ERR_INVALID_ARG;
-    if (q.M > kSkinnyMaxM) return WQ_ERR_UNSUPPORTED;
+    if (q.M > kBatchedMaxM) return WQ_ERR_UNSUPPORTED;
     a[i] = WoArgs{q.M, q.N, q.K, q.X, q.ldx, q.W, q.ldw, q.scales, q.Y, q.ldy, nullptr, 0, nullptr, q.group_n};
   }
   pl = plan_batched(a, count, bits);

@@ -80,9 +80,11 @@ typedef struct CUstream_st* wq_stream_t;
  *   Y        fp16 [M, N] output, row stride ldy (elements, ldy >= N).
  *   workspace, ws_bytes  device scratch of at least
  *            wq_workspace_size(WQ_OP_W4A16, M, N, K) bytes, 16-byte aligned
- *            (may be NULL when that size is 0).  For M <= 64 the K dimension
- *            is split across CTAs: the first 64 KiB hold one counter per
- *            tile, the partial sums of split tiles follow.  Zero-fill the
+ *            (may be NULL when that size is 0).  For M <= 16 the K dimension
+ *            may be split across CTAs that meet here: the first 64 KiB hold
+ *            one counter per tile, the partial sums of split tiles follow.
+ *            (16 < M <= 64 splits K inside a thread-block cluster and needs
+ *            no workspace; larger M needs none either.)  Zero-fill the
  *            workspace once before its first use; every call that returns
  *            WQ_OK leaves the counter area zero again (the rest is scratch),
  *            so one buffer serves any sequence of calls and shapes on one

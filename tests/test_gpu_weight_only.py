@@ -2,8 +2,8 @@
 
 Tolerance: |y - y_ref| <= 5e-3 * max|y_ref| + 1 fp16 ulp at y_ref, per element.
 Small cases span several 128-column tiles, ragged N/K/M tails and padded leading
-dimensions; the decode workloads run at full size with every output checked;
-large M is checked on sampled rows."""
+dimensions; the decode workloads, the mid-M (17..64 rows) Llama shapes and
+M = 4096 run at full size with every output checked."""
 import numpy as np
 import pytest
 
@@ -113,6 +113,55 @@ def test_out_of_tile_columns_untouched(wq):
     assert_gemm_close(buf[:, :100], _ref(4, case), "fp16")
 
 
+MID_M = [  # (M, K, N, ldx, ldw, ldy): one 64-row activation tile, K split over a cluster
+    (17, 4096, 4096, None, None, None),
+    (64, 64, 128, None, None, None),          # one k-step: clusters of one CTA
+    (48, 128, 4000, None, None, None),        # two k-steps: clusters of two
+    (20, 1000, 300, 1008, 304, 312),          # ragged N and K (partial last k-step), padded strides
+    (33, 712, 1000, None, 1008, None),        # 12 k-steps over clusters of 8
+    (64, 4096, 14336, None, None, None),
+]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N,ldx,ldw,ldy", MID_M)
+def test_mid_m_cases(wq, bits, M, K, N, ldx, ldw, ldy):
+    case = _case(bits, M, K, N, seed=M * 5 + K + N)
+    y = _run(wq, bits, case, ldx, ldw, ldy)
+    assert_gemm_close(y, _ref(bits, case), "fp16")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [17, 33, 64])
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 11008), (11008, 4096)])
+def test_mid_m_llama_shapes(wq, bits, M, K, N):
+    """Every output of the Llama-7B-shaped linears at M in {17, 33, 64}."""
+    case = _case(bits, M, K, N, seed=M + K + N)
+    assert_gemm_close(_run(wq, bits, case), _ref(bits, case), "fp16")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_mid_m_needs_no_workspace_and_is_deterministic(wq, bits):
+    """The cluster K-split adds the partial tiles in a fixed rank order, so two
+    calls give identical bits; it needs no workspace; the padding columns of
+    Y beyond N keep their contents."""
+    M, K, N = 40, 4096, 1000
+    op = wq.WQ_OP_W4A16 if bits == 4 else wq.WQ_OP_W8A16
+    assert wq.wq_workspace_size(op, M, N, K) == 0
+    case = _case(bits, M, K, N, seed=21)
+    x = torch.from_numpy(case.x).cuda()
+    w = dev_matrix(torch, case.w, 1008)
+    s = torch.from_numpy(case.scales).cuda()
+    fn = wq.wq_gemm_w4a16 if bits == 4 else wq.wq_gemm_w8a16
+    buf = torch.full((M, 1024), 7.0, dtype=torch.float16, device="cuda")
+    fn(x, w, s, y=buf[:, :N])
+    y2 = fn(x, w, s)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:, N:] == 7.0)
+    assert torch.equal(buf[:, :N], y2)
+    assert_gemm_close(y2, _ref(bits, case), "fp16")
+
+
 LARGE_M = [  # (M, K, N, ldx, ldw, ldy): the tensor-memory path (M > 64)
     (65, 64, 128, None, None, None),
     (100, 256, 384, None, None, None),
@@ -141,7 +190,7 @@ def test_w8a16_large_m_every_element(wq, M, K, N):
 # with |sum(x)|, which zero-mean activations keep small.  Long K and shifted
 # activations check it against the tolerance (the tensor-memory path, M > 64,
 # subtracts before its MMAs and is checked too).
-SHIFTED = [(1, 14336, 4096), (16, 14336, 4096), (16, 11008, 1024), (100, 14336, 512)]
+SHIFTED = [(1, 14336, 4096), (16, 14336, 4096), (16, 11008, 1024), (40, 14336, 1024), (100, 14336, 512)]
 
 
 @pytest.mark.parametrize("kind", ["normal_mean2", "uniform01"])
@@ -163,7 +212,7 @@ def test_int8_shifted_activations_grouped_zero_points(wq, kind, M, K, N):
     assert_gemm_close(y, O.gemm_w8a16_grouped(x, g.w, g.scales, g.zeros, 128), "fp16")
 
 
-@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 512), (4, 1, 11008, 512), (4, 64, 4096, 256)])
+@pytest.mark.parametrize("bits,M,K,N", [(8, 16, 4096, 512), (4, 1, 11008, 512), (4, 16, 4096, 256)])
 def test_split_k_workspace_contract(wq, bits, M, K, N):
     """Split tiles need scratch; a call leaves the counter area (the first
     64 KiB) zero again, repeated calls are bit-identical (fixed reduction

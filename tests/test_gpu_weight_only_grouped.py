@@ -53,7 +53,9 @@ CASES = [  # (M, K, N, group_n, ldx, ldw, ldy)
     (5, 1000, 3008, 7, None, None, None),         # short last group, ragged K
     (3, 96, 257, 5, None, 272, 264),              # ragged N, padded strides
     (9, 2048, 1000, 1000, 2056, 1008, 1000),      # one group for all columns
-    (64, 2048, 640, 1, None, None, None),         # four 16-row M tiles, per-column groups
+    (64, 2048, 640, 1, None, None, None),         # mid M: K split over a cluster, per-column groups
+    (40, 4096, 4096, 128, None, None, None),      # mid M, eight-CTA clusters
+    (17, 1000, 300, 7, 1008, 304, 312),           # mid M, ragged K and N, padded strides
     (300, 1024, 520, 64, None, 528, None),        # tensor-memory GEMM, ragged M and N
 ]
 
