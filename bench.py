@@ -495,11 +495,40 @@ def time_calls_flushed(torch, wl, steps, warmup):
 # kernel (the profile named beside it).  A figure is used only while the
 # kernel's code is the code it was taken on (same SHA-256 of the source with
 # comments removed, code_sha256); else the roofline reports traffic null.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# a call, from an ncu capture of that call, with the SHA-256 of the code of
+# every source its kernel is compiled from (code_sha256 of each, in order).
+# A figure is reported only while those sources still hold that code.
+SKINNY_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/wo_skinny.cu",
+                  "bit_quantized_gemm_dequant_gb300/csrc/skinny_common.cuh",
+                  "bit_quantized_gemm_dequant_gb300/csrc/tc_common.cuh",
+                  "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
+BATCHED_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/wo_batched.cu",
+                   "bit_quantized_gemm_dequant_gb300/csrc/skinny_common.cuh",
+                   "bit_quantized_gemm_dequant_gb300/csrc/tc_common.cuh",
+                   "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
+WO_GEMM_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/wo_gemm.cu",
+                   "bit_quantized_gemm_dequant_gb300/csrc/tc_common.cuh",
+                   "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
+FP4_GEMM_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/gemm_mxf4.cu",
+                    "bit_quantized_gemm_dequant_gb300/csrc/tc_common.cuh",
+                    "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
+FP8_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/gemm_fp8.cu",
+               "bit_quantized_gemm_dequant_gb300/csrc/tc_common.cuh",
+               "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
 CAPTURED_TRAFFIC = {
-    "w8a16_16x4096x14336": {"bytes": 58_927_360 + 114_432,
-                            "source": "bit_quantized_gemm_dequant_gb300/csrc/wo_skinny.cu",
-                            "sha256": "f939ffb55552f7cb17112bd021a5f104681bd9177ec65473698c9b1de0a08e2e",  # code_sha256
-                            "profile": "profiles/wo_skinny_w8a16_16x4096x14336.md"},
+    "w8a16_16x4096x14336":
+        {"bytes": 58_928_640 + 106_240, "sources": SKINNY_SOURCES, "sha256": "375b74071be0c58c5efd5d8e273ac2b3f7630d7315fa13e37cc6affc92d1380a"},
+    "w8a16_batched_1x4096x4096+4x4096x4096+16x4096x4096+1x4096x14336+4x4096x14336+16x4096x14336":
+        {"bytes": 288_100_864 + 5_674_752, "sources": BATCHED_SOURCES, "sha256": "55a32e47edfb61af6be6edafee3b1923399b30827e1cf203473ea77e299da8e1"},
+    "w4a16_64x4096x11008":
+        {"bytes": 23_120_128 + 0, "sources": WO_GEMM_SOURCES, "sha256": "d818744d19d5bcc0d98991c8aea39771a631eebec17444770932dfa94034cac8"},
+    "mx_gemm_2048x8192x8192":
+        {"bytes": 44_681_472 + 15_734_272, "sources": FP4_GEMM_SOURCES, "sha256": "c0444f47e7e10c91ca8d1431af03c3ef911bf708a0b3cf1b1b9ead66b506329a"},
+    "nv_gemm_2048x8192x8192":
+        {"bytes": 47_315_968 + 16_574_208, "sources": FP4_GEMM_SOURCES, "sha256": "c0444f47e7e10c91ca8d1431af03c3ef911bf708a0b3cf1b1b9ead66b506329a"},
+    "fp8_4096x4096x4096":
+        {"bytes": 33_621_760 + 259_072, "sources": FP8_SOURCES, "sha256": "97433e6524ab3783edb8efbc49fc0dc567493b7763dadc8187e0dfd292484d1a"},
 }
 
 
@@ -515,16 +544,26 @@ def code_sha256(text):
     return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
 
 
+def sources_sha256(paths):
+    """One SHA-256 over the code_sha256 of each source, in order."""
+    import hashlib
+
+    parts = []
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            parts.append(code_sha256(f.read()))
+    return hashlib.sha256("\n".join(parts).encode()).hexdigest()
+
+
 def captured_traffic(call_name):
-    """DRAM bytes of one launch from an ncu capture, while the kernel's code
-    (comments aside) is still the code that was captured; else None."""
+    """DRAM bytes of one launch from an ncu capture, while the kernel's
+    sources (comments aside) still hold the code that was captured; else None."""
     t = CAPTURED_TRAFFIC.get(call_name)
     if t is None:
         return None
     try:
-        with open(os.path.join(ROOT, t["source"]), encoding="utf-8") as f:
-            if code_sha256(f.read()) != t["sha256"]:
-                return None
+        if sources_sha256(t["sources"]) != t["sha256"]:
+            return None
     except OSError:
         return None
     return t["bytes"]
@@ -760,7 +799,7 @@ def run_ours(args):
                 breakdown.append(row)
             else:
                 for c in time_calls_flushed(torch, other, 5, 3):
-                    row = {"workload": name, **c, "roofline": roofline_for(c, peaks)}
+                    row = {"workload": name, **c, "roofline": roofline_for(c, peaks, captured_traffic(c["call"]))}
                     if args.cpu_budget > 0:
                         row["cpu_baseline"] = oracle_rate(other, [next(x for x in other.calls if x["call"] == c["call"])],
                                                           row["roofline"]["unit"], 0.7)

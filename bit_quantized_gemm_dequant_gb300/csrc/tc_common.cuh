@@ -207,6 +207,16 @@ __device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar
                : "memory");
 }
 
+// Generic address of `local`'s counterpart in CTA `rank` of the cluster.
+// Ordinary loads through it read that CTA's shared memory, and the compiler
+// may schedule them freely between two cluster barriers (which order them).
+template <typename T>
+__device__ __forceinline__ const T* peer_ptr(const T* local, uint32_t rank) {
+  uint64_t out;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<const T*>(out);
+}
+
 // Load a float from shared::cluster address `addr` (another CTA's shared
 // memory after a cluster barrier).
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {

@@ -308,20 +308,25 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     // two cluster barriers end.  First: all partial tiles are in place.
     tc::cluster_sync_all();
     if (warp >= 2) {
-      // Rows r0 .. r1 - 1 of the tile, four columns per item; all S peers'
-      // float4s of an item are loaded before they are added in rank order.
+      // Rows r0 .. r1 - 1 of the tile, four columns per item; the S peers'
+      // float4s of an item (plain loads through generic addresses, which the
+      // compiler batches) are added in rank order.
       const int r0 = rank * BM / S;
       const int r1 = min((rank + 1) * BM / S, p.M - m0);
       const float4* part = reinterpret_cast<const float4*>(smem);
+      const float4* peer[kMaxClusterK];
+#pragma unroll
+      for (int q = 0; q < kMaxClusterK; ++q) peer[q] = tc::peer_ptr(part, q < S ? q : 0);
       const __half* scales = static_cast<const __half*>(p.scales);
       __half* Y = static_cast<__half*>(p.Y);
       const bool live = !*abort;
       for (int it = threadIdx.x - 64; it < (r1 - r0) * (BN / 4); it += kThreads - 64) {
         const int r = r0 + it / (BN / 4), c4 = it % (BN / 4);
+        const int off = r * (BN / 4) + c4;
         float4 v[kMaxClusterK];
 #pragma unroll
         for (int q = 0; q < kMaxClusterK; ++q)
-          if (q < S) v[q] = tc::dsmem_ld_f4(tc::dsmem_addr(part + r * (BN / 4) + c4, q));
+          if (q < S) v[q] = peer[q][off];
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < kMaxClusterK; ++q)

@@ -41,5 +41,21 @@ def test_code_hash_ignores_comments_only():
 def test_captured_traffic_only_for_known_calls():
     assert bench.captured_traffic("no_such_call") is None
     for name, t in bench.CAPTURED_TRAFFIC.items():
-        assert t["bytes"] > 0 and os.path.exists(os.path.join(ROOT, t["source"]))
-        assert os.path.exists(os.path.join(ROOT, t["profile"]))
+        assert t["bytes"] > 0 and t["sources"]
+        for rel in t["sources"]:
+            assert os.path.exists(os.path.join(ROOT, rel))
+
+
+def test_sources_hash_tracks_every_source(tmp_path, monkeypatch):
+    """A capture is dropped when any of its sources changes code."""
+    a, b = tmp_path / "a.cu", tmp_path / "b.cuh"
+    a.write_text("int f() { return 1; }\n")
+    b.write_text("int g() { return 2; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.sources_sha256(["a.cu", "b.cuh"])
+    monkeypatch.setitem(bench.CAPTURED_TRAFFIC, "probe_call", {"bytes": 10, "sources": ["a.cu", "b.cuh"], "sha256": h})
+    assert bench.captured_traffic("probe_call") == 10
+    b.write_text("// comment only\nint g() { return 2; }\n")
+    assert bench.captured_traffic("probe_call") == 10
+    b.write_text("int g() { return 3; }\n")
+    assert bench.captured_traffic("probe_call") is None

@@ -42,6 +42,7 @@ def _run(wq, case, lda=None, ldb=None, ldc=None):
     (12, 1000, 520, 1008, 528, 528),     # second MMA column block, ragged N
     (9, 4096, 14336, None, None, None),
     (17, 512, 384, None, None, None),    # just above the skinny bound
+    (2048, 512, 2500, None, 2512, 2504),  # 160 persistent tiles on 152 SMs, ragged N, padded strides
 ])
 def test_fp8_cases(wq, M, K, N, lda, ldb, ldc):
     case = workloads.fp8_case(M, K, N, seed=M + K + N)
