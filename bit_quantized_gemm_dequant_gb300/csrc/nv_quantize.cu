@@ -86,6 +86,26 @@ __device__ __forceinline__ uint32_t e2m1_index(float v) {
   return (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) + (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
 }
 
+// The same index for v = RN(a / d) (a >= 0, d > 0), without the division.
+// Each midpoint t has at most three significant bits and an even last
+// mantissa bit, so RN(a/d) > t exactly when a/d exceeds t + ulp(t)/2 (a tie
+// rounds to the even t), i.e. when a - t*d > h*d with h = ulp(t)/2, a power
+// of two.  The FMA forms a - t*d exactly where it matters: when
+// |a - t*d| <= 4h*d the difference is a multiple of 2^-25 * 2^(e_t + e_d)
+// below 2^-21 * 2^(e_t + e_d), at most four significant bits; beyond that,
+// rounding cannot carry it across h*d.  h*d is exact while d >= 2^-100 (the
+// caller divides otherwise).  Three comparisons, a binary search over the
+// seven midpoints.  hd[i] = h_i * d.
+__device__ __forceinline__ uint32_t e2m1_index_quotient(float a, float d, const float (&hd)[7]) {
+  const bool b2 = __fmaf_rn(-1.75f, d, a) > hd[3];
+  const float t1 = b2 ? 3.5f : 0.75f, h1 = b2 ? hd[5] : hd[1];
+  const bool b1 = __fmaf_rn(-t1, d, a) > h1;
+  const float t0 = b2 ? (b1 ? 5.0f : 2.5f) : (b1 ? 1.25f : 0.25f);
+  const float h0 = b2 ? (b1 ? hd[6] : hd[4]) : (b1 ? hd[2] : hd[0]);
+  const bool b0 = __fmaf_rn(-t0, d, a) > h0;
+  return (b2 ? 4u : 0u) + (b1 ? 2u : 0u) + (b0 ? 1u : 0u);
+}
+
 // One 16-element block per four lanes: the block amax by two shuffles, the
 // E4M3 scale, then each lane's four codes.  Lane 4k gathers the block's four
 // 16-bit code groups into 8 bytes.
@@ -98,8 +118,15 @@ __device__ __forceinline__ void quantize_row4(const NvQuantArgs& p, int r, int c
   const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sb_f, __NV_SATFINITE, __NV_E4M3);
   const float d = __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3))), g);
   uint32_t codes = 0;
-  if (d > 0.0f) {
-    const float xs[4] = {x.x, x.y, x.z, x.w};
+  const float xs[4] = {x.x, x.y, x.z, x.w};
+  if (d >= 0x1p-100f) {
+    // ulp(t)/2 of the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, times d.
+    const float hd[7] = {d * 0x1p-26f, d * 0x1p-25f, d * 0x1p-24f, d * 0x1p-24f, d * 0x1p-23f, d * 0x1p-23f,
+                         d * 0x1p-22f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      codes |= ((xs[i] < 0.0f ? 8u : 0u) | e2m1_index_quotient(fabsf(xs[i]), d, hd)) << (4 * i);
+  } else if (d > 0.0f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       codes |= ((xs[i] < 0.0f ? 8u : 0u) | e2m1_index(__fdiv_rn(xs[i], d))) << (4 * i);
