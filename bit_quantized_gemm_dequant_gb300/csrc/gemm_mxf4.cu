@@ -74,9 +74,12 @@ static_assert(kAccCols + kStages * Fmt<false>::kSfCols <= kTmemCols, "TMEM budge
 
 // K splits: when the output tiles cannot fill half the GPU (M = 128 at
 // N = 8192: 32 tiles), split K so that tiles x splits fill it, keeping at
-// least four K steps per split.  The splits add their partial tiles into C
-// with FP32 reductions, so the order of those (at most 8) additions, and the
-// last bits of C, can differ from call to call.
+// least four K steps per split and at most the portable cluster size.  A
+// tile's splits are one thread-block cluster and add their partial tiles in
+// distributed shared memory, in rank order: the result is deterministic.
+constexpr int kMaxSplits = 8;
+static_assert(BM * BN * 4 <= kStages * kStageBytes, "a partial tile fits in the idle ring");
+
 int mx_splits(int M, int N, int K) {
   const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
   const int kt = (K / 2 + BKB - 1) / BKB;
@@ -84,7 +87,7 @@ int mx_splits(int M, int N, int K) {
   if (2 * tiles >= sms) return 1;
   int S = sms / tiles;
   if (S > kt / 4) S = kt / 4;
-  if (S > 8) S = 8;
+  if (S > kMaxSplits) S = kMaxSplits;
   return S < 1 ? 1 : S;
 }
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -216,12 +219,23 @@ __device__ __forceinline__ float tensor_scale(const MxGemmArgs& p) {
   return 1.0f;
 }
 
-// Add four floats to C (16-byte aligned) in one reduction, without reading
-// them back.
-__device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(__uint_as_float(a)),
-               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
-               : "memory");
+
+// Transpose a 32 x 32 block held one row per lane (lane i: v[j] = B[i][j])
+// into one column per lane (lane j: v[i] = B[i][j]), with five butterfly
+// stages of register exchanges between lanes.
+__device__ __forceinline__ void warp_transpose32(uint32_t (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j & m) continue;
+      const uint32_t send = upper ? v[j] : v[j + m];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+      if (upper) v[j] = recv;
+      else v[j + m] = recv;
+    }
+  }
 }
 
 template <bool kNv, bool kSfTma>
@@ -349,31 +363,30 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc::tc_fence_after();
     const int q = warp & 3;
     const int row_l = 32 * q + lane, row = m0 + row_l;
-    // Split K (gridDim.z > 1): C was zeroed on the stream before the launch,
-    // and every split adds its FP32 partial tile into it.
+    // Split K (a cluster of gridDim.z CTAs): park the FP32 partial tile in
+    // the idle ring (every load has landed and every MMA has completed); the
+    // cluster adds the parts below.  Row r is BN / 4 float4s; within each
+    // group of 8 (32 columns) the float4 v sits at slot (v + r) % 8, so the
+    // eight lanes of a 128-bit store phase (eight rows) hit eight different
+    // bank groups.
     const int S = gridDim.z;
+    float4* part = reinterpret_cast<float4*>(smem);
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
       tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
       tc::tmem_ld_wait();
+      if (S > 1) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          part[row_l * (BN / 4) + 8 * c + ((v + row_l) & 7)] =
+              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
+                          __uint_as_float(r[4 * v + 3]));
+        continue;
+      }
       if (!ok) continue;
       if constexpr (kNv) {
 #pragma unroll
         for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gs);
-      }
-      if (S > 1) {
-        const int col0 = n0 + 32 * c;
-        if (row >= p.M || col0 >= p.N) continue;
-        float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col0;
-        if (col0 + 32 <= p.N) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) red_add_v4(dst + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (col0 + t < p.N) atomicAdd(dst + t, __uint_as_float(r[t]));
-        }
-        continue;
       }
       if (row >= p.M) continue;
       const int col0 = n0 + 32 * c;
@@ -391,27 +404,61 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
   tc::tc_fence_before();
   tc::cta_barrier();
+  if (gridDim.z > 1) {
+    // Every CTA of the cluster gets here (all its waits are bounded), so both
+    // cluster barriers end.  First: every partial tile is in place.
+    tc::cluster_sync_all();
+    const int S = gridDim.z, rank = static_cast<int>(tc::cluster_ctarank());
+    const int r0 = rank * BM / S, r1 = (rank + 1) * BM / S;
+    const float4* part = reinterpret_cast<const float4*>(smem);
+    const float4* peer[kMaxSplits];
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j) peer[j] = tc::peer_ptr(part, j < S ? j : 0);
+    const float gs = tensor_scale<kNv>(p);
+    const bool live = !*abort;
+    // Rows r0 .. r1 - 1 of the tile, four columns per item: the S parts added
+    // in rank order (deterministic), then the tensor scales (NVFP4).
+    for (int it = threadIdx.x; it < (r1 - r0) * (BN / 4); it += blockDim.x) {
+      const int rr = r0 + it / (BN / 4), c4 = it % (BN / 4);
+      const int slot = rr * (BN / 4) + (c4 & ~7) + (((c4 & 7) + rr) & 7);  // the parking rotation
+      float4 v[kMaxSplits];
+#pragma unroll
+      for (int j = 0; j < kMaxSplits; ++j)
+        if (j < S) v[j] = peer[j][slot];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kMaxSplits; ++j)
+        if (j < S) {
+          acc.x += v[j].x;
+          acc.y += v[j].y;
+          acc.z += v[j].z;
+          acc.w += v[j].w;
+        }
+      if constexpr (kNv) {
+        acc.x *= gs;
+        acc.y *= gs;
+        acc.z *= gs;
+        acc.w *= gs;
+      }
+      const int row = m0 + rr, col = n0 + 4 * c4;
+      if (!live || row >= p.M || col >= p.N) continue;
+      float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
+      if (col + 4 <= p.N) {
+        *reinterpret_cast<float4*>(dst) = acc;  // C 16-byte aligned, ldc a multiple of 4
+      } else {
+        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (col + t < p.N) dst[t] = a4[t];
+      }
+    }
+    // Second: no CTA leaves (releasing its shared memory) while a peer may
+    // still read its partial tile.
+    tc::cluster_sync_all();
+  }
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// Transpose a 32 x 32 block held one row per lane (lane i: v[j] = B[i][j])
-// into one column per lane (lane j: v[i] = B[i][j]), with five butterfly
-// stages of register exchanges between lanes.
-__device__ __forceinline__ void warp_transpose32(uint32_t (&v)[32], int lane) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j & m) continue;
-      const uint32_t send = upper ? v[j] : v[j + m];
-      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
-      if (upper) v[j] = recv;
-      else v[j + m] = recv;
-    }
   }
 }
 
@@ -698,12 +745,22 @@ cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
         return e == cudaSuccess;
       }))
     return e;
-  if (splits > 1) {  // the splits add into C
-    e = cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
-    if (e != cudaSuccess) return e;
-  }
-  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
+  // Split K: each tile's splits form a thread-block cluster (along z) that
+  // adds its partial tiles in distributed shared memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tA, tW, tSA, tSW, a, device_error_word());
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -288,10 +288,9 @@ int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
  * Alignment: A, W 16-byte aligned with lda, ldw multiples of 16; C 16-byte
  * aligned with ldc a multiple of 4.
  * When the output tiles are too few to fill the GPU (small M), K is split
- * across CTAs: C is zeroed on `stream` and each split adds its FP32 partial
- * into it.  The order of those additions is not fixed, so the last bits of
- * C may differ between two calls on the same inputs; larger M computes each
- * output in one pass, in a fixed order.
+ * across the CTAs of a thread-block cluster, which add their FP32 partial
+ * tiles in distributed shared memory in a fixed order.  Every shape writes C
+ * once, and two calls on the same inputs give identical bits.
  */
 int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
                 const uint8_t* SA, int64_t ldsa, const uint8_t* W,
@@ -347,8 +346,8 @@ int nv_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
  *   C         fp32 [M, N] output, row stride ldc (elements).
  *   workspace, ws_bytes  unused (0 bytes needed).
  * Alignment: as for mx_gemm_fp4, plus scale_a and scale_w 4-byte aligned.
- * Small M splits K across CTAs as mx_gemm_fp4 does (C is zeroed on `stream`
- * and the splits add into it, in no fixed order).
+ * Small M splits K across a cluster of CTAs as mx_gemm_fp4 does; the result
+ * is deterministic.
  */
 int nv_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
                 const uint8_t* SA, int64_t ldsa, const float* scale_a,

@@ -131,12 +131,12 @@ def test_k_zero(wq):
     assert torch.all(c == 0)
 
 
-def test_split_k_adds_into_c(wq):
-    """M = 128 at N = 8192 has too few tiles to fill the GPU, so K is split and
-    the splits add their partial tiles into C (zeroed first, inside the call).
-    No workspace is needed; repeated calls agree within the tolerance (the
-    order of the additions may differ), and C's previous contents do not
-    matter."""
+def test_split_k_cluster_is_deterministic(wq):
+    """M = 128 at N = 8192 has too few tiles to fill the GPU, so K is split
+    over a cluster of CTAs that add their partial tiles in distributed shared
+    memory, in rank order.  No workspace is needed; C's previous contents do
+    not matter; two calls give identical bits; every element matches the
+    oracle."""
     M, N, K = 128, 8192, 4096
     assert wq.wq_workspace_size(wq.WQ_OP_MX_GEMM, M, N, K) == 0
     a = workloads.mx_source(M, K, seed=3, stream=0)
@@ -147,8 +147,20 @@ def test_split_k_adds_into_c(wq):
     wq.mx_gemm_fp4(ad, asc, wd, wsc, c=c)
     c2 = wq.mx_gemm_fp4(ad, asc, wd, wsc)
     torch.cuda.synchronize()
-    rows = np.array([0, 1, 63, 127])
-    ref = O.mx_gemm_fp4(ad.cpu().numpy(), asc.cpu().numpy(), wd.cpu().numpy(), wsc.cpu().numpy(), rows=rows)
-    idx = torch.from_numpy(rows).cuda()
-    assert_gemm_close(c[idx], ref, "fp32")
-    assert_gemm_close(c2[idx], ref, "fp32")
+    assert torch.equal(c, c2)
+    ref = O.mx_dequantize(ad.cpu().numpy(), asc.cpu().numpy()) @ O.mx_dequantize(wd.cpu().numpy(), wsc.cpu().numpy()).T
+    assert_gemm_close(c, ref, "fp32")
+
+
+@pytest.mark.parametrize("M,N,K,ldc", [(1, 2560, 8192, 2564), (100, 300, 2048, 304), (8, 256, 4096, None)])
+def test_split_k_cluster_ragged(wq, M, N, K, ldc):
+    """Split-K clusters with ragged M and N (the rows and columns past the
+    matrix are neither read nor written), clusters of 8 and a padded ldc."""
+    a = workloads.mx_source(M, K, seed=M, stream=0)
+    w = workloads.mx_source(N, K, seed=N, stream=1)
+    ad, asc = O.mx_quantize_fp4(a)
+    wd, wsc = O.mx_quantize_fp4(w)
+    c = dev_empty(torch, M, N, torch.float32, ldc, fill=float("nan"))
+    wq.mx_gemm_fp4(dev_matrix(torch, ad), dev_matrix(torch, asc), dev_matrix(torch, wd), dev_matrix(torch, wsc), c=c)
+    torch.cuda.synchronize()
+    assert_gemm_close(c, O.mx_dequantize(ad, asc) @ O.mx_dequantize(wd, wsc).T, "fp32")
