@@ -53,10 +53,9 @@ namespace wq {
 namespace {
 
 constexpr int BN = 128;            // weight columns per CTA (MMA M)
-constexpr int BK = 64;             // k per stage
+constexpr int kXBoxK = 64;         // k per X box (128 bytes of fp16: one swizzle span)
 constexpr int kDequantWarps = 8;   // two per TMEM lane quarter
 constexpr int kThreads = (2 + kDequantWarps) * 32;
-constexpr int kAColsPerStage = BK / 2;  // fp16 pairs per TMEM lane
 constexpr int kMidRows = 64;       // activation rows of the mid-M (cluster K-split) instance
 constexpr int kMaxClusterK = 8;    // portable cluster size
 
@@ -65,15 +64,24 @@ constexpr int kSmemPerCtaReserved = 1024;
 
 template <int BITS, int BM>
 struct WoGemmCfg {
-  static constexpr int kXBytes = BM * BK * 2;
-  static constexpr int kWRows = BITS == 4 ? BK / 2 : BK;
+  // k per stage.  A stage has a fixed cost (the barrier round trips of its
+  // TMA -> dequant -> MMA chain), so fewer, larger stages pay off where the
+  // ring still holds several: INT4 at every tile height (W4A16 4096^3 went
+  // from 138 to 118 us, M = 64 at N = 11008 from 18.1 to 16.3 us) and INT8 at
+  // 128 rows (M = 512: 34.5 to 28.4 us).  INT8 keeps 64 at 64 rows (three
+  // stages instead of six: 5% slower) and at 256 rows (two stages: 19% slower).
+  static constexpr int kBK = (BITS == 4 || BM == 128) ? 128 : 64;
+  static constexpr int kXBoxes = kBK / kXBoxK;     // X boxes per stage
+  static constexpr int kACols = kBK / 2;           // TMEM columns (fp16 pairs) per A slice
+  static constexpr int kXBytes = BM * kBK * 2;
+  static constexpr int kWRows = BITS == 4 ? kBK / 2 : kBK;
   static constexpr int kWBytes = kWRows * BN;
   static constexpr int kStageBytes = ((kXBytes + kWBytes + 1023) / 1024) * 1024;
   static constexpr int kAccCols = BM;
   static constexpr int kTmemCols = BM == kMidRows ? 256 : 512;  // mid M: two CTAs per SM
   static constexpr int kCtasPerSm = 512 / kTmemCols;
   // TMEM A ring: the columns the accumulator leaves, at most 8 slices.
-  static constexpr int kAStagesFit = (kTmemCols - kAccCols) / kAColsPerStage;
+  static constexpr int kAStagesFit = (kTmemCols - kAccCols) / kACols;
   static constexpr int kAStages = kAStagesFit > 8 ? 8 : kAStagesFit;
   // Shared-memory ring: as deep as the SM's share for kCtasPerSm CTAs allows
   // (at most 8 stages).  The ring also keeps a (kCtasPerSm + 1)-th CTA off
@@ -84,7 +92,8 @@ struct WoGemmCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
   static_assert(kStages >= 2, "ring depth");
   static_assert((kSmemBytes + kSmemPerCtaReserved) * (kCtasPerSm + 1) > kSmPerSmem, "one CTA too many per SM");
-  static_assert(kAccCols + kAStages * kAColsPerStage <= kTmemCols, "TMEM budget");
+  static_assert(kAccCols + kAStages * kACols <= kTmemCols, "TMEM budget");
+  static_assert(kAStages >= 2, "TMEM A ring depth");
   // Mid M: the FP32 partial tile [BM rows][BN columns] reuses the idle ring.
   static_assert(BM != kMidRows || BM * BN * 4 <= kStages * kStageBytes, "partial tile fits in the ring");
 };
@@ -121,7 +130,7 @@ __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
 }
 
 template <int BITS, int BM, bool kCluster>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCluster ? 2 : 1)  // mid M: two CTAs per SM
 wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, WoArgs p,
                int* err) {
   using Cfg = WoGemmCfg<BITS, BM>;
@@ -139,7 +148,7 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KT = (p.K + BK - 1) / BK;
+  const int KT = (p.K + Cfg::kBK - 1) / Cfg::kBK;
   // This CTA's 128-column tile and its k-tiles [kt0, kt0 + nk): all of K, or
   // (cluster K-split) the rank's share.
   int n_tile = blockIdx.x, rank = 0, S = 1;
@@ -190,7 +199,9 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         if (!tc::mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer)) break;
         uint8_t* st = smem + s * Cfg::kStageBytes;
         tc::mbar_arrive_expect_tx(&full[s], Cfg::kXBytes + Cfg::kWBytes);
-        tc::tma_load_2d(st, &tmX, kt * BK, m0, &full[s]);
+#pragma unroll
+        for (int h = 0; h < Cfg::kXBoxes; ++h)
+          tc::tma_load_2d(st + h * BM * kXBoxK * 2, &tmX, kt * Cfg::kBK + h * kXBoxK, m0, &full[s]);
         tc::tma_load_2d(st + Cfg::kXBytes, &tmW, n0, kt * Cfg::kWRows, &full[s]);
         issued = i + 1;
       }
@@ -208,9 +219,10 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         tc::tc_fence_after();
         const uint32_t xs = tc::smem_u32(smem + s * Cfg::kStageBytes);
 #pragma unroll
-        for (int j = 0; j < BK / 16; ++j) {
-          const uint64_t bdesc = tc::smem_desc(xs + 32 * j, 1024, 1024, tc::kSwizzle128B);
-          mma_f16_tmem_a(tmem, a_ring + t * kAColsPerStage + 8 * j, bdesc, idesc, (i | j) != 0);
+        for (int j = 0; j < Cfg::kBK / 16; ++j) {  // 16 k per MMA, four per 64-k X box
+          const uint64_t bdesc =
+              tc::smem_desc(xs + (j / 4) * BM * kXBoxK * 2 + 32 * (j % 4), 1024, 1024, tc::kSwizzle128B);
+          mma_f16_tmem_a(tmem, a_ring + t * Cfg::kACols + 8 * j, bdesc, idesc, (i | j) != 0);
         }
         tc::tc_commit(&empty[s]);
         tc::tc_commit(&a_empty[t]);
@@ -247,26 +259,32 @@ wo_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       ok = ok && tc::mbar_wait(&a_empty[t], ((i / kAStages) & 1) ^ 1, abort, err, kSiteGemmTmemFree);
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint8_t* wt = smem + s * Cfg::kStageBytes + Cfg::kXBytes + nl;
-      uint32_t r[32];
-      if constexpr (BITS == 4) {
+      tc::tc_fence_after();
+      // The stage's k in 64-k halves (32 fp16 pairs each), so that one half's
+      // registers are live at a time.
+#pragma unroll 1
+      for (int h = 0; h < Cfg::kXBoxes; ++h) {
+        uint32_t r[32];
+        if constexpr (BITS == 4) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t b = wt[c * BN];  // codes of k = 2c (low nibble), 2c + 1
-          const uint32_t v = ((b * 0x1001u) & 0x000F000Fu) | 0x64006400u;
-          r[c] = h2_sub(v, sub);  // minus 1024 + zero point
-        }
-      } else {
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t b = wt[(32 * h + c) * BN];  // codes of k = 2c (low nibble), 2c + 1 of the half
+            const uint32_t v = ((b * 0x1001u) & 0x000F000Fu) | 0x64006400u;
+            r[c] = h2_sub(v, sub);  // minus 1024 + zero point
+          }
+        } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t b = static_cast<uint32_t>(wt[(2 * c) * BN]) | (static_cast<uint32_t>(wt[(2 * c + 1) * BN]) << 16);
-          r[c] = h2_sub((b ^ 0x00800080u) | 0x64006400u, sub);  // minus 1152 + zero point
+          for (int c = 0; c < 32; ++c) {
+            const int row = 64 * h + 2 * c;
+            const uint32_t b = static_cast<uint32_t>(wt[row * BN]) | (static_cast<uint32_t>(wt[(row + 1) * BN]) << 16);
+            r[c] = h2_sub((b ^ 0x00800080u) | 0x64006400u, sub);  // minus 1152 + zero point
+          }
         }
+        tmem_st_32x32b_x32(a_ring + t * Cfg::kACols + 32 * h + lane_off, r);
       }
       tc::fence_proxy_async_smem();  // generic reads of the tile before its TMA refill
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&empty[s]);  // this warp is done with the packed tile
-      tc::tc_fence_after();
-      tmem_st_32x32b_x32(a_ring + t * kAColsPerStage + lane_off, r);
       tmem_st_wait();
       tc::tc_fence_before();
       __syncwarp();
@@ -385,7 +403,7 @@ template <int BITS, int BM>
 cudaError_t launch_tc(const WoArgs& a, cudaStream_t s) {
   using Cfg = WoGemmCfg<BITS, BM>;
   CUtensorMap tX, tW;
-  cudaError_t e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.K, a.M, a.ldx * 2, BK, BM,
+  cudaError_t e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.K, a.M, a.ldx * 2, kXBoxK, BM,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   const uint64_t w_rows = BITS == 4 ? a.K / 2 : a.K;
@@ -405,7 +423,7 @@ cudaError_t launch_tc(const WoArgs& a, cudaStream_t s) {
 template <int BITS>
 int mid_split(int N, int K) {
   using Cfg = WoGemmCfg<BITS, kMidRows>;
-  const int64_t tiles = (N + BN - 1) / BN, kt = (K + BK - 1) / BK;
+  const int64_t tiles = (N + BN - 1) / BN, kt = (K + Cfg::kBK - 1) / Cfg::kBK;
   int64_t S = static_cast<int64_t>(sm_count()) * Cfg::kCtasPerSm / tiles;
   if (S > kMaxClusterK) S = kMaxClusterK;
   if (S > kt) S = kt;
@@ -416,7 +434,7 @@ template <int BITS>
 cudaError_t launch_mid(const WoArgs& a, cudaStream_t s) {
   using Cfg = WoGemmCfg<BITS, kMidRows>;
   CUtensorMap tX, tW;
-  cudaError_t e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.K, a.M, a.ldx * 2, BK, kMidRows,
+  cudaError_t e = make_tmap_2d(&tX, a.X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.K, a.M, a.ldx * 2, kXBoxK, kMidRows,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   const uint64_t w_rows = BITS == 4 ? a.K / 2 : a.K;
