@@ -522,11 +522,11 @@ CAPTURED_TRAFFIC = {
     "w8a16_batched_1x4096x4096+4x4096x4096+16x4096x4096+1x4096x14336+4x4096x14336+16x4096x14336":
         {"bytes": 288_100_864 + 5_674_752, "sources": BATCHED_SOURCES, "sha256": "55a32e47edfb61af6be6edafee3b1923399b30827e1cf203473ea77e299da8e1"},
     "w4a16_64x4096x11008":
-        {"bytes": 23_120_128 + 0, "sources": WO_GEMM_SOURCES, "sha256": "d818744d19d5bcc0d98991c8aea39771a631eebec17444770932dfa94034cac8"},
+        {"bytes": 23_121_408 + 0, "sources": WO_GEMM_SOURCES, "sha256": "45782ffb76b9a8b537c105903b0d991a79009bd3bdc6b13d451be3c6779c16a2"},
     "mx_gemm_2048x8192x8192":
-        {"bytes": 44_681_472 + 15_734_272, "sources": FP4_GEMM_SOURCES, "sha256": "c0444f47e7e10c91ca8d1431af03c3ef911bf708a0b3cf1b1b9ead66b506329a"},
+        {"bytes": 44_657_152 + 16_124_928, "sources": FP4_GEMM_SOURCES, "sha256": "26da4d076ef70a3eaeb7c7c71b1b51712691eb48b30080b5d1e2ecafa481dcfe"},
     "nv_gemm_2048x8192x8192":
-        {"bytes": 47_315_968 + 16_574_208, "sources": FP4_GEMM_SOURCES, "sha256": "c0444f47e7e10c91ca8d1431af03c3ef911bf708a0b3cf1b1b9ead66b506329a"},
+        {"bytes": 47_307_264 + 16_542_464, "sources": FP4_GEMM_SOURCES, "sha256": "26da4d076ef70a3eaeb7c7c71b1b51712691eb48b30080b5d1e2ecafa481dcfe"},
     "fp8_4096x4096x4096":
         {"bytes": 33_621_760 + 259_072, "sources": FP8_SOURCES, "sha256": "97433e6524ab3783edb8efbc49fc0dc567493b7763dadc8187e0dfd292484d1a"},
 }
