@@ -403,8 +403,12 @@ cudaError_t launch_batched_variant(const WoArgs* probs, int count, const BatchPl
     units += bp.tiles * bp.chunks;
     tiles += bp.tiles;
     const uint64_t rows = BITS == kInt4 ? a.K / 2 : a.K;
+    // 128-byte L2 fetches: a CTA's run walks one tile's K range, so the 128
+    // bytes next to a box row (the neighbouring tile) are read by another CTA
+    // much later; with 256-byte fetches they were fetched twice (ncu: 288 MB
+    // of DRAM reads for 227 MB of weights, 229 MB with 128-byte fetches).
     e = make_tmap_2d(&tb.tmW[n], a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, rows, a.ldw, kTileN, kBoxRows,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
     if (e != cudaSuccess) return e;
     const CUtensorMapSwizzle xs = C::kXRowBytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : C::kXRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
