@@ -518,9 +518,9 @@ FP8_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/gemm_fp8.cu",
                "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
 CAPTURED_TRAFFIC = {
     "w8a16_16x4096x14336":
-        {"bytes": 58_928_640 + 106_240, "sources": SKINNY_SOURCES, "sha256": "375b74071be0c58c5efd5d8e273ac2b3f7630d7315fa13e37cc6affc92d1380a"},
+        {"bytes": 58_928_640 + 70_400, "sources": SKINNY_SOURCES, "sha256": "0012c4e4480b5913ea94e04d9d782aca4a797f80180c6c7af3290f0a3e2b85c8"},
     "w8a16_batched_1x4096x4096+4x4096x4096+16x4096x4096+1x4096x14336+4x4096x14336+16x4096x14336":
-        {"bytes": 288_100_864 + 5_674_752, "sources": BATCHED_SOURCES, "sha256": "55a32e47edfb61af6be6edafee3b1923399b30827e1cf203473ea77e299da8e1"},
+        {"bytes": 227_880_704 + 5_643_776, "sources": BATCHED_SOURCES, "sha256": "fb11efdcfa21174e7bb33e576a97be592795b111cc459230fff55d447cdca3bb"},
     "w4a16_64x4096x11008":
         {"bytes": 23_121_408 + 0, "sources": WO_GEMM_SOURCES, "sha256": "45782ffb76b9a8b537c105903b0d991a79009bd3bdc6b13d451be3c6779c16a2"},
     "mx_gemm_2048x8192x8192":
