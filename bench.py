@@ -186,7 +186,10 @@ class WeightOnly:
 
 
 class MxFp4:
-    """Per M: quantize A [M, K] and W [N, K] on the device, then C = A W^T."""
+    """Per M: quantize A [M, K] and W [N, K] on the device, then C = A W^T.
+    W's block scales go into the tensor cores' layout once per step, as part
+    of preparing W (the quantize-W call); each GEMM call rearranges A's
+    scales, then runs mx_gemm_fp4_tc."""
 
     def __init__(self, torch, wq, shapes, replicas, seed=0):
         self.torch, self.wq = torch, wq
@@ -199,20 +202,20 @@ class MxFp4:
         for _ in range(replicas if wq is not None else 0):  # wq None: host-side sources only (oracle arm)
             w = torch.from_numpy(self.w_src).cuda()
             wd, wsc = wq.mx_quantize_fp4(w)
-            reps = {"w": (w, wd, wsc), "a": []}
+            reps = {"w": (w, wd, wsc, wq.fp4_scales_tc(wsc, K)), "a": []}
             for a_src in self.a_srcs:
                 a = torch.from_numpy(a_src).cuda()
                 ad, asc = wq.mx_quantize_fp4(a)
                 c = torch.empty((a.shape[0], N), dtype=torch.float32, device="cuda")
-                reps["a"].append((a, ad, asc, c))
+                reps["a"].append((a, ad, asc, wq.fp4_scales_tc(asc, K), c))
             self.dev.append(reps)
-        self.calls = [{"call": f"mx_quantize_{N}x{K}", "index": ("qw", 0),
+        self.calls = [{"call": f"mx_quantize_{N}x{K}", "index": ("qw", 0), "launches": 2,
                        "bytes": N * K * 4 + N * K // 2 + N * K // 32, "flops": 0, "bound": "hbm", "dtype": "fp4"}]
         for i, (M, _, _) in enumerate(shapes):
             self.calls.append({"call": f"mx_quantize_{M}x{K}", "index": ("qa", i),
                                "bytes": M * K * 4 + M * K // 2 + M * K // 32, "flops": 0, "bound": "hbm",
                                "dtype": "fp4"})
-            self.calls.append({"call": f"mx_gemm_{M}x{K}x{N}", "index": ("g", i),
+            self.calls.append({"call": f"mx_gemm_{M}x{K}x{N}", "index": ("g", i), "launches": 2,
                                "bytes": (M + N) * (K // 2 + K // 32) + 4 * M * N, "flops": 2 * M * N * K,
                                "bound": "hbm" if M <= 128 else "tensor", "dtype": "fp4"})
 
@@ -243,19 +246,22 @@ class MxFp4:
     def run(self, r, idx):
         kind, i = idx
         d = self.dev[r]
-        w, wd, wsc = d["w"]
+        w, wd, wsc, wsc_tc = d["w"]
         if kind == "qw":
             self.wq.mx_quantize_fp4(w, wd, wsc)
+            self.wq.fp4_scales_tc(wsc, self.K, out=wsc_tc)
             return
-        a, ad, asc, c = d["a"][i]
+        a, ad, asc, asc_tc, c = d["a"][i]
         if kind == "qa":
             self.wq.mx_quantize_fp4(a, ad, asc)
         else:
-            self.wq.mx_gemm_fp4(ad, asc, wd, wsc, c=c)
+            self.wq.fp4_scales_tc(asc, self.K, out=asc_tc)
+            self.wq.mx_gemm_fp4_tc(ad, asc_tc, wd, wsc_tc, c=c)
 
 
 class NvFp4:
-    """Per M: quantize A [M, K] and W [N, K] to NVFP4 on the device, then C = A W^T."""
+    """Per M: quantize A [M, K] and W [N, K] to NVFP4 on the device, then C = A W^T
+    (block scales rearranged as in MxFp4)."""
 
     def __init__(self, torch, wq, shapes, replicas, seed=0):
         self.torch, self.wq = torch, wq
@@ -268,23 +274,24 @@ class NvFp4:
         for _ in range(replicas if wq is not None else 0):  # wq None: host-side sources only (oracle arm)
             w = torch.from_numpy(self.w_src).cuda()
             wd, wsc, gw = wq.nv_quantize_fp4(w)
-            reps = {"w": (w, wd, wsc, gw), "a": []}
+            nv = wq.WQ_FP4_NV
+            reps = {"w": (w, wd, wsc, gw, wq.fp4_scales_tc(wsc, K, nv)), "a": []}
             for a_src in self.a_srcs:
                 a = torch.from_numpy(a_src).cuda()
                 ad, asc, ga = wq.nv_quantize_fp4(a)
                 c = torch.empty((a.shape[0], N), dtype=torch.float32, device="cuda")
-                reps["a"].append((a, ad, asc, ga, c))
+                reps["a"].append((a, ad, asc, ga, wq.fp4_scales_tc(asc, K, nv), c))
             self.dev.append(reps)
 
         def qbytes(r):  # the source twice (amax, then codes), codes and E4M3 scales out
             return r * K * 8 + r * K // 2 + r * K // 16
 
-        self.calls = [{"call": f"nv_quantize_{N}x{K}", "index": ("qw", 0), "bytes": qbytes(N), "flops": 0,
-                       "bound": "hbm", "dtype": "fp4"}]
+        self.calls = [{"call": f"nv_quantize_{N}x{K}", "index": ("qw", 0), "launches": 4, "bytes": qbytes(N),
+                       "flops": 0, "bound": "hbm", "dtype": "fp4"}]
         for i, (M, _, _) in enumerate(shapes):
-            self.calls.append({"call": f"nv_quantize_{M}x{K}", "index": ("qa", i), "bytes": qbytes(M), "flops": 0,
-                               "bound": "hbm", "dtype": "fp4"})
-            self.calls.append({"call": f"nv_gemm_{M}x{K}x{N}", "index": ("g", i),
+            self.calls.append({"call": f"nv_quantize_{M}x{K}", "index": ("qa", i), "launches": 3,
+                               "bytes": qbytes(M), "flops": 0, "bound": "hbm", "dtype": "fp4"})
+            self.calls.append({"call": f"nv_gemm_{M}x{K}x{N}", "index": ("g", i), "launches": 2,
                                "bytes": (M + N) * (K // 2 + K // 16) + 4 * M * N, "flops": 2 * M * N * K,
                                "bound": "hbm" if M <= 128 else "tensor", "dtype": "fp4"})
 
@@ -314,15 +321,18 @@ class NvFp4:
     def run(self, r, idx):
         kind, i = idx
         d = self.dev[r]
-        w, wd, wsc, gw = d["w"]
+        w, wd, wsc, gw, wsc_tc = d["w"]
+        nv = self.wq.WQ_FP4_NV
         if kind == "qw":
             self.wq.nv_quantize_fp4(w, wd, wsc, gw)
+            self.wq.fp4_scales_tc(wsc, self.K, nv, out=wsc_tc)
             return
-        a, ad, asc, ga, c = d["a"][i]
+        a, ad, asc, ga, asc_tc, c = d["a"][i]
         if kind == "qa":
             self.wq.nv_quantize_fp4(a, ad, asc, ga)
         else:
-            self.wq.nv_gemm_fp4(ad, asc, ga, wd, wsc, gw, c=c)
+            self.wq.fp4_scales_tc(asc, self.K, nv, out=asc_tc)
+            self.wq.nv_gemm_fp4_tc(ad, asc_tc, ga, wd, wsc_tc, gw, c=c)
 
 
 class Fp8:
@@ -824,7 +834,7 @@ def run_ours(args):
             "roofline": roof,
             "per_call": [{**c, "achieved": roofline_for(c, peaks)["achieved"]} for c in per_call],
             "e2e": e2e,
-            "gpu_launches": len(wl.calls) * args.steps,
+            "gpu_launches": sum(c.get("launches", 1) for c in wl.calls) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "breakdown": breakdown,

@@ -33,7 +33,8 @@ WQ_ERR_WORKSPACE = 4
 WQ_ERR_LAUNCH = 5
 WQ_ERR_DEVICE = 6
 
-WQ_OP_W4A16, WQ_OP_W8A16, WQ_OP_MX_QUANTIZE, WQ_OP_MX_GEMM, WQ_OP_FP8_GEMM = range(5)
+WQ_OP_W4A16, WQ_OP_W8A16, WQ_OP_MX_QUANTIZE, WQ_OP_MX_GEMM, WQ_OP_FP8_GEMM, WQ_OP_NV_GEMM = range(6)
+WQ_FP4_MX, WQ_FP4_NV = 0, 1
 
 _i, _i64, _p, _sz, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
 _SIGS = {
@@ -47,6 +48,10 @@ _SIGS = {
     "fp8_gemm": [_i, _i, _i, _p, _i64, _p, _i64, _f, _f, _p, _i64, _p, _sz, _p],
     "nv_quantize_fp4": [_i, _i, _p, _i64, _p, _i64, _p, _i64, _p, _p],
     "nv_gemm_fp4": [_i, _i, _i, _p, _i64, _p, _i64, _p, _p, _i64, _p, _i64, _p, _p, _i64, _p, _sz, _p],
+    "fp4_scales_tc_size": [_i, _i, _i],
+    "fp4_scales_tc": [_i, _i, _i, _p, _i64, _p, _sz, _p],
+    "mx_gemm_fp4_tc": [_i, _i, _i, _p, _i64, _p, _sz, _p, _i64, _p, _sz, _p, _i64, _p],
+    "nv_gemm_fp4_tc": [_i, _i, _i, _p, _i64, _p, _sz, _p, _p, _i64, _p, _sz, _p, _p, _i64, _p],
     "wq_workspace_size": [_i, _i, _i, _i],
     "wq_status_string": [_i],
     "wq_get_device_error": [_p, ctypes.POINTER(_i)],
@@ -70,6 +75,7 @@ for _name, _args in _SIGS.items():
     _fn.argtypes = _args
     _fn.restype = _i
 lib.wq_workspace_size.restype = _sz
+lib.fp4_scales_tc_size.restype = _sz
 lib.wq_batched_workspace_size.restype = _sz
 lib.wq_status_string.restype = ctypes.c_char_p
 
@@ -186,18 +192,21 @@ def auto_workspace(op: int, M: int, N: int, K: int, device):
     zero-filled when created, cached per (device, stream) and grown on demand.
     Every successful call leaves its counter area zero again, so the cached
     buffer is reused as is; calls that share one must not overlap on the GPU
-    (one cache entry per stream)."""
+    (one cache entry per stream).  The FP4 GEMMs' scratch (rewritten scales,
+    no counters) has a cache entry of its own, so that it never overwrites
+    the weight-only calls' counters."""
     import torch
 
-    return _cached_workspace(wq_workspace_size(op, M, N, K), device)
+    tag = "fp4" if op in (WQ_OP_MX_GEMM, WQ_OP_NV_GEMM) else "counters"
+    return _cached_workspace(wq_workspace_size(op, M, N, K), device, tag)
 
 
-def _cached_workspace(need: int, device):
+def _cached_workspace(need: int, device, tag: str = "counters"):
     import torch
 
     if need == 0:
         return None
-    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    key = (tag, torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
     buf = _WS_CACHE.get(key)
     if buf is None or buf.numel() < need:
         buf = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=device)
@@ -370,9 +379,54 @@ def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
     _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
     if c is None:
         c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    if workspace is None:
+        workspace = auto_workspace(WQ_OP_MX_GEMM, M, N, K, a.device)
     wsp, wsb = _ws(workspace)
     _check(lib.mx_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
                            _ptr(c), _ld(c), wsp, wsb, _stream(stream)), "mx_gemm_fp4")
+    return c
+
+
+def fp4_scales_tc(scales, K, fmt=WQ_FP4_MX, out=None, stream=None):
+    """Block scales uint8 [rows, K / block] -> the tensor-core layout (a flat
+    uint8 tensor of fp4_scales_tc_size bytes) that mx_gemm_fp4_tc and
+    nv_gemm_fp4_tc read."""
+    import torch
+
+    where = "fp4_scales_tc"
+    _on_gpu(where, scales, out)
+    _kind(where, scales, "scales", size=1)
+    _require(scales.dim() == 2, where, "scales must be 2-D")
+    block = 16 if fmt == WQ_FP4_NV else 32
+    rows = scales.shape[0]
+    _require(K % block == 0 and scales.shape[1] == K // block, where, f"scales must be [rows, {K // block}]")
+    need = int(lib.fp4_scales_tc_size(fmt, rows, K))
+    if out is None:
+        out = torch.empty(max(need, 1), dtype=torch.uint8, device=scales.device)
+    _kind(where, out, "out", size=1)
+    _check(lib.fp4_scales_tc(fmt, rows, K, _ptr(scales), _ld(scales), _ptr(out), out.numel(), _stream(stream)), where)
+    return out
+
+
+def mx_gemm_fp4_tc(a, sa_tc, w, sw_tc, c=None, stream=None):
+    """mx_gemm_fp4 with both scale arrays already in the tensor-core layout
+    (fp4_scales_tc): C fp32 [M, N] = A * W^T."""
+    import torch
+
+    where = "mx_gemm_fp4_tc"
+    _on_gpu(where, a, sa_tc, w, sw_tc, c)
+    for t, n in ((a, "a"), (sa_tc, "sa_tc"), (w, "w"), (sw_tc, "sw_tc")):
+        _kind(where, t, n, size=1)
+    _require(a.dim() == 2 and w.dim() == 2, where, "a and w must be 2-D")
+    _require(sa_tc.is_contiguous() and sw_tc.is_contiguous(), where, "tensor-core scales must be contiguous")
+    _kind(where, c, "c", dtype="float32")
+    M, N, K = a.shape[0], w.shape[0], a.shape[1] * 2
+    _require(w.shape[1] * 2 == K, where, "a and w must have the same K")
+    _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check(lib.mx_gemm_fp4_tc(M, N, K, _ptr(a), _ld(a), _ptr(sa_tc), sa_tc.numel(), _ptr(w), _ld(w), _ptr(sw_tc),
+                              sw_tc.numel(), _ptr(c), _ld(c), _stream(stream)), where)
     return c
 
 
@@ -403,7 +457,7 @@ def nv_quantize_fp4(src, data=None, scales=None, tensor_scale=None, stream=None)
     return data, scales, tensor_scale
 
 
-def nv_gemm_fp4(a, sa, ga, w, sw, gw, c=None, stream=None):
+def nv_gemm_fp4(a, sa, ga, w, sw, gw, c=None, workspace=None, stream=None):
     """C fp32 [M, N] = A * W^T for NVFP4 operands (data [rows, K/2], E4M3
     scales [rows, K/16], tensor scale [1] on the device)."""
     import torch
@@ -423,8 +477,35 @@ def nv_gemm_fp4(a, sa, ga, w, sw, gw, c=None, stream=None):
     _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
     if c is None:
         c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    if workspace is None:
+        workspace = auto_workspace(WQ_OP_NV_GEMM, M, N, K, a.device)
+    wsp, wsb = _ws(workspace)
     _check(lib.nv_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(ga), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
-                           _ptr(gw), _ptr(c), _ld(c), _p(0), 0, _stream(stream)), where)
+                           _ptr(gw), _ptr(c), _ld(c), wsp, wsb, _stream(stream)), where)
+    return c
+
+
+def nv_gemm_fp4_tc(a, sa_tc, ga, w, sw_tc, gw, c=None, stream=None):
+    """nv_gemm_fp4 with both E4M3 scale arrays already in the tensor-core
+    layout (fp4_scales_tc with WQ_FP4_NV)."""
+    import torch
+
+    where = "nv_gemm_fp4_tc"
+    _on_gpu(where, a, sa_tc, ga, w, sw_tc, gw, c)
+    for t, n in ((a, "a"), (sa_tc, "sa_tc"), (w, "w"), (sw_tc, "sw_tc")):
+        _kind(where, t, n, size=1)
+    _require(a.dim() == 2 and w.dim() == 2, where, "a and w must be 2-D")
+    _require(sa_tc.is_contiguous() and sw_tc.is_contiguous(), where, "tensor-core scales must be contiguous")
+    for t, n in ((ga, "ga"), (gw, "gw")):
+        _kind(where, t, n, dtype="float32")
+    _kind(where, c, "c", dtype="float32")
+    M, N, K = a.shape[0], w.shape[0], a.shape[1] * 2
+    _require(w.shape[1] * 2 == K, where, "a and w must have the same K")
+    _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check(lib.nv_gemm_fp4_tc(M, N, K, _ptr(a), _ld(a), _ptr(sa_tc), sa_tc.numel(), _ptr(ga), _ptr(w), _ld(w),
+                              _ptr(sw_tc), sw_tc.numel(), _ptr(gw), _ptr(c), _ld(c), _stream(stream)), where)
     return c
 
 

@@ -15,22 +15,17 @@
 // steps through a 4-stage ring.
 //   warp 0      producer.  Lane 0 issues the TMA loads of the A and W data
 //               tiles (A 128 rows, W 256 rows, x 128 bytes, 128-byte swizzle)
-//               and of the stage's E8M0 bytes: a 16-byte box per row (the 16
-//               blocks of two stages; the box must start on a 16-byte column).
-//   warp 2      scale-layout warp during the main loop: rewrites the stage's
-//               8 scale bytes per row, in place, into the 128-row x 4-block
-//               chunk layout tcgen05.cp expects (byte 16*(r%32) + 4*(r/32) + kb
-//               of a 512-byte chunk).  Each lane reads exactly the rows whose
-//               bytes it then overwrites, so no lane waits on another.
-//   warp 1      TMEM allocator and MMA issuer: per stage, six tcgen05.cp
-//               32x128b.warpx4 (scale chunks -> TMEM) and four
-//               tcgen05.mma 128 x 256 x 64 with scale_vec::2X (one per K
-//               step; the A tile is read once per step), the scale byte pair
+//               and three bulk copies of the step's scale chunks (A's row
+//               group, W's two), all counted on the stage's one barrier.  The
+//               scales arrive already in the tensor cores' chunk layout
+//               (fp4_scales.cu), so the stage is ready for the MMA warp the
+//               moment it lands.
+//   warp 1      TMEM allocator and MMA issuer: per stage, six (MXFP4) or
+//               twelve (NVFP4) tcgen05.cp 32x128b.warpx4 (scale chunks ->
+//               TMEM) and four tcgen05.mma 128 x 256 x 64 (one per 64-element
+//               K slice; the A tile is read once per slice), the scale bytes
 //               chosen by the descriptor's scale-factor ids.
 //   warps 2-5   epilogue: tcgen05.ld and FP32 stores.
-// Scale arrays whose row stride is not a multiple of 16 bytes cannot be
-// described to TMA; for them the producer warp gathers the bytes with plain
-// loads and writes the chunk layout itself (slower, same result).
 #include "tc_common.cuh"
 #include "tma_host.h"
 #include "wq_internal.h"
@@ -43,9 +38,8 @@ constexpr int BKB = 128;                    // K bytes per stage (256 E2M1 eleme
 constexpr int kStages = 4;
 constexpr int kABytes = BM * BKB;           // 16 KB
 constexpr int kBBytes = BN * BKB;           // 32 KB
-constexpr int kSfChunk = 512;               // 128 rows x 4 scale bytes
-constexpr int kSfRowBytes = 16;             // scale bytes per row and TMA box
-constexpr int kSfBytes = (BM + BN) * kSfRowBytes;  // 6 KB: raw boxes, rewritten into chunks in place
+constexpr int kSfChunk = kTcSfChunk;        // 128 rows x 4 scale bytes
+constexpr int kSfBytes = 12 * kSfChunk;     // 6 KB: the step's scale chunks (NVFP4 12, MXFP4 6)
 constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // 54 KB (multiple of 1024)
 constexpr int kAccCols = BN;                // FP32 accumulator columns
 constexpr int kTmemCols = 512;              // accumulator + 4 stages of scale columns, rounded up
@@ -53,11 +47,11 @@ constexpr int kThreads = 192;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 
 // The two FP4 formats.  MXFP4: 32-element blocks with E8M0 scales, 8 scale
-// bytes per row per K step (the 16-byte scale box spans two steps), scales
-// in pairs per TMEM word (scale_vec::2X).  NVFP4: 16-element blocks with
-// E4M3 scales, 16 scale bytes per row per K step (one box per step), one
-// TMEM word of four scales per MMA (scale_vec::4X), and two FP32 tensor
-// scales applied in the epilogue.
+// bytes per row per K step (two chunks per row group), scales in pairs per
+// TMEM word (scale_vec::2X).  NVFP4: 16-element blocks with E4M3 scales, 16
+// scale bytes per row per K step (four chunks per row group), one TMEM word
+// of four scales per MMA (scale_vec::4X), and two FP32 tensor scales applied
+// in the epilogue.
 template <bool kNv>
 struct Fmt {
   static constexpr int kBlock = kNv ? 16 : 32;          // elements per scale
@@ -65,10 +59,9 @@ struct Fmt {
   static constexpr int kWords = kSfPerStep / 4;         // 4-byte chunk lines per row per K step
   static constexpr int kChunks = 3 * kWords;            // 512-byte chunks per K step (A, W 0-127, W 128-255)
   static constexpr int kSfCols = 4 * kChunks;           // TMEM columns per stage
-  // Scale bytes of rows or blocks outside the matrix (their data reads as
-  // zero, so any finite scale gives zero): 2^0 for E8M0, 0 for E4M3.
-  static constexpr uint32_t kFill = kNv ? 0u : 0x7F7F7F7Fu;
+  static constexpr uint32_t kPiece = kWords * kSfChunk;  // bytes of one row group's chunks per K step
 };
+static_assert(3 * Fmt<true>::kPiece <= kSfBytes && 3 * Fmt<false>::kPiece <= kSfBytes, "scale area");
 static_assert(kAccCols + kStages * Fmt<true>::kSfCols <= kTmemCols, "TMEM budget");
 static_assert(kAccCols + kStages * Fmt<false>::kSfCols <= kTmemCols, "TMEM budget");
 
@@ -92,81 +85,20 @@ int mx_splits(int M, int N, int K) {
 }
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
-// Gather 8 scale bytes (blocks kb0 .. kb0+7) of one row; rows or blocks
-// outside the matrix read as `fill` (a finite scale, so that zero-filled
-// data stays zero).
-__device__ __forceinline__ void load_sf8(const uint8_t* S, int64_t ld, int row, int rows, int kb0, int nkb,
-                                         bool aligned4, uint32_t fill, uint32_t& lo, uint32_t& hi) {
-  if (row < rows && kb0 + 8 <= nkb && aligned4) {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(S + static_cast<int64_t>(row) * ld + kb0);
-    lo = __ldg(p);
-    hi = __ldg(p + 1);
-    return;
-  }
-  uint32_t w[2] = {fill, fill};
-  if (row < rows) {
-    const uint8_t* p = S + static_cast<int64_t>(row) * ld;
-    for (int i = 0; i < 8; ++i)
-      if (kb0 + i < nkb) {
-        w[i >> 2] &= ~(0xFFu << (8 * (i & 3)));
-        w[i >> 2] |= static_cast<uint32_t>(__ldg(p + kb0 + i)) << (8 * (i & 3));
-      }
-  }
-  lo = w[0];
-  hi = w[1];
-}
-
-// Rewrite the stage's raw scale boxes (A: 128 rows, W: 256 rows, 16 bytes
-// each; the stage uses bytes off .. off + kSfPerStep - 1 of each row) into
-// 512-byte chunks at the start of the same area, group by group (A, W rows
-// 0-127, W rows 128-255) and 4-byte word by word: chunk grp * kWords + w,
-// line l = word w of rows l, l + 32, l + 64, l + 96 of the group (the layout
-// tcgen05.cp 32x128b.warpx4 copies into TMEM).  Lane l reads rows l + 32q of
-// each group and writes line l of each chunk, which lies in bytes it read.
+// The K step's scale chunks into the stage's scale area: kWords chunks (from
+// chunk kt * kWords) of A's row group m0 / 128, then of W's row groups
+// n0 / 128 and n0 / 128 + 1 (W's rows are padded to a multiple of 256, so
+// both exist).  This order is the one mma_step copies into TMEM.
 template <bool kNv>
-__device__ __forceinline__ void sf_to_chunks(uint8_t* sf, int off, int lane) {
-  constexpr int W = Fmt<kNv>::kWords;
-  uint32_t v[3][W][4];
-#pragma unroll
-  for (int grp = 0; grp < 3; ++grp)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint8_t* row = sf + (grp * 128 + lane + 32 * q) * kSfRowBytes + off;
-#pragma unroll
-      for (int w = 0; w < W; ++w) v[grp][w][q] = *reinterpret_cast<const uint32_t*>(row + 4 * w);
-    }
-#pragma unroll
-  for (int grp = 0; grp < 3; ++grp)
-#pragma unroll
-    for (int w = 0; w < W; ++w)
-      *reinterpret_cast<uint4*>(sf + (grp * W + w) * kSfChunk + 16 * lane) =
-          make_uint4(v[grp][w][0], v[grp][w][1], v[grp][w][2], v[grp][w][3]);
-}
-
-// Gather mode: the producer warp writes the same chunks from global memory.
-template <bool kNv>
-__device__ __forceinline__ void gather_sf_chunks(uint8_t* sf, const MxGemmArgs& p, int m0, int n0, int kt, int lane,
-                                                 bool a4, bool w4) {
-  constexpr int W = Fmt<kNv>::kWords;
-  const int nkb = p.K / Fmt<kNv>::kBlock;
-  const int kb0 = kt * Fmt<kNv>::kSfPerStep;
-#pragma unroll
-  for (int side = 0; side < 3; ++side) {
-    uint32_t v[W][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane + 32 * i;
-#pragma unroll
-      for (int h = 0; h < W / 2; ++h) {
-        if (side == 0) load_sf8(p.SA, p.ldsa, m0 + r, p.M, kb0 + 8 * h, nkb, a4, Fmt<kNv>::kFill, v[2 * h][i], v[2 * h + 1][i]);
-        else load_sf8(p.SW, p.ldsw, n0 + 128 * (side - 1) + r, p.N, kb0 + 8 * h, nkb, w4, Fmt<kNv>::kFill,
-                      v[2 * h][i], v[2 * h + 1][i]);
-      }
-    }
-#pragma unroll
-    for (int w = 0; w < W; ++w)
-      *reinterpret_cast<uint4*>(sf + (side * W + w) * kSfChunk + 16 * lane) = make_uint4(v[w][0], v[w][1], v[w][2], v[w][3]);
-  }
+__device__ __forceinline__ void load_sf_stage(uint8_t* sf, const MxGemmArgs& p, int m0, int n0, int kt,
+                                              uint64_t* bar) {
+  constexpr uint32_t kPiece = Fmt<kNv>::kPiece;
+  const int64_t chunks = tc_sf_chunks(kNv, p.K);
+  const int64_t c = static_cast<int64_t>(kt) * Fmt<kNv>::kWords;
+  tc::bulk_load(sf, p.SA + ((m0 / 128) * chunks + c) * kSfChunk, kPiece, bar);
+  const uint8_t* w = p.SW + ((n0 / 128) * chunks + c) * kSfChunk;
+  tc::bulk_load(sf + kPiece, w, kPiece, bar);
+  tc::bulk_load(sf + 2 * kPiece, w + chunks * kSfChunk, kPiece, bar);
 }
 
 // One K step on the tensor cores: copy the stage's scale chunks into its TMEM
@@ -238,17 +170,15 @@ __device__ __forceinline__ void warp_transpose32(uint32_t (&v)[32], int lane) {
   }
 }
 
-template <bool kNv, bool kSfTma>
+template <bool kNv>
 __global__ void __launch_bounds__(kThreads, 1)
-mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW, MxGemmArgs p,
+mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
                int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* sf_ready = empty + kStages;
-  uint64_t* accum = sf_ready + kStages;
+  uint64_t* accum = empty + kStages;
   uint64_t* drain = accum + 1;  // MMAs in flight after a give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -263,11 +193,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // TMA mode: the transaction bytes alone complete a stage.  Gather mode:
-      // the TMA arrival plus the producer warp's scale arrival.
-      tc::mbar_init(&full[s], kSfTma ? 1 : 2);
+      tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
-      tc::mbar_init(&sf_ready[s], 1);
     }
     tc::mbar_init(accum, 1);
     tc::mbar_init(drain, 1);
@@ -282,41 +209,26 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc::cta_barrier();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the scale re-layout: every read
+  // of the inputs and every write of C comes after this.
+  tc::griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmA);
       tc::tma_prefetch_desc(&tmW);
-      if (kSfTma) {
-        tc::tma_prefetch_desc(&tmSA);
-        tc::tma_prefetch_desc(&tmSW);
-      }
     }
-    const bool a4 = ((reinterpret_cast<uintptr_t>(p.SA) | static_cast<uintptr_t>(p.ldsa)) & 3) == 0;
-    const bool w4 = ((reinterpret_cast<uintptr_t>(p.SW) | static_cast<uintptr_t>(p.ldsw)) & 3) == 0;
     int issued = 0;
     for (int i = 0; i < KT; ++i) {
       const int kt = kt0 + i, s = i % kStages;
       const bool free_slot = tc::mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
       if (!__all_sync(0xffffffffu, free_slot)) break;  // warp-uniform exit
       uint8_t* st = smem + s * kStageBytes;
-      uint8_t* sf = st + kABytes + kBBytes;
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + (kSfTma ? kSfBytes : 0));
+        tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + 3 * Fmt<kNv>::kPiece);
         tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
         tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
-        if (kSfTma) {
-          // the 16-byte aligned column of the scale arrays that holds this step's bytes
-          const int x = (kt * Fmt<kNv>::kSfPerStep) & ~(kSfRowBytes - 1);
-          tc::tma_load_2d(sf, &tmSA, x, m0, &full[s]);
-          tc::tma_load_2d(sf + BM * kSfRowBytes, &tmSW, x, n0, &full[s]);
-        }
-      }
-      if (!kSfTma) {
-        gather_sf_chunks<kNv>(sf, p, m0, n0, kt, lane, a4, w4);
-        tc::fence_proxy_async_smem();  // scale bytes -> visible to tcgen05.cp
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full[s]);
+        load_sf_stage<kNv>(st + kABytes + kBBytes, p, m0, n0, kt, &full[s]);
       }
       issued = i + 1;
     }
@@ -327,8 +239,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1 && lane == 0) {
     for (int i = 0; i < KT; ++i) {
       const int s = i % kStages;
-      uint64_t* ready = kSfTma ? &sf_ready[s] : &full[s];
-      if (!tc::mbar_wait(ready, (i / kStages) & 1, abort, err, kSiteGemmMma)) break;
+      if (!tc::mbar_wait(&full[s], (i / kStages) & 1, abort, err, kSiteGemmMma)) break;
       tc::tc_fence_after();
       const uint32_t a = tc::smem_u32(smem + s * kStageBytes);
       const uint32_t b = a + kABytes;
@@ -345,19 +256,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc::mbar_wait_drain(drain, 0);
     }
   } else if (warp >= 2) {
-    if (kSfTma && warp == 2) {
-      // Scale-layout duty during the main loop.
-      for (int i = 0; i < KT; ++i) {
-        const int kt = kt0 + i, s = i % kStages;
-        const bool ok = tc::mbar_wait(&full[s], (i / kStages) & 1, abort, err, kSiteGemmMma);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        sf_to_chunks<kNv>(smem + s * kStageBytes + kABytes + kBBytes, (kt * Fmt<kNv>::kSfPerStep) & (kSfRowBytes - 1),
-                          lane);
-        tc::fence_proxy_async_smem();  // chunk bytes -> visible to tcgen05.cp
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sf_ready[s]);
-      }
-    }
     const float gs = tensor_scale<kNv>(p);
     const bool ok = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
@@ -474,12 +372,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // per thread, 32 rows per instruction, either held the accumulator for a
 // third of each tile or, done after the hand-back, flooded the SM's memory
 // path and starved the next tile's TMA loads.)
-//   warp 0      TMA producer (gather mode: also the scale-chunk writer)
+//   warp 0      TMA producer (data tiles and scale chunks)
 //   warp 1      TMEM allocator and MMA issuer
-//   warp 2      scale-layout warp (TMA mode)
-//   warps 3-10  epilogue: warp w reads TMEM lanes 32 (w % 4) .. (the lane
-//               quarter it may access) and columns 128 ((w - 3) / 4) ..
-constexpr int kPThreads = 352;
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. (the lane
+//               quarter it may access) and columns 128 ((w - 2) / 4) ..
+constexpr int kPThreads = 320;
 constexpr int kEpiWarps = 8;
 
 // Wait for an accumulator hand-off that is normally microseconds away: poll
@@ -502,17 +399,15 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
   }
 }
 
-template <bool kNv, bool kSfTma>
+template <bool kNv>
 __global__ void __launch_bounds__(kPThreads, 1)
-mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSW,
-                   MxGemmArgs p, int* err) {
+mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
+                   int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* sf_ready = empty + kStages;
-  uint64_t* acc_full = sf_ready + kStages;  // MMA -> epilogue
+  uint64_t* acc_full = empty + kStages;     // MMA -> epilogue
   uint64_t* acc_empty = acc_full + 1;       // epilogue warps -> MMA
   uint64_t* drain = acc_empty + 1;          // MMAs in flight after a give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -525,9 +420,8 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], kSfTma ? 1 : 2);
+      tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
-      tc::mbar_init(&sf_ready[s], 1);
     }
     tc::mbar_init(acc_full, 1);
     tc::mbar_init(acc_empty, kEpiWarps);
@@ -543,18 +437,15 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   tc::cta_barrier();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the scale re-layout: every read
+  // of the inputs and every write of C comes after this.
+  tc::griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmA);
       tc::tma_prefetch_desc(&tmW);
-      if (kSfTma) {
-        tc::tma_prefetch_desc(&tmSA);
-        tc::tma_prefetch_desc(&tmSW);
-      }
     }
-    const bool a4 = ((reinterpret_cast<uintptr_t>(p.SA) | static_cast<uintptr_t>(p.ldsa)) & 3) == 0;
-    const bool w4 = ((reinterpret_cast<uintptr_t>(p.SW) | static_cast<uintptr_t>(p.ldsw)) & 3) == 0;
     int it = 0, issued = 0;
     bool go = true;
     for (int t = blockIdx.x; t < tiles && go; t += gridDim.x) {
@@ -567,22 +458,11 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           break;
         }
         uint8_t* st = smem + s * kStageBytes;
-        uint8_t* sf = st + kABytes + kBBytes;
         if (lane == 0) {
-          tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + (kSfTma ? kSfBytes : 0));
+          tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + 3 * Fmt<kNv>::kPiece);
           tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
           tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
-          if (kSfTma) {
-            const int x = (kt * Fmt<kNv>::kSfPerStep) & ~(kSfRowBytes - 1);
-            tc::tma_load_2d(sf, &tmSA, x, m0, &full[s]);
-            tc::tma_load_2d(sf + BM * kSfRowBytes, &tmSW, x, n0, &full[s]);
-          }
-        }
-        if (!kSfTma) {
-          gather_sf_chunks<kNv>(sf, p, m0, n0, kt, lane, a4, w4);
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&full[s]);
+          load_sf_stage<kNv>(st + kABytes + kBBytes, p, m0, n0, kt, &full[s]);
         }
         issued = it + 1;
       }
@@ -599,8 +479,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       bool ok = true;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int s = it % kStages;
-        uint64_t* ready = kSfTma ? &sf_ready[s] : &full[s];
-        if (!tc::mbar_wait(ready, (it / kStages) & 1, abort, err, kSiteGemmMma)) {
+        if (!tc::mbar_wait(&full[s], (it / kStages) & 1, abort, err, kSiteGemmMma)) {
           ok = false;
           break;
         }
@@ -621,29 +500,9 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       tc::tc_commit(drain);
       tc::mbar_wait_drain(drain, 0);
     }
-  } else if (warp == 2) {
-    if (kSfTma) {
-      int it = 0;
-      bool go = true;
-      for (int t = blockIdx.x; t < tiles && go; t += gridDim.x) {
-        for (int kt = 0; kt < KT; ++kt, ++it) {
-          const int s = it % kStages;
-          const bool ok = tc::mbar_wait(&full[s], (it / kStages) & 1, abort, err, kSiteGemmMma);
-          if (!__all_sync(0xffffffffu, ok)) {
-            go = false;
-            break;
-          }
-          sf_to_chunks<kNv>(smem + s * kStageBytes + kABytes + kBBytes,
-                            (kt * Fmt<kNv>::kSfPerStep) & (kSfRowBytes - 1), lane);
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sf_ready[s]);
-        }
-      }
-    }
-  } else if (warp >= 3) {
+  } else if (warp >= 2) {
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int h = (warp - 3) >> 2;   // column half: 128 h .. 128 h + 127
+    const int h = (warp - 2) >> 2;   // column half: 128 h .. 128 h + 127
     const float gs = tensor_scale<kNv>(p);
     int local = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
@@ -699,47 +558,44 @@ template <bool kNv>
 cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
   if (a.K == 0)
     return cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
-  CUtensorMap tA, tW, tSA, tSW;
+  CUtensorMap tA, tW;
   cudaError_t e = make_tmap_2d(&tA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.lda, BKB, BM,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.N, a.ldw, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  // Scale arrays go through TMA when their rows start on 16-byte boundaries.
-  const bool sf_tma = ((reinterpret_cast<uintptr_t>(a.SA) | reinterpret_cast<uintptr_t>(a.SW) |
-                        static_cast<uintptr_t>(a.ldsa) | static_cast<uintptr_t>(a.ldsw)) & 15) == 0;
-  const uint64_t sf_cols = a.K / Fmt<kNv>::kBlock;
-  if (sf_tma) {
-    e = make_tmap_2d(&tSA, a.SA, CU_TENSOR_MAP_DATA_TYPE_UINT8, sf_cols, a.M, a.ldsa, kSfRowBytes, BM,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (e != cudaSuccess) return e;
-    e = make_tmap_2d(&tSW, a.SW, CU_TENSOR_MAP_DATA_TYPE_UINT8, sf_cols, a.N, a.ldsw, kSfRowBytes, BN,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (e != cudaSuccess) return e;
-  } else {
-    tSA = tA;  // unused by the gather variant
-    tSW = tW;
-  }
   const int splits = mx_splits(a.M, a.N, a.K);
+  // Both kernels start as programmatic dependents of the launch before them
+  // (normally the scale re-layout) and wait for it before touching memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(splits == 1 ? kPThreads : kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (splits == 1) {  // persistent: one CTA per SM
-    auto pk = sf_tma ? mx_gemm_persistent<kNv, true> : mx_gemm_persistent<kNv, false>;
-    static PerDevice<bool> pconfigured[2];
+    auto pk = mx_gemm_persistent<kNv>;
+    static PerDevice<bool> pconfigured;
     bool pdone = false;
-    if (!pconfigured[sf_tma].get(pdone, [&](bool& v) {
+    if (!pconfigured.get(pdone, [&](bool& v) {
           e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
           v = true;
           return e == cudaSuccess;
         }))
       return e;
     const int tiles = ((a.N + BN - 1) / BN) * ((a.M + BM - 1) / BM);
-    const int grid = tiles < sm_count() ? tiles : sm_count();
-    pk<<<grid, kPThreads, kSmemBytes, s>>>(tA, tW, tSA, tSW, a, device_error_word());
+    cfg.gridDim = dim3(tiles < sm_count() ? tiles : sm_count());
+    e = cudaLaunchKernelEx(&cfg, pk, tA, tW, a, device_error_word());
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  auto kern = sf_tma ? mx_gemm_kernel<kNv, true> : mx_gemm_kernel<kNv, false>;
-  static PerDevice<bool> configured[2];
+  auto kern = mx_gemm_kernel<kNv>;
+  static PerDevice<bool> configured;
   bool done = false;
-  if (!configured[sf_tma].get(done, [&](bool& v) {
+  if (!configured.get(done, [&](bool& v) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         v = true;
         return e == cudaSuccess;
@@ -747,19 +603,13 @@ cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
     return e;
   // Split K: each tile's splits form a thread-block cluster (along z) that
   // adds its partial tiles in distributed shared memory.
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, tA, tW, tSA, tSW, a, device_error_word());
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = splits;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, tA, tW, a, device_error_word());
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

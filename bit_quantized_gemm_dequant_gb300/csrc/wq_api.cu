@@ -214,20 +214,89 @@ int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_
   return launch_status(launch_mx_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// FP4 GEMMs.  The kernels read block scales in the tensor-core layout
+// (tc_sf_chunks); the row-major entry points first rearrange both operands'
+// scales into the caller's workspace.
+static size_t fp4_ws_a_bytes(bool nv, int M, int K) { return (tc_sf_bytes(nv, M, K) + 255) & ~size_t(255); }
+
+static int check_fp4_gemm(bool nv, int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* W, int64_t ldw,
+                          const float* C, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0 || K % (nv ? 16 : 32)) return WQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQ_OK;
+  if (!C || (K > 0 && (!A || !W))) return WQ_ERR_INVALID_ARG;
+  if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2))) return WQ_ERR_INVALID_ARG;
+  if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(A, 16) || !aligned(W, 16) || lda % 16 || ldw % 16)) return WQ_ERR_MISALIGNED;
+  if (M > kMaxTiledM || N > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
+  return WQ_OK;
+}
+
+// Row-major scales -> workspace in the tensor-core layout, then the GEMM.
+static int fp4_gemm_rowmajor(bool nv, MxGemmArgs a, const uint8_t* SA, int64_t ldsa, const uint8_t* SW, int64_t ldsw,
+                             void* workspace, size_t ws_bytes, cudaStream_t s) {
+  const int st = check_fp4_gemm(nv, a.M, a.N, a.K, a.A, a.lda, a.W, a.ldw, a.C, a.ldc);
+  if (st != WQ_OK || a.M == 0 || a.N == 0) return st;
+  if (a.K > 0) {
+    if (!SA || !SW) return WQ_ERR_INVALID_ARG;
+    const int nb = a.K / (nv ? 16 : 32);
+    if (ldsa < nb || ldsw < nb) return WQ_ERR_INVALID_ARG;
+    if (ws_bytes < wq_workspace_size(nv ? WQ_OP_NV_GEMM : WQ_OP_MX_GEMM, a.M, a.N, a.K) || !workspace ||
+        !aligned(workspace, 256))
+      return WQ_ERR_WORKSPACE;
+    uint8_t* sa_tc = static_cast<uint8_t*>(workspace);
+    uint8_t* sw_tc = sa_tc + fp4_ws_a_bytes(nv, a.M, a.K);
+    cudaError_t e = launch_fp4_scales_tc(nv, a.M, a.K, SA, ldsa, sa_tc, s);
+    if (e == cudaSuccess) e = launch_fp4_scales_tc(nv, a.N, a.K, SW, ldsw, sw_tc, s);
+    if (e != cudaSuccess) return launch_status(e);
+    a.SA = sa_tc;
+    a.SW = sw_tc;
+  }
+  return launch_status(nv ? launch_nv_gemm(a, s) : launch_mx_gemm(a, s));
+}
+
+// Scales already in the tensor-core layout.
+static int fp4_gemm_tc(bool nv, const MxGemmArgs& a, size_t sa_bytes, size_t sw_bytes, cudaStream_t s) {
+  const int st = check_fp4_gemm(nv, a.M, a.N, a.K, a.A, a.lda, a.W, a.ldw, a.C, a.ldc);
+  if (st != WQ_OK || a.M == 0 || a.N == 0) return st;
+  if (a.K > 0) {
+    if (!a.SA || !a.SW) return WQ_ERR_INVALID_ARG;
+    if (sa_bytes < tc_sf_bytes(nv, a.M, a.K) || sw_bytes < tc_sf_bytes(nv, a.N, a.K)) return WQ_ERR_INVALID_ARG;
+    if (!aligned(a.SA, 16) || !aligned(a.SW, 16)) return WQ_ERR_MISALIGNED;
+  }
+  return launch_status(nv ? launch_nv_gemm(a, s) : launch_mx_gemm(a, s));
+}
+
 int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* SA, int64_t ldsa,
                 const uint8_t* W, int64_t ldw, const uint8_t* SW, int64_t ldsw, float* C, int64_t ldc,
                 void* workspace, size_t ws_bytes, wq_stream_t stream) {
-  (void)workspace;
-  if (M < 0 || N < 0 || K < 0 || K % 32) return WQ_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return WQ_OK;
-  if (!C || (K > 0 && (!A || !SA || !W || !SW))) return WQ_ERR_INVALID_ARG;
-  if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2 || ldsa < K / 32 || ldsw < K / 32))) return WQ_ERR_INVALID_ARG;
-  if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
-  if (K > 0 && (!aligned(A, 16) || !aligned(W, 16) || lda % 16 || ldw % 16)) return WQ_ERR_MISALIGNED;
-  if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
-  if (ws_bytes < wq_workspace_size(WQ_OP_MX_GEMM, M, N, K)) return WQ_ERR_WORKSPACE;
-  MxGemmArgs a{M, N, K, A, lda, SA, ldsa, W, ldw, SW, ldsw, C, ldc};
-  return launch_status(launch_mx_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+  MxGemmArgs a{M, N, K, A, lda, nullptr, W, ldw, nullptr, C, ldc};
+  return fp4_gemm_rowmajor(false, a, SA, ldsa, SW, ldsw, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm_fp4_tc(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* SA, size_t sa_bytes,
+                   const uint8_t* W, int64_t ldw, const uint8_t* SW, size_t sw_bytes, float* C, int64_t ldc,
+                   wq_stream_t stream) {
+  MxGemmArgs a{M, N, K, A, lda, SA, W, ldw, SW, C, ldc};
+  return fp4_gemm_tc(false, a, sa_bytes, sw_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fp4_scales_tc_size(int format, int rows, int K) {
+  if ((format != WQ_FP4_MX && format != WQ_FP4_NV) || rows <= 0 || K <= 0) return 0;
+  if (K % (format == WQ_FP4_NV ? 16 : 32)) return 0;
+  return tc_sf_bytes(format == WQ_FP4_NV, rows, K);
+}
+
+int fp4_scales_tc(int format, int rows, int K, const uint8_t* S, int64_t lds, uint8_t* out, size_t out_bytes,
+                  wq_stream_t stream) {
+  if (format != WQ_FP4_MX && format != WQ_FP4_NV) return WQ_ERR_INVALID_ARG;
+  const bool nv = format == WQ_FP4_NV;
+  if (rows < 0 || K < 0 || K % (nv ? 16 : 32)) return WQ_ERR_INVALID_ARG;
+  if (rows == 0 || K == 0) return WQ_OK;
+  if (!S || !out || lds < K / (nv ? 16 : 32)) return WQ_ERR_INVALID_ARG;
+  if (out_bytes < tc_sf_bytes(nv, rows, K)) return WQ_ERR_INVALID_ARG;
+  if (!aligned(out, 16)) return WQ_ERR_MISALIGNED;
+  if (rows > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
+  return launch_status(launch_fp4_scales_tc(nv, rows, K, S, lds, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int nv_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_t* data, int64_t ld_data,
@@ -244,22 +313,33 @@ int nv_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src, uint8_
   return launch_status(launch_nv_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int check_nv_scales(int M, int N, int K, const float* scale_a, const float* scale_w) {
+  if (M <= 0 || N <= 0 || K <= 0) return WQ_OK;
+  if (!scale_a || !scale_w) return WQ_ERR_INVALID_ARG;
+  if (!aligned(scale_a, 4) || !aligned(scale_w, 4)) return WQ_ERR_MISALIGNED;
+  return WQ_OK;
+}
+
 int nv_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* SA, int64_t ldsa,
                 const float* scale_a, const uint8_t* W, int64_t ldw, const uint8_t* SW, int64_t ldsw,
                 const float* scale_w, float* C, int64_t ldc, void* workspace, size_t ws_bytes, wq_stream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
-  if (M < 0 || N < 0 || K < 0 || K % 16) return WQ_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return WQ_OK;
-  if (!C || (K > 0 && (!A || !SA || !W || !SW || !scale_a || !scale_w))) return WQ_ERR_INVALID_ARG;
-  if (ldc < N || (K > 0 && (lda < K / 2 || ldw < K / 2 || ldsa < K / 16 || ldsw < K / 16))) return WQ_ERR_INVALID_ARG;
-  if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
-  if (K > 0 && (!aligned(A, 16) || !aligned(W, 16) || lda % 16 || ldw % 16 || !aligned(scale_a, 4) ||
-                !aligned(scale_w, 4)))
-    return WQ_ERR_MISALIGNED;
-  if (M > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
-  MxGemmArgs a{M, N, K, A, lda, SA, ldsa, W, ldw, SW, ldsw, C, ldc, scale_a, scale_w};
-  return launch_status(launch_nv_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+  const int st = check_fp4_gemm(true, M, N, K, A, lda, W, ldw, C, ldc);
+  if (st != WQ_OK) return st;
+  const int sg = check_nv_scales(M, N, K, scale_a, scale_w);
+  if (sg != WQ_OK) return sg;
+  MxGemmArgs a{M, N, K, A, lda, nullptr, W, ldw, nullptr, C, ldc, scale_a, scale_w};
+  return fp4_gemm_rowmajor(true, a, SA, ldsa, SW, ldsw, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nv_gemm_fp4_tc(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* SA, size_t sa_bytes,
+                   const float* scale_a, const uint8_t* W, int64_t ldw, const uint8_t* SW, size_t sw_bytes,
+                   const float* scale_w, float* C, int64_t ldc, wq_stream_t stream) {
+  const int st = check_fp4_gemm(true, M, N, K, A, lda, W, ldw, C, ldc);
+  if (st != WQ_OK) return st;
+  const int sg = check_nv_scales(M, N, K, scale_a, scale_w);
+  if (sg != WQ_OK) return sg;
+  MxGemmArgs a{M, N, K, A, lda, SA, W, ldw, SW, C, ldc, scale_a, scale_w};
+  return fp4_gemm_tc(true, a, sa_bytes, sw_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8_gemm(int M, int N, int K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb, float scale_a,
@@ -303,6 +383,10 @@ size_t wq_workspace_size(int op, int M, int N, int K) {
   if (op == WQ_OP_W4A16 && K % 2 == 0) return weight_only_workspace(4, M, N, K);
   if (op == WQ_OP_W8A16 && K % 2 == 0) return weight_only_workspace(8, M, N, K);
   if (op == WQ_OP_FP8_GEMM && M <= kFp8SkinnyMaxM) return plan_skinny(M, N, K, 9).ws_bytes;
+  if ((op == WQ_OP_MX_GEMM && K % 32 == 0) || (op == WQ_OP_NV_GEMM && K % 16 == 0)) {
+    const bool nv = op == WQ_OP_NV_GEMM;
+    return fp4_ws_a_bytes(nv, M, K) + tc_sf_bytes(nv, N, K);
+  }
   return 0;
 }
 

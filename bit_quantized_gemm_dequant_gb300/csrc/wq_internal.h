@@ -86,12 +86,26 @@ struct MxQuantArgs {
   uint8_t* scales; int64_t ld_scales;
 };
 
+// Block scales of the FP4 GEMMs in the tensor cores' layout.  Rows are padded
+// to a multiple of 256 and K to a multiple of 256 elements.  Row group g (rows
+// 128 g .. 128 g + 127) holds tc_sf_chunks(nv, K) chunks of 512 bytes; chunk c
+// holds the scales of blocks 4 c .. 4 c + 3 of the group's rows, the scale of
+// row r and block b at byte 16 (r % 32) + 4 ((r / 32) % 4) + b % 4: the order
+// in which tcgen05.cp 32x128b.warpx4 copies a chunk into four TMEM columns.
+// Chunk (g, c) starts at byte 512 (g tc_sf_chunks + c).  Padding holds a
+// finite scale (2^0 for E8M0, 0 for E4M3), so zero-filled data stays zero.
+constexpr int kTcSfChunk = 512;
+__host__ __device__ inline int tc_sf_chunks(bool nv, int K) { return ((K + 255) / 256) * (nv ? 4 : 2); }
+inline size_t tc_sf_bytes(bool nv, int rows, int K) {
+  return static_cast<size_t>((rows + 255) / 256) * 2 * tc_sf_chunks(nv, K) * kTcSfChunk;
+}
+
 struct MxGemmArgs {  // MXFP4 and NVFP4 GEMMs
   int M, N, K;
   const uint8_t* A; int64_t lda;
-  const uint8_t* SA; int64_t ldsa;
+  const uint8_t* SA;  // A's block scales, tensor-core layout
   const uint8_t* W; int64_t ldw;
-  const uint8_t* SW; int64_t ldsw;
+  const uint8_t* SW;  // W's block scales, tensor-core layout
   float* C; int64_t ldc;
   const float* ga = nullptr;  // NVFP4: the tensor scales of A and W (device memory)
   const float* gw = nullptr;
@@ -137,6 +151,10 @@ cudaError_t launch_wo_skinny(const WoArgs& a, int bits, const SkinnyPlan& pl, cu
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s);
 cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s);
+// Row-major block scales S [rows, K / block] (row stride lds bytes) -> the
+// tensor-core layout above, tc_sf_bytes(nv, rows, K) bytes at out.
+cudaError_t launch_fp4_scales_tc(bool nv, int rows, int K, const uint8_t* S, int64_t lds, uint8_t* out,
+                                 cudaStream_t s);
 cudaError_t launch_nv_gemm(const MxGemmArgs& a, cudaStream_t s);
 cudaError_t launch_nv_quantize(const NvQuantArgs& a, cudaStream_t s);
 cudaError_t launch_fp8_gemm(const Fp8GemmArgs& a, cudaStream_t s);

@@ -64,6 +64,7 @@ typedef struct CUstream_st* wq_stream_t;
 #define WQ_OP_MX_QUANTIZE 2
 #define WQ_OP_MX_GEMM 3
 #define WQ_OP_FP8_GEMM 4
+#define WQ_OP_NV_GEMM 5
 
 /*
  * wq_gemm_w4a16 — Y = X * ((q - 8) * s), INT4 weights dequantized on chip.
@@ -284,9 +285,12 @@ int mx_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
  *   W, SW    the same for W [N, K] (row strides ldw, ldsw).
  *   C        fp32 [M, N] output, row stride ldc (elements).
  *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_MX_GEMM, M, N, K)
- *            (currently 0 for every shape).
+ *            bytes, 256-byte aligned: the call first rewrites both scale
+ *            arrays there in the tensor-core layout (fp4_scales_tc), then
+ *            runs mx_gemm_fp4_tc.  Too small or NULL (K > 0):
+ *            WQ_ERR_WORKSPACE.  Two calls in flight must not share it.
  * Alignment: A, W 16-byte aligned with lda, ldw multiples of 16; C 16-byte
- * aligned with ldc a multiple of 4.
+ * aligned with ldc a multiple of 4.  M and N at most 65535 * 128.
  * When the output tiles are too few to fill the GPU (small M), K is split
  * across the CTAs of a thread-block cluster, which add their FP32 partial
  * tiles in distributed shared memory in a fixed order.  Every shape writes C
@@ -297,6 +301,53 @@ int mx_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
                 int64_t ldw, const uint8_t* SW, int64_t ldsw, float* C,
                 int64_t ldc, void* workspace, size_t ws_bytes,
                 wq_stream_t stream);
+
+/*
+ * fp4_scales_tc — rearrange FP4 block scales into the tensor-core layout
+ * that mx_gemm_fp4_tc and nv_gemm_fp4_tc read.
+ *
+ * The block-scaled tensor cores ([MXFP4] §二.1-§二.2: the block exponents
+ * enter the dot product in hardware) read scales from tensor memory, copied
+ * there in 512-byte chunks of 128 rows x 4 blocks.  This call writes the
+ * scales in that order once, so that a GEMM moves them with plain bulk
+ * copies.  For weights, do it once when the weights are loaded.
+ *
+ *   format   WQ_FP4_MX (E8M0 scales of 32-element blocks, K % 32 == 0) or
+ *            WQ_FP4_NV (E4M3 scales of 16-element blocks, K % 16 == 0).
+ *   rows, K  the operand's rows and K in elements (the scale array is
+ *            [rows, K / block]).
+ *   S        uint8 [rows, K / block] scales, row stride lds bytes (any
+ *            alignment), as mx_quantize_fp4 / nv_quantize_fp4 write them.
+ *   out      device buffer of at least fp4_scales_tc_size(format, rows, K)
+ *            bytes (out_bytes), 16-byte aligned.
+ * Layout of out: rows padded to a multiple of 256 and K to a multiple of
+ * 256 elements; row group g = rows 128 g .. 128 g + 127 holds
+ * Kc = (K_padded / 256) * (2 for MX, 4 for NV) chunks of 512 bytes; chunk
+ * c of group g starts at byte 512 (g Kc + c) and holds blocks 4 c .. 4 c + 3
+ * of the group's rows, the scale of row r, block b at byte
+ * 16 (r % 32) + 4 ((r / 32) % 4) + b % 4.  Padding holds 0x7F (2^0) for
+ * MX and 0x00 for NV.
+ */
+#define WQ_FP4_MX 0
+#define WQ_FP4_NV 1
+size_t fp4_scales_tc_size(int format, int rows, int K);
+int fp4_scales_tc(int format, int rows, int K, const uint8_t* S, int64_t lds,
+                  uint8_t* out, size_t out_bytes, wq_stream_t stream);
+
+/*
+ * mx_gemm_fp4_tc — mx_gemm_fp4 with both scale arrays already in the
+ * tensor-core layout (fp4_scales_tc): no workspace, one kernel launch.
+ *
+ *   SA, sa_bytes  A's scales from fp4_scales_tc(WQ_FP4_MX, M, K, ...) and
+ *                 that buffer's size; SW, sw_bytes the same for W (N rows).
+ *                 A buffer smaller than fp4_scales_tc_size: WQ_ERR_INVALID_ARG.
+ *   Every other argument, the result and the alignment rules are those of
+ *   mx_gemm_fp4; SA and SW must be 16-byte aligned.
+ */
+int mx_gemm_fp4_tc(int M, int N, int K, const uint8_t* A, int64_t lda,
+                   const uint8_t* SA, size_t sa_bytes, const uint8_t* W,
+                   int64_t ldw, const uint8_t* SW, size_t sw_bytes, float* C,
+                   int64_t ldc, wq_stream_t stream);
 
 /*
  * nv_quantize_fp4 — quantize FP32 rows to NVFP4: E2M1 elements in 16-element
@@ -344,7 +395,9 @@ int nv_quantize_fp4(int rows, int cols, const float* src, int64_t ld_src,
  *   scale_a   device pointer to A's tensor scale gA (from nv_quantize_fp4).
  *   W, SW, scale_w  the same for W [N, K].
  *   C         fp32 [M, N] output, row stride ldc (elements).
- *   workspace, ws_bytes  unused (0 bytes needed).
+ *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_NV_GEMM, M, N, K)
+ *             bytes, 256-byte aligned, used as in mx_gemm_fp4 (the scales
+ *             are rewritten there, then nv_gemm_fp4_tc runs).
  * Alignment: as for mx_gemm_fp4, plus scale_a and scale_w 4-byte aligned.
  * Small M splits K across a cluster of CTAs as mx_gemm_fp4 does; the result
  * is deterministic.
@@ -354,6 +407,18 @@ int nv_gemm_fp4(int M, int N, int K, const uint8_t* A, int64_t lda,
                 const uint8_t* W, int64_t ldw, const uint8_t* SW,
                 int64_t ldsw, const float* scale_w, float* C, int64_t ldc,
                 void* workspace, size_t ws_bytes, wq_stream_t stream);
+
+/*
+ * nv_gemm_fp4_tc — nv_gemm_fp4 with both E4M3 scale arrays already in the
+ * tensor-core layout (fp4_scales_tc with WQ_FP4_NV): no workspace.
+ * SA/sa_bytes and SW/sw_bytes as for mx_gemm_fp4_tc; everything else as for
+ * nv_gemm_fp4.
+ */
+int nv_gemm_fp4_tc(int M, int N, int K, const uint8_t* A, int64_t lda,
+                   const uint8_t* SA, size_t sa_bytes, const float* scale_a,
+                   const uint8_t* W, int64_t ldw, const uint8_t* SW,
+                   size_t sw_bytes, const float* scale_w, float* C,
+                   int64_t ldc, wq_stream_t stream);
 
 /*
  * fp8_gemm — C = bf16((A * B) * scale_a * scale_b) for e4m3 operands.

@@ -417,6 +417,42 @@ def nv_gemm_fp4(a_data, a_scales, ga, w_data, w_scales, gw, rows=None) -> np.nda
 
 
 # --------------------------------------------------------------------------
+# Block scales in the tensor cores' order.  This is not arithmetic of the
+# pages: the block-scaled tensor cores (MXFP4 page §二.1-§二.2, the exponents
+# added inside the dot product) take their scales in 512-byte chunks of 128
+# rows x 4 blocks, and the CUDA library's GEMMs read scales stored in that
+# order.  The library documents the layout with its re-layout call; this is a
+# plain restatement of that definition, element by element, against which
+# the call is checked byte for byte.
+# --------------------------------------------------------------------------
+
+TC_CHUNK = 512
+
+
+def fp4_scales_tc(scales: np.ndarray, K: int, block: int) -> np.ndarray:
+    """Row-major block scales uint8 ``[rows, K / block]`` (block 32: E8M0,
+    block 16: E4M3) -> the flat tensor-core layout.
+
+    Rows pad to a multiple of 256 and K to a multiple of 256 elements.  Row
+    group g (rows 128 g .. 128 g + 127) holds ``kc`` chunks of 512 bytes,
+    kc = (padded K / 256) * (256 / block / 4); chunk c of group g starts at
+    byte 512 (g kc + c) and holds blocks 4 c .. 4 c + 3; the scale of row r,
+    block b sits at byte 16 (r % 32) + 4 ((r // 32) % 4) + b % 4 of its chunk.
+    Padding is 0x7F (2^0) for E8M0 and 0x00 for E4M3."""
+    rows, nb = scales.shape
+    assert K % block == 0 and nb == K // block
+    steps = -(-K // 256)
+    kc = steps * (256 // block) // 4
+    groups = 2 * (-(-rows // 256))
+    out = np.full(groups * kc * TC_CHUNK, 0x7F if block == 32 else 0x00, dtype=np.uint8)
+    r = np.arange(rows)[:, None]
+    b = np.arange(nb)[None, :]
+    offset = ((r // 128) * kc + b // 4) * TC_CHUNK + 16 * (r % 32) + 4 * ((r // 32) % 4) + b % 4
+    out[offset] = scales
+    return out
+
+
+# --------------------------------------------------------------------------
 # Output rounding and the comparison rule
 # --------------------------------------------------------------------------
 

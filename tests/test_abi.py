@@ -97,6 +97,36 @@ def test_mx_and_fp8_validation(wq):
     assert L.fp8_gemm(0, 8, 32, 0, 32, 0, 16, ctypes.c_float(1), ctypes.c_float(1), 0, 8, None, 0, None) == wq.WQ_OK
 
 
+def test_fp4_tensor_core_scale_validation(wq):
+    """Sizes of the tensor-core scale layout (worked by hand: MXFP4 300 rows,
+    K 1024 -> 4 row groups x 8 chunks x 512 bytes; 520 rows -> 6 groups), and
+    argument checks that return before any CUDA call."""
+    L = wq.lib
+    MX, NV = wq.WQ_FP4_MX, wq.WQ_FP4_NV
+    assert L.fp4_scales_tc_size(MX, 300, 1024) == 4 * 8 * 512
+    assert L.fp4_scales_tc_size(MX, 520, 1024) == 6 * 8 * 512
+    assert L.fp4_scales_tc_size(NV, 5, 80) == 2 * 4 * 512
+    assert L.fp4_scales_tc_size(MX, 8, 48) == 0 and L.fp4_scales_tc_size(2, 8, 64) == 0
+    # the row-major GEMMs' workspace: A's part rounded up to 256 bytes, then W's
+    assert L.wq_workspace_size(wq.WQ_OP_MX_GEMM, 300, 520, 1024) == 4 * 8 * 512 + 6 * 8 * 512
+    assert L.wq_workspace_size(wq.WQ_OP_NV_GEMM, 300, 520, 1024) == 4 * 16 * 512 + 6 * 16 * 512
+    assert L.fp4_scales_tc(2, 8, 64, FAKE, 2, FAKE, 1 << 20, None) == wq.WQ_ERR_INVALID_ARG       # format
+    assert L.fp4_scales_tc(MX, 8, 48, FAKE, 2, FAKE, 1 << 20, None) == wq.WQ_ERR_INVALID_ARG      # K % 32
+    assert L.fp4_scales_tc(MX, 8, 64, FAKE, 1, FAKE, 1 << 20, None) == wq.WQ_ERR_INVALID_ARG      # lds < K / 32
+    assert L.fp4_scales_tc(MX, 8, 64, FAKE, 2, FAKE, 100, None) == wq.WQ_ERR_INVALID_ARG          # out too small
+    assert L.fp4_scales_tc(MX, 8, 64, FAKE, 2, FAKE + 8, 1 << 20, None) == wq.WQ_ERR_MISALIGNED
+    assert L.fp4_scales_tc(MX, 0, 64, 0, 2, 0, 0, None) == wq.WQ_OK
+    # a scale buffer smaller than the layout of its operand
+    assert L.mx_gemm_fp4_tc(8, 8, 64, FAKE, 32, FAKE, 100, FAKE, 32, FAKE, 1 << 20, FAKE, 8, None) \
+        == wq.WQ_ERR_INVALID_ARG
+    assert L.nv_gemm_fp4_tc(8, 8, 64, FAKE, 32, FAKE, 1 << 20, FAKE, FAKE, 32, FAKE, 100, FAKE, FAKE, 8, None) \
+        == wq.WQ_ERR_INVALID_ARG
+    # row-major scales need the workspace
+    assert L.mx_gemm_fp4(8, 8, 64, FAKE, 32, FAKE, 2, FAKE, 32, FAKE, 2, FAKE, 8, None, 0, None) == wq.WQ_ERR_WORKSPACE
+    assert L.nv_gemm_fp4(8, 8, 64, FAKE, 32, FAKE, 4, FAKE, FAKE, 32, FAKE, 4, FAKE, FAKE, 8, None, 0, None) \
+        == wq.WQ_ERR_WORKSPACE
+
+
 def test_problem_struct_matches_header(wq, tmp_path):
     """The binding's wq_problem has the C layout of include/wq.h (checked with
     the host C compiler)."""
@@ -246,9 +276,18 @@ def test_binding_functions_marshal_without_cuda(wq, monkeypatch):
     assert c.shape == (4, 8) and c.dtype == torch.float32
     c8 = wq.fp8_gemm(torch.zeros((4, 64), dtype=torch.uint8), torch.zeros((64, 16), dtype=torch.uint8), 1.0, 2.0)
     assert c8.shape == (4, 16) and c8.dtype == torch.bfloat16
+    sa_tc = wq.fp4_scales_tc(e, 64)
+    ct = wq.mx_gemm_fp4_tc(d, sa_tc, torch.zeros((8, 32), dtype=torch.uint8), sa_tc)
+    assert ct.shape == (4, 8) and ct.dtype == torch.float32
+    g1 = torch.ones(1, dtype=torch.float32)
+    e16 = torch.zeros((4, 4), dtype=torch.uint8)
+    cn = wq.nv_gemm_fp4(d, e16, g1, torch.zeros((8, 32), dtype=torch.uint8), torch.zeros((8, 4), dtype=torch.uint8), g1)
+    cnt = wq.nv_gemm_fp4_tc(d, sa_tc, g1, torch.zeros((8, 32), dtype=torch.uint8), sa_tc, g1)
+    assert cn.shape == cnt.shape == (4, 8)
     names = [n for n, _ in fake.calls]
     assert names == ["wq_gemm_w4a16", "wq_gemm_w8a16", "wq_gemm_w8a16_noalloc", "wq_gemm_w4a16_grouped",
-                     "wq_gemm_w8a16_grouped", "mx_quantize_fp4", "mx_gemm_fp4", "fp8_gemm"]
+                     "wq_gemm_w8a16_grouped", "mx_quantize_fp4", "mx_gemm_fp4", "fp8_gemm",
+                     "fp4_scales_tc_size", "fp4_scales_tc", "mx_gemm_fp4_tc", "nv_gemm_fp4", "nv_gemm_fp4_tc"]
     argc = {n: len(a) for n, a in fake.calls}
     for n, sig in wq._SIGS.items():
         if n in argc:

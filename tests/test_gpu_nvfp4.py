@@ -138,11 +138,11 @@ def test_gemm_per_row_and_per_block_scales(wq):
 @pytest.mark.parametrize("M,N,K,lda,ldsa,ldw,ldsw,ldc", [
     (128, 256, 256, None, None, None, None, None),
     (1, 16, 16, 16, None, 16, None, None),            # one scale block
-    (200, 300, 800, 400, 50, 400, 51, 304),           # ragged M/N/K, odd scale stride (gather path)
+    (200, 300, 800, 400, 50, 400, 51, 304),           # ragged M/N/K, odd scale stride (byte loads in the re-layout)
     (130, 256, 8192, None, None, None, None, None),
     (384, 128, 4096, 2064, 272, 2048, 256, 132),
-    (300, 520, 1040, 528, None, 528, None, None),     # K not a multiple of 256: partial last step (gather)
-    (64, 256, 1040, 528, 80, 528, 80, None),          # partial last step through the TMA scale path
+    (300, 520, 1040, 528, None, 528, None, None),     # K not a multiple of 256: partial last step
+    (64, 256, 1040, 528, 80, 528, 80, None),          # partial last step, 16-byte scale rows
 ])
 def test_gemm_random_quantized(wq, M, N, K, lda, ldsa, ldw, ldsw, ldc):
     a = workloads.mx_source(M, K, seed=M + K, stream=0)

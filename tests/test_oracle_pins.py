@@ -845,3 +845,53 @@ def test_pins_catch_planted_mistakes(mutant, checks):
     for check in checks:
         with pytest.raises(AssertionError):
             check(mutant)
+
+
+# ---------------------------------------------------------------- tensor-core scale layout
+# Offsets worked by hand from the layout's definition (row group g = r // 128,
+# chunk c = b // 4, kc chunks per group):
+#   offset = 512 (g kc + c) + 16 (r % 32) + 4 ((r // 32) % 4) + b % 4.
+# MXFP4, rows 300, K 512: 16 blocks per row, K pads to 512 = 2 steps of 256,
+# kc = 2 * 8 / 4 = 4 chunks per group; rows pad to 512, 4 groups, 8192 bytes.
+_TC_MX_CASES = [
+    (0, 0, 0),
+    (33, 5, 512 + 16 + 4 + 1),                     # g 0, c 1, line 1, word 1, byte 1
+    (200, 9, (1 * 4 + 2) * 512 + 16 * 8 + 4 * 2 + 1),  # g 1, c 2, line 8, word 2 (200 // 32 = 6), byte 1 = 3209
+    (299, 15, (2 * 4 + 3) * 512 + 16 * 11 + 4 * 1 + 3),  # g 2, c 3, line 11, word 1 (299 // 32 = 9), byte 3 = 5815
+]
+
+
+def _tc_scales(rows, nb, lo, hi, seed):
+    return np.random.default_rng(seed).integers(lo, hi, size=(rows, nb), dtype=np.uint8)
+
+
+def test_fp4_scales_tc_worked_offsets():
+    s = _tc_scales(300, 16, 1, 127, 11)
+    out = O.fp4_scales_tc(s, 512, 32)
+    assert out.shape == (8192,)
+    for r, b, off in _TC_MX_CASES:
+        assert off in (0, 533, 3209, 5815)
+        assert out[off] == s[r, b], (r, b, off)
+    # padding: row 300 (g 2, line 12, word 1, block 0) and all of group 3 hold 2^0
+    assert out[(2 * 4) * 512 + 16 * 12 + 4 * 1] == 0x7F
+    assert np.all(out[3 * 4 * 512:] == 0x7F)
+    # NVFP4, rows 5, K 80: 5 blocks, K pads to 256 = one step of 16 blocks,
+    # kc = 4; rows pad to 256, 2 groups, 4096 bytes.  Row 4, block 4: chunk 1,
+    # line 4, word 0, byte 0 -> 512 + 64 = 576; block 5 of row 4 is padding (0).
+    sn = _tc_scales(5, 5, 1, 255, 12)
+    outn = O.fp4_scales_tc(sn, 80, 16)
+    assert outn.shape == (4096,)
+    assert outn[576] == sn[4, 4] and outn[577] == 0 and outn[3] == sn[0, 3]
+
+
+@pytest.mark.parametrize("rows,K,block", [(300, 512, 32), (1, 32, 32), (257, 8192, 32), (5, 80, 16),
+                                          (130, 4096, 16)])
+def test_fp4_scales_tc_is_a_permutation_plus_padding(rows, K, block):
+    """Every scale lands in a distinct byte and everything else is padding:
+    the non-padding bytes are exactly the input bytes (as a multiset)."""
+    fill = 0x7F if block == 32 else 0x00
+    s = _tc_scales(rows, K // block, 1, 127 if block == 32 else 255, rows + K)
+    out = O.fp4_scales_tc(s, K, block)
+    kept = out[out != fill]
+    assert kept.size == s.size
+    np.testing.assert_array_equal(np.sort(kept), np.sort(s.ravel()))
