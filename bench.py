@@ -189,10 +189,12 @@ class MxFp4:
     """Per M: quantize A [M, K] and W [N, K] on the device, then C = A W^T.
     W's block scales go into the tensor cores' layout once per step, as part
     of preparing W (the quantize-W call); each GEMM call rearranges A's
-    scales, then runs mx_gemm_fp4_tc."""
+    scales, then runs mx_gemm_fp4_tc.  fused_a: A is quantized inside the
+    GEMM launch instead (mx_gemm_fp4_qa), one call per M."""
 
-    def __init__(self, torch, wq, shapes, replicas, seed=0):
+    def __init__(self, torch, wq, shapes, replicas, seed=0, fused_a=False):
         self.torch, self.wq = torch, wq
+        self.fused_a = fused_a
         K, N = shapes[0][1], shapes[0][2]
         self.K, self.N = K, N
         self.w_src = workloads.mx_source(N, K, seed=seed, stream=1)
@@ -212,6 +214,11 @@ class MxFp4:
         self.calls = [{"call": f"mx_quantize_{N}x{K}", "index": ("qw", 0), "launches": 2,
                        "bytes": N * K * 4 + N * K // 2 + N * K // 32, "flops": 0, "bound": "hbm", "dtype": "fp4"}]
         for i, (M, _, _) in enumerate(shapes):
+            if fused_a:  # one launch: A read as FP32, W, C written
+                self.calls.append({"call": f"mx_gemm_qa_{M}x{K}x{N}", "index": ("gq", i),
+                                   "bytes": M * K * 4 + N * (K // 2 + K // 32) + 4 * M * N, "flops": 2 * M * N * K,
+                                   "bound": "hbm" if M <= 128 else "tensor", "dtype": "fp4"})
+                continue
             self.calls.append({"call": f"mx_quantize_{M}x{K}", "index": ("qa", i),
                                "bytes": M * K * 4 + M * K // 2 + M * K // 32, "flops": 0, "bound": "hbm",
                                "dtype": "fp4"})
@@ -236,10 +243,16 @@ class MxFp4:
             self._oracle_ops = (O.mx_quantize_fp4(self.w_src[:self.G_ROWS_W]),
                                 [O.mx_quantize_fp4(a[:self.G_ROWS_A]) for a in self.a_srcs])
         (wd, ws), a_ops = self._oracle_ops
+        M = self.a_srcs[i].shape[0]
+        if kind == "gq":  # A's rows quantized inside the timed sample, as the fused call does
+            ad, asc = O.mx_quantize_fp4(self.a_srcs[i][:self.G_ROWS_A])
+            O.mx_gemm_fp4(ad, asc, wd, ws)
+            m, n = ad.shape[0], wd.shape[0]
+            return (m * K * 4 + n * (K // 2 + K // 32) + 4 * m * n, 2 * m * n * K,
+                    f"{m} of {M} rows of A (quantized) x {n} of {N} rows of W (extrapolated)")
         ad, asc = a_ops[i]
         O.mx_gemm_fp4(ad, asc, wd, ws)
         m, n = ad.shape[0], wd.shape[0]
-        M = self.a_srcs[i].shape[0]
         return ((m + n) * (K // 2 + K // 32) + 4 * m * n, 2 * m * n * K,
                 f"{m} of {M} rows of A x {n} of {N} rows of W (extrapolated)")
 
@@ -252,7 +265,9 @@ class MxFp4:
             self.wq.fp4_scales_tc(wsc, self.K, out=wsc_tc)
             return
         a, ad, asc, asc_tc, c = d["a"][i]
-        if kind == "qa":
+        if kind == "gq":
+            self.wq.mx_gemm_fp4_qa(a, wd, wsc_tc, c=c)
+        elif kind == "qa":
             self.wq.mx_quantize_fp4(a, ad, asc)
         else:
             self.wq.fp4_scales_tc(asc, self.K, out=asc_tc)
@@ -374,7 +389,7 @@ def make_workload(torch, wq, name, replicas, only=None):
                         group_n=spec.get("group_n"), asym=spec.get("asym", False),
                         batched=spec.get("batched", False))
     elif spec["op"] == "mxfp4":
-        wl = MxFp4(torch, wq, shapes, replicas)
+        wl = MxFp4(torch, wq, shapes, replicas, fused_a=spec.get("fused_a", False))
     elif spec["op"] == "nvfp4":
         wl = NvFp4(torch, wq, shapes, replicas)
     else:
@@ -388,7 +403,7 @@ def make_workload(torch, wq, name, replicas, only=None):
 
 # Workloads reported in `breakdown` besides the headline one.
 BREAKDOWN = ("w8a16_decode_batched", "w4a16_decode", "w4a16_decode_batched", "w4a16_llama7b",
-             "w8a16_grouped_decode", "mxfp4", "nvfp4", "fp8")
+             "w8a16_grouped_decode", "mxfp4", "mxfp4_qa", "nvfp4", "fp8")
 
 
 def replicas_for(step_bytes):

@@ -33,7 +33,7 @@ WQ_ERR_WORKSPACE = 4
 WQ_ERR_LAUNCH = 5
 WQ_ERR_DEVICE = 6
 
-WQ_OP_W4A16, WQ_OP_W8A16, WQ_OP_MX_QUANTIZE, WQ_OP_MX_GEMM, WQ_OP_FP8_GEMM, WQ_OP_NV_GEMM = range(6)
+WQ_OP_W4A16, WQ_OP_W8A16, WQ_OP_MX_QUANTIZE, WQ_OP_MX_GEMM, WQ_OP_FP8_GEMM, WQ_OP_NV_GEMM, WQ_OP_MX_GEMM_QA = range(7)
 WQ_FP4_MX, WQ_FP4_NV = 0, 1
 
 _i, _i64, _p, _sz, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
@@ -51,6 +51,7 @@ _SIGS = {
     "fp4_scales_tc_size": [_i, _i, _i],
     "fp4_scales_tc": [_i, _i, _i, _p, _i64, _p, _sz, _p],
     "mx_gemm_fp4_tc": [_i, _i, _i, _p, _i64, _p, _sz, _p, _i64, _p, _sz, _p, _i64, _p],
+    "mx_gemm_fp4_qa": [_i, _i, _i, _p, _i64, _p, _i64, _p, _sz, _p, _i64, _p, _sz, _p],
     "nv_gemm_fp4_tc": [_i, _i, _i, _p, _i64, _p, _sz, _p, _p, _i64, _p, _sz, _p, _p, _i64, _p],
     "wq_workspace_size": [_i, _i, _i, _i],
     "wq_status_string": [_i],
@@ -193,11 +194,12 @@ def auto_workspace(op: int, M: int, N: int, K: int, device):
     Every successful call leaves its counter area zero again, so the cached
     buffer is reused as is; calls that share one must not overlap on the GPU
     (one cache entry per stream).  The FP4 GEMMs' scratch (rewritten scales,
-    no counters) has a cache entry of its own, so that it never overwrites
-    the weight-only calls' counters."""
+    no counters) and the quantize-A GEMM's (its barrier words first, then
+    scratch) have cache entries of their own, so that no call's scratch
+    overwrites another's counters."""
     import torch
 
-    tag = "fp4" if op in (WQ_OP_MX_GEMM, WQ_OP_NV_GEMM) else "counters"
+    tag = {WQ_OP_MX_GEMM: "fp4", WQ_OP_NV_GEMM: "fp4", WQ_OP_MX_GEMM_QA: "fp4qa"}.get(op, "counters")
     return _cached_workspace(wq_workspace_size(op, M, N, K), device, tag)
 
 
@@ -384,6 +386,33 @@ def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
     wsp, wsb = _ws(workspace)
     _check(lib.mx_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
                            _ptr(c), _ld(c), wsp, wsb, _stream(stream)), "mx_gemm_fp4")
+    return c
+
+
+def mx_gemm_fp4_qa(a, w, sw_tc, c=None, workspace=None, stream=None):
+    """C fp32 [M, N] = MXFP4(A) * W^T with A fp32 [M, K] quantized inside the
+    GEMM launch; W uint8 [N, K/2] with its scales in the tensor-core layout
+    (fp4_scales_tc)."""
+    import torch
+
+    where = "mx_gemm_fp4_qa"
+    _on_gpu(where, a, w, sw_tc, c, workspace)
+    _kind(where, a, "a", dtype="float32")
+    _kind(where, w, "w", size=1)
+    _kind(where, sw_tc, "sw_tc", size=1)
+    _kind(where, c, "c", dtype="float32")
+    _require(a.dim() == 2 and w.dim() == 2, where, "a and w must be 2-D")
+    _require(sw_tc.is_contiguous(), where, "tensor-core scales must be contiguous")
+    M, K, N = a.shape[0], a.shape[1], w.shape[0]
+    _require(w.shape[1] * 2 == K, where, "w must be [N, K/2]")
+    _require(c is None or tuple(c.shape) == (M, N), where, f"c must be [{M}, {N}]")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    if workspace is None:
+        workspace = auto_workspace(WQ_OP_MX_GEMM_QA, M, N, K, a.device)
+    wsp, wsb = _ws(workspace)
+    _check(lib.mx_gemm_fp4_qa(M, N, K, _ptr(a), _ld(a), _ptr(w), _ld(w), _ptr(sw_tc), sw_tc.numel(), _ptr(c), _ld(c),
+                              wsp, wsb, _stream(stream)), where)
     return c
 
 

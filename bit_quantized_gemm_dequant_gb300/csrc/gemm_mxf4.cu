@@ -26,6 +26,7 @@
 //               K slice; the A tile is read once per slice), the scale bytes
 //               chosen by the descriptor's scale-factor ids.
 //   warps 2-5   epilogue: tcgen05.ld and FP32 stores.
+#include "mx_block.cuh"
 #include "tc_common.cuh"
 #include "tma_host.h"
 #include "wq_internal.h"
@@ -85,21 +86,35 @@ int mx_splits(int M, int N, int K) {
 }
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
-// The K step's scale chunks into the stage's scale area: kWords chunks (from
-// chunk kt * kWords) of A's row group m0 / 128, then of W's row groups
-// n0 / 128 and n0 / 128 + 1 (W's rows are padded to a multiple of 256, so
-// both exist).  This order is the one mma_step copies into TMEM.
+// One K step's operands into ring stage `st`: [A tile][W tile][scale area].
+// The scale area takes kWords chunks (from chunk kt * kWords) of A's row group
+// m0 / 128, then of W's row groups n0 / 128 and n0 / 128 + 1 (W's rows are
+// padded to a multiple of 256, so both exist), the order mma_step copies into
+// TMEM.  The W half and the A half are issued separately, so that a launch
+// that quantizes A first can start W's stream before A exists.
 template <bool kNv>
-__device__ __forceinline__ void load_sf_stage(uint8_t* sf, const MxGemmArgs& p, int m0, int n0, int kt,
-                                              uint64_t* bar) {
+__device__ __forceinline__ void load_stage_w(uint8_t* st, const CUtensorMap* tmW, const MxGemmArgs& p, int n0, int kt,
+                                             uint64_t* bar) {
   constexpr uint32_t kPiece = Fmt<kNv>::kPiece;
   const int64_t chunks = tc_sf_chunks(kNv, p.K);
-  const int64_t c = static_cast<int64_t>(kt) * Fmt<kNv>::kWords;
-  tc::bulk_load(sf, p.SA + ((m0 / 128) * chunks + c) * kSfChunk, kPiece, bar);
-  const uint8_t* w = p.SW + ((n0 / 128) * chunks + c) * kSfChunk;
+  tc::tma_load_2d(st + kABytes, tmW, kt * BKB, n0, bar);
+  const uint8_t* w = p.SW + ((n0 / 128) * chunks + static_cast<int64_t>(kt) * Fmt<kNv>::kWords) * kSfChunk;
+  uint8_t* sf = st + kABytes + kBBytes;
   tc::bulk_load(sf + kPiece, w, kPiece, bar);
   tc::bulk_load(sf + 2 * kPiece, w + chunks * kSfChunk, kPiece, bar);
 }
+
+template <bool kNv>
+__device__ __forceinline__ void load_stage_a(uint8_t* st, const CUtensorMap* tmA, const MxGemmArgs& p, int m0, int kt,
+                                             uint64_t* bar) {
+  const int64_t chunks = tc_sf_chunks(kNv, p.K);
+  tc::tma_load_2d(st, tmA, kt * BKB, m0, bar);
+  tc::bulk_load(st + kABytes + kBBytes,
+                p.SA + ((m0 / 128) * chunks + static_cast<int64_t>(kt) * Fmt<kNv>::kWords) * kSfChunk,
+                Fmt<kNv>::kPiece, bar);
+}
+
+__host__ __device__ constexpr uint32_t stage_tx(bool nv) { return kABytes + kBBytes + 3 * (nv ? Fmt<true>::kPiece : Fmt<false>::kPiece); }
 
 // One K step on the tensor cores: copy the stage's scale chunks into its TMEM
 // columns, then four 128 x 256 x 64 block-scaled MMAs.
@@ -152,6 +167,160 @@ __device__ __forceinline__ float tensor_scale(const MxGemmArgs& p) {
 }
 
 
+// ------------------------------------------------ A quantized in the launch
+// mx_gemm_fp4_qa: the MXFP4 page's flow quantizes both operands before the
+// GEMM (§三); here A's quantization is the first phase of the GEMM launch.
+// Every CTA quantizes its share of A into the workspace (codes, and scales
+// already in the tensor-core layout), the grid meets at one barrier, and the
+// GEMM proper reads A from there through the same TMA and bulk copies as
+// always.  Each element is quantized exactly once, with the arithmetic of
+// mx_quantize_fp4 (mx_block.cuh), so the codes and the result are those of
+// quantize-then-GEMM, bit for bit.
+//
+// Items are (row r < M rounded up to 256, chunk c < kc): blocks 4c .. 4c + 3
+// of row r, 128 elements, for a group of 16 threads (four per block, eight
+// elements each), numbered row by row.  The items of A's rows and those of
+// the padding rows (scale 2^0, no codes: their data reads as zero through
+// the tensor map) are split over the CTAs separately, so that every CTA gets
+// the same share of real rows.  A group handles kQaUnroll items per round
+// and loads the next round's elements before it quantizes the current ones,
+// so the loads stay in flight while the arithmetic runs.
+constexpr int kQaUnroll = 4;
+
+// This CTA's items: local index v < n maps to real item r0 + v (v < nr) or
+// padding item p0 + v - nr.
+struct QaItems {
+  uint32_t chunks, nb, r0, nr, p0, n;
+  __device__ __forceinline__ uint32_t item(uint32_t v) const { return v < nr ? r0 + v : p0 + (v - nr); }
+};
+
+__device__ __forceinline__ QaItems qa_items(const MxGemmArgs& p) {
+  QaItems q;
+  q.chunks = static_cast<uint32_t>(tc_sf_chunks(false, p.K));
+  q.nb = static_cast<uint32_t>(p.K / 32);
+  const uint32_t real = static_cast<uint32_t>(p.M) * q.chunks;
+  const uint32_t pad = static_cast<uint32_t>((p.M + 255) / 256 * 256 - p.M) * q.chunks;  // total < 2^31 (host check)
+  const uint64_t G = gridDim.x * gridDim.y * gridDim.z;
+  const uint64_t b = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  q.r0 = static_cast<uint32_t>(b * real / G);
+  q.nr = static_cast<uint32_t>((b + 1) * real / G) - q.r0;
+  q.p0 = real + static_cast<uint32_t>(b * pad / G);
+  q.n = q.nr + (real + static_cast<uint32_t>((b + 1) * pad / G) - q.p0);
+  return q;
+}
+
+// One round's loads: this thread's eight elements of local item base + grp + u ngrp,
+// and each item's row and chunk column (kept for the quantization step).
+__device__ __forceinline__ void qa_load(const MxGemmArgs& p, const QaItems& q, uint32_t base, uint32_t grp,
+                                        uint32_t ngrp, uint32_t j, uint32_t qq, float4 (&v)[kQaUnroll][2],
+                                        uint32_t (&rows)[kQaUnroll], uint32_t (&cols)[kQaUnroll]) {
+#pragma unroll
+  for (int u = 0; u < kQaUnroll; ++u) {
+    const uint32_t lv = base + grp + u * ngrp;
+    const uint32_t item = q.item(lv);
+    const uint32_t row = item / q.chunks, col = item - row * q.chunks, blk = 4 * col + j;
+    rows[u] = row;
+    cols[u] = col;
+    if (lv < q.n && row < static_cast<uint32_t>(p.M) && blk < q.nb) {
+      const float4* src = reinterpret_cast<const float4*>(p.A32 + static_cast<int64_t>(row) * p.lda32 + 32 * blk + 8 * qq);
+      v[u][0] = __ldcs(src);
+      v[u][1] = __ldcs(src + 1);
+    } else {
+      v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+__device__ void quantize_a_share(const MxGemmArgs& p) {
+  const QaItems q = qa_items(p);
+  const int lane = threadIdx.x & 31, t16 = lane & 15;
+  const uint32_t grp = threadIdx.x >> 4, ngrp = blockDim.x >> 4;
+  const uint32_t j = t16 >> 2, qq = t16 & 3;  // block within the item, quarter within the block
+  const uint32_t step = ngrp * kQaUnroll;
+  float4 nxt[kQaUnroll][2];
+  uint32_t nrow[kQaUnroll], ncol[kQaUnroll];
+  if (q.n > 0) qa_load(p, q, 0, grp, ngrp, j, qq, nxt, nrow, ncol);
+  // The loop bound is the same for every thread, so all lanes reach the shuffles.
+  for (uint32_t base = 0; base < q.n; base += step) {
+    float4 v[kQaUnroll][2];
+    uint32_t crow[kQaUnroll], ccol[kQaUnroll];
+#pragma unroll
+    for (int u = 0; u < kQaUnroll; ++u) {
+      v[u][0] = nxt[u][0];
+      v[u][1] = nxt[u][1];
+      crow[u] = nrow[u];
+      ccol[u] = ncol[u];
+    }
+    if (base + step < q.n) qa_load(p, q, base + step, grp, ngrp, j, qq, nxt, nrow, ncol);
+#pragma unroll
+    for (int u = 0; u < kQaUnroll; ++u) {
+      const bool item_ok = base + grp + u * ngrp < q.n;
+      const uint32_t row = crow[u], col = ccol[u];
+      const uint32_t blk = 4 * col + j;
+      const bool real = item_ok && row < static_cast<uint32_t>(p.M) && blk < q.nb;
+      const float xs[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                           v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(xs[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, 1e-8f);
+      const int e = mx_block_exponent(amax);
+      const uint32_t word = e2m1_word(xs, mx_inv_scale(e));
+      if (real) *reinterpret_cast<uint32_t*>(p.Aq + static_cast<int64_t>(row) * p.ldq + 16 * blk + 4 * qq) = word;
+      // The four blocks' scale bytes, gathered from the quad leaders of this
+      // 16-thread group, form one word of the chunk line.
+      const uint32_t sb = real ? static_cast<uint32_t>(e + 127) : 0x7Fu;
+      const int g0 = lane & 16;
+      const uint32_t sw = __shfl_sync(0xffffffffu, sb, g0) | (__shfl_sync(0xffffffffu, sb, g0 + 4) << 8) |
+                          (__shfl_sync(0xffffffffu, sb, g0 + 8) << 16) | (__shfl_sync(0xffffffffu, sb, g0 + 12) << 24);
+      if (t16 == 0 && item_ok)
+        *reinterpret_cast<uint32_t*>(p.SAq + (static_cast<int64_t>(row / 128) * q.chunks + col) * kSfChunk +
+                                     16 * (row % 32) + 4 * ((row / 32) % 4)) = sw;
+    }
+  }
+}
+
+// One barrier over the whole grid (the launch is cooperative, so every CTA is
+// resident).  Word 0 of grid_bar counts arrivals, word 1 departures; the last
+// CTA to leave zeroes both, so the next call finds them zero.  Returns false,
+// with the error recorded and *abort raised, if the other CTAs do not all
+// arrive within the wait limit.  Before it, each thread fences its global
+// writes for the async proxy (the GEMM reads them with TMA and bulk copies).
+__device__ bool grid_barrier(unsigned* bar, volatile int* abort, int* err) {
+  tc::fence_proxy_async_all();
+  tc::cta_barrier();
+  if (threadIdx.x == 0) {
+    const unsigned G = gridDim.x * gridDim.y * gridDim.z;
+    __threadfence();
+    atomicAdd(&bar[0], 1u);
+    const uint64_t t0 = tc::globaltimer_ns();
+    bool ok = true;
+    // Spin for the first few microseconds (the CTAs normally arrive within
+    // one or two), then poll with a short sleep; give up after the limit.
+    for (uint32_t it = 0; tc::ld_acquire_gpu(&bar[0]) < G; ++it) {
+      if ((it & 63u) != 63u) continue;
+      const uint64_t dt = tc::globaltimer_ns() - t0;
+      if (dt > 2000000000ull) {
+        if (err) atomicCAS(err, 0, kSiteGridBarrier);
+        *abort = 1;
+        ok = false;
+        break;
+      }
+      if (dt > 8000u) __nanosleep(64);
+    }
+    if (ok && atomicAdd(&bar[1], 1u) == G - 1) {
+      atomicExch(&bar[0], 0u);
+      atomicExch(&bar[1], 0u);
+    }
+    __threadfence();
+  }
+  tc::cta_barrier();
+  tc::fence_proxy_async_all();
+  return !*abort;
+}
+
 // Transpose a 32 x 32 block held one row per lane (lane i: v[j] = B[i][j])
 // into one column per lane (lane j: v[i] = B[i][j]), with five butterfly
 // stages of register exchanges between lanes.
@@ -170,7 +339,7 @@ __device__ __forceinline__ void warp_transpose32(uint32_t (&v)[32], int lane) {
   }
 }
 
-template <bool kNv>
+template <bool kNv, bool kQA>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
                int* err) {
@@ -212,8 +381,30 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // Launched as a programmatic dependent of the scale re-layout: every read
   // of the inputs and every write of C comes after this.
   tc::griddep_wait();
+  // Quantizing A first: the W halves of the first stages (fresh ring slots)
+  // are issued before, so that W's stream overlaps A's quantization.
+  const int pre = kQA ? (KT < kStages ? KT : kStages) : 0;
+  if constexpr (kQA) {
+    if (warp == 0 && lane == 0) {
+      tc::tma_prefetch_desc(&tmW);
+      for (int i = 0; i < pre; ++i) {
+        tc::mbar_arrive_expect_tx(&full[i], stage_tx(kNv));
+        load_stage_w<kNv>(smem + i * kStageBytes, &tmW, p, n0, kt0 + i, &full[i]);
+      }
+    }
+    quantize_a_share(p);
+    grid_barrier(p.grid_bar, abort, err);
+  }
 
-  if (warp == 0) {
+  if (kQA && *abort) {
+    // The grid barrier gave up: no role runs (the cluster steps below still
+    // do).  The early W copies are in flight: complete their stages with the
+    // A halves (in-bounds reads of the workspace) and wait for them.
+    if (warp == 0 && lane == 0) {
+      for (int i = 0; i < pre; ++i) load_stage_a<kNv>(smem + i * kStageBytes, &tmA, p, m0, kt0 + i, &full[i]);
+      for (int i = 0; i < pre; ++i) tc::mbar_wait_drain(&full[i], 0);
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmA);
       tc::tma_prefetch_desc(&tmW);
@@ -221,14 +412,18 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int issued = 0;
     for (int i = 0; i < KT; ++i) {
       const int kt = kt0 + i, s = i % kStages;
+      uint8_t* st = smem + s * kStageBytes;
+      if (i < pre) {  // W half already issued
+        if (lane == 0) load_stage_a<kNv>(st, &tmA, p, m0, kt, &full[s]);
+        issued = i + 1;
+        continue;
+      }
       const bool free_slot = tc::mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
       if (!__all_sync(0xffffffffu, free_slot)) break;  // warp-uniform exit
-      uint8_t* st = smem + s * kStageBytes;
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + 3 * Fmt<kNv>::kPiece);
-        tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
-        tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
-        load_sf_stage<kNv>(st + kABytes + kBBytes, p, m0, n0, kt, &full[s]);
+        tc::mbar_arrive_expect_tx(&full[s], stage_tx(kNv));
+        load_stage_a<kNv>(st, &tmA, p, m0, kt, &full[s]);
+        load_stage_w<kNv>(st, &tmW, p, n0, kt, &full[s]);
       }
       issued = i + 1;
     }
@@ -399,7 +594,7 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
   }
 }
 
-template <bool kNv>
+template <bool kNv, bool kQA>
 __global__ void __launch_bounds__(kPThreads, 1)
 mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
                    int* err) {
@@ -440,8 +635,31 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   // Launched as a programmatic dependent of the scale re-layout: every read
   // of the inputs and every write of C comes after this.
   tc::griddep_wait();
+  // Quantizing A first: the W halves of the first tile's first stages are
+  // issued before, so that W's stream overlaps A's quantization (the grid is
+  // at most one CTA per tile, so every CTA has a first tile).
+  const int pre = kQA ? (KT < kStages ? KT : kStages) : 0;
+  const int m00 = (static_cast<int>(blockIdx.x) % m_tiles) * BM, n00 = (static_cast<int>(blockIdx.x) / m_tiles) * BN;
+  if constexpr (kQA) {
+    if (warp == 0 && lane == 0) {
+      tc::tma_prefetch_desc(&tmW);
+      for (int i = 0; i < pre; ++i) {
+        tc::mbar_arrive_expect_tx(&full[i], stage_tx(kNv));
+        load_stage_w<kNv>(smem + i * kStageBytes, &tmW, p, n00, i, &full[i]);
+      }
+    }
+    quantize_a_share(p);
+    grid_barrier(p.grid_bar, abort, err);
+  }
 
-  if (warp == 0) {
+  if (kQA && *abort) {
+    // The grid barrier gave up: no role runs.  Complete the early stages
+    // with their A halves and wait for them, so no copy is left in flight.
+    if (warp == 0 && lane == 0) {
+      for (int i = 0; i < pre; ++i) load_stage_a<kNv>(smem + i * kStageBytes, &tmA, p, m00, i, &full[i]);
+      for (int i = 0; i < pre; ++i) tc::mbar_wait_drain(&full[i], 0);
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmA);
       tc::tma_prefetch_desc(&tmW);
@@ -452,17 +670,21 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       const int m0 = (t % m_tiles) * BM, n0 = (t / m_tiles) * BN;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int s = it % kStages;
+        uint8_t* st = smem + s * kStageBytes;
+        if (it < pre) {  // W half already issued (first tile, fresh slot)
+          if (lane == 0) load_stage_a<kNv>(st, &tmA, p, m0, kt, &full[s]);
+          issued = it + 1;
+          continue;
+        }
         const bool free_slot = tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
         if (!__all_sync(0xffffffffu, free_slot)) {
           go = false;
           break;
         }
-        uint8_t* st = smem + s * kStageBytes;
         if (lane == 0) {
-          tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes + 3 * Fmt<kNv>::kPiece);
-          tc::tma_load_2d(st, &tmA, kt * BKB, m0, &full[s]);
-          tc::tma_load_2d(st + kABytes, &tmW, kt * BKB, n0, &full[s]);
-          load_sf_stage<kNv>(st + kABytes + kBBytes, p, m0, n0, kt, &full[s]);
+          tc::mbar_arrive_expect_tx(&full[s], stage_tx(kNv));
+          load_stage_a<kNv>(st, &tmA, p, m0, kt, &full[s]);
+          load_stage_w<kNv>(st, &tmW, p, n0, kt, &full[s]);
         }
         issued = it + 1;
       }
@@ -554,30 +776,64 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 namespace {
 
-template <bool kNv>
+// kQA: A arrives as FP32 and is quantized in the same launch (MXFP4 only).
+// That launch is cooperative (its CTAs meet at a grid barrier), so its grid
+// must be resident at once: the persistent grid is one CTA per SM at most,
+// and a K split is narrowed until the occupancy query says its clusters fit.
+template <bool kNv, bool kQA = false>
 cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
   if (a.K == 0)
     return cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
   CUtensorMap tA, tW;
-  cudaError_t e = make_tmap_2d(&tA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.lda, BKB, BM,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+  cudaError_t e = kQA ? make_tmap_2d(&tA, a.Aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.ldq, BKB, BM,
+                                     CU_TENSOR_MAP_SWIZZLE_128B)
+                      : make_tmap_2d(&tA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.lda, BKB, BM,
+                                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.N, a.ldw, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  const int splits = mx_splits(a.M, a.N, a.K);
+  int splits = mx_splits(a.M, a.N, a.K);
   // Both kernels start as programmatic dependents of the launch before them
   // (normally the scale re-layout) and wait for it before touching memory.
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(splits == 1 ? kPThreads : kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[3];
+  attr[0].id = kQA ? cudaLaunchAttributeCooperative : cudaLaunchAttributeProgrammaticStreamSerialization;
+  if (kQA) attr[0].val.cooperative = 1;
+  else attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  auto kern = mx_gemm_kernel<kNv, kQA>;
+  static PerDevice<bool> configured;
+  bool done = false;
+  if (splits > 1 &&
+      !configured.get(done, [&](bool& v) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        v = true;
+        return e == cudaSuccess;
+      }))
+    return e;
+  const int tiles = ((a.N + BN - 1) / BN) * ((a.M + BM - 1) / BM);
+  if (kQA) {
+    for (; splits > 1; --splits) {
+      cudaLaunchConfig_t q = cfg;
+      cudaLaunchAttribute ca[1];
+      ca[0].id = cudaLaunchAttributeClusterDimension;
+      ca[0].val.clusterDim.x = 1;
+      ca[0].val.clusterDim.y = 1;
+      ca[0].val.clusterDim.z = splits;
+      q.attrs = ca;
+      q.numAttrs = 1;
+      q.blockDim = dim3(kThreads);
+      q.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &q) == cudaSuccess && clusters >= tiles) break;
+    }
+  }
+  cfg.blockDim = dim3(splits == 1 ? kPThreads : kThreads);
   if (splits == 1) {  // persistent: one CTA per SM
-    auto pk = mx_gemm_persistent<kNv>;
+    auto pk = mx_gemm_persistent<kNv, kQA>;
     static PerDevice<bool> pconfigured;
     bool pdone = false;
     if (!pconfigured.get(pdone, [&](bool& v) {
@@ -586,21 +842,11 @@ cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
           return e == cudaSuccess;
         }))
       return e;
-    const int tiles = ((a.N + BN - 1) / BN) * ((a.M + BM - 1) / BM);
     cfg.gridDim = dim3(tiles < sm_count() ? tiles : sm_count());
     e = cudaLaunchKernelEx(&cfg, pk, tA, tW, a, device_error_word());
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  auto kern = mx_gemm_kernel<kNv>;
-  static PerDevice<bool> configured;
-  bool done = false;
-  if (!configured.get(done, [&](bool& v) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        v = true;
-        return e == cudaSuccess;
-      }))
-    return e;
   // Split K: each tile's splits form a thread-block cluster (along z) that
   // adds its partial tiles in distributed shared memory.
   cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
@@ -617,6 +863,8 @@ cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s) { return launch_fp4_gemm<false>(a, s); }
+
+cudaError_t launch_mx_gemm_qa(const MxGemmArgs& a, cudaStream_t s) { return launch_fp4_gemm<false, true>(a, s); }
 
 cudaError_t launch_nv_gemm(const MxGemmArgs& a, cudaStream_t s) { return launch_fp4_gemm<true>(a, s); }
 

@@ -9,6 +9,7 @@
 // own one block: each loads 32 contiguous bytes (two 128-bit loads), the
 // block amax is a 4-lane shuffle max, and each thread stores one 32-bit word
 // of packed codes, so a warp reads 1 KB and writes 128 B contiguously.
+#include "mx_block.cuh"
 #include "wq_internal.h"
 
 namespace wq {
@@ -16,25 +17,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;  // blocks in flight per thread quad
-
-__device__ __forceinline__ uint32_t e2m1_code(float x, float inv_scale) {
-  // v = x * 2^-e is exact (a power-of-two scaling) and |v| <= 6.  The index
-  // of the nearest grid point, the smaller one on a tie (the first index of
-  // the argmin), is the number of grid midpoints strictly below |v|:
-  //   |v| >= 1: the grid is every float with one mantissa bit from 1 to 6.
-  //             Adding just under half a unit of that bit (2^21 - 1) and
-  //             truncating rounds to nearest with ties to the smaller
-  //             magnitude; the index is 2 * (unbiased exponent + 1) plus the
-  //             kept mantissa bit, i.e. (bits >> 22) - 252.
-  //   |v| < 1:  the grid is 0, 0.5, 1, with midpoints 0.25 and 0.75.
-  // Non-negative float bits compare like the floats.  This equals counting
-  // the seven midpoints (0.25 .. 5) one by one for every float32 in [0, 6].
-  const uint32_t a = __float_as_uint(x * inv_scale) & 0x7FFFFFFFu;
-  const uint32_t big = ((a + 0x1FFFFFu) >> 22) - 252u;
-  const uint32_t small = (a > 0x3E800000u) + (a > 0x3F400000u);  // 0.25f, 0.75f
-  const uint32_t j = a >= 0x3F800000u ? big : small;              // 1.0f
-  return (x < 0.0f ? 8u : 0u) | j;
-}
 
 // Element offsets of 32-element block `item` in the source, data and scale
 // arrays.  kDense: rows are packed back to back (every leading dimension is
@@ -92,19 +74,8 @@ mx_quantize_kernel(MxQuantArgs p, uint32_t n_items) {
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       amax = fmaxf(amax, 1e-8f);
-      // e = ceil(log2 q) with q = amax / 6 rounded to FP32, read off amax's
-      // own bits.  With amax = m 2^E (1 <= m < 2): amax / 6 = (m / 1.5) 2^(E-2),
-      // and m / 1.5 lies in (1, 4/3) when m > 1.5 (e = E - 1) and in [2/3, 1]
-      // otherwise (e = E - 2).  Rounding m / 1.5 to FP32 never lands on 1 from
-      // either side except at m = 1.5 itself, so e = E - 2 + [m > 1.5].  amax
-      // and q are normal because amax >= 1e-8.  (Equal to the rounded
-      // quotient's ceil(log2) for every mantissa, checked exhaustively.)
-      const uint32_t ab = __float_as_uint(amax);
-      const int e = static_cast<int>(ab >> 23) - 129 + ((ab & 0x7FFFFFu) > 0x400000u);
-      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-      uint32_t word = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) word |= e2m1_code(xs[i], inv_scale) << (4 * i);
+      const int e = mx_block_exponent(amax);
+      const uint32_t word = e2m1_word(xs, mx_inv_scale(e));
       if (src[u] >= 0) {
         __stcs(reinterpret_cast<unsigned int*>(p.data + data[u] + quad_lane * 4), word);
         if (quad_lane == 0) p.scales[sc[u]] = static_cast<uint8_t>(e + 127);

@@ -280,6 +280,43 @@ int mx_gemm_fp4_tc(int M, int N, int K, const uint8_t* A, int64_t lda, const uin
   return fp4_gemm_tc(false, a, sa_bytes, sw_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// mx_gemm_fp4_qa workspace: the grid barrier's words, A's codes, A's scales
+// (tensor-core layout), each part starting on a 256-byte boundary.
+static int64_t qa_ldq(int K) { return (static_cast<int64_t>(K / 2) + 15) / 16 * 16; }
+static size_t qa_codes_bytes(int M, int K) { return (static_cast<size_t>(M) * qa_ldq(K) + 255) & ~size_t(255); }
+constexpr size_t kQaBarrierBytes = 256;
+
+int mx_gemm_fp4_qa(int M, int N, int K, const float* A, int64_t lda, const uint8_t* W, int64_t ldw, const uint8_t* SW,
+                   size_t sw_bytes, float* C, int64_t ldc, void* workspace, size_t ws_bytes, wq_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || K % 32) return WQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return WQ_OK;
+  if (!C || ldc < N) return WQ_ERR_INVALID_ARG;
+  if (!aligned(C, 16) || ldc % 4) return WQ_ERR_MISALIGNED;
+  if (M > kMaxTiledM || N > kMaxTiledM) return WQ_ERR_UNSUPPORTED;
+  if (K > 0) {
+    if (!A || !W || !SW || lda < K || ldw < K / 2) return WQ_ERR_INVALID_ARG;
+    if (sw_bytes < tc_sf_bytes(false, N, K)) return WQ_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || lda % 4 || !aligned(W, 16) || ldw % 16 || !aligned(SW, 16)) return WQ_ERR_MISALIGNED;
+    // 32-bit item counters in the quantize phase
+    if (static_cast<int64_t>((M + 255) / 256 * 256) * tc_sf_chunks(false, K) >= (int64_t(1) << 31))
+      return WQ_ERR_UNSUPPORTED;
+    if (ws_bytes < wq_workspace_size(WQ_OP_MX_GEMM_QA, M, N, K) || !workspace || !aligned(workspace, 256))
+      return WQ_ERR_WORKSPACE;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  MxGemmArgs a{M, N, K, nullptr, 0, nullptr, W, ldw, SW, C, ldc};
+  a.A32 = A;
+  a.lda32 = lda;
+  a.grid_bar = reinterpret_cast<unsigned*>(ws);
+  a.Aq = ws + kQaBarrierBytes;
+  a.ldq = qa_ldq(K);
+  a.SAq = a.Aq + qa_codes_bytes(M, K);
+  a.A = a.Aq;
+  a.lda = a.ldq;
+  a.SA = a.SAq;
+  return launch_status(launch_mx_gemm_qa(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t fp4_scales_tc_size(int format, int rows, int K) {
   if ((format != WQ_FP4_MX && format != WQ_FP4_NV) || rows <= 0 || K <= 0) return 0;
   if (K % (format == WQ_FP4_NV ? 16 : 32)) return 0;
@@ -383,6 +420,8 @@ size_t wq_workspace_size(int op, int M, int N, int K) {
   if (op == WQ_OP_W4A16 && K % 2 == 0) return weight_only_workspace(4, M, N, K);
   if (op == WQ_OP_W8A16 && K % 2 == 0) return weight_only_workspace(8, M, N, K);
   if (op == WQ_OP_FP8_GEMM && M <= kFp8SkinnyMaxM) return plan_skinny(M, N, K, 9).ws_bytes;
+  if (op == WQ_OP_MX_GEMM_QA && K % 32 == 0)
+    return kQaBarrierBytes + qa_codes_bytes(M, K) + tc_sf_bytes(false, M, K);
   if ((op == WQ_OP_MX_GEMM && K % 32 == 0) || (op == WQ_OP_NV_GEMM && K % 16 == 0)) {
     const bool nv = op == WQ_OP_NV_GEMM;
     return fp4_ws_a_bytes(nv, M, K) + tc_sf_bytes(nv, N, K);

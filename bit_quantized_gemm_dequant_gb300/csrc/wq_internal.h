@@ -64,6 +64,7 @@ enum ErrorSite : int {
   kSiteGemmTmemFree = 4,   // MMA issuer waited too long for the epilogue
   kSiteClusterRecv = 5,    // a CTA waited too long for its cluster peers' partial sums
   kSiteBatchRecv = 6,      // a batched-call CTA waited too long for its neighbours' published parts
+  kSiteGridBarrier = 7,    // a CTA of the quantize-then-GEMM launch waited too long for the others
 };
 
 struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
@@ -109,6 +110,14 @@ struct MxGemmArgs {  // MXFP4 and NVFP4 GEMMs
   float* C; int64_t ldc;
   const float* ga = nullptr;  // NVFP4: the tensor scales of A and W (device memory)
   const float* gw = nullptr;
+  // mx_gemm_fp4_qa: A arrives as FP32 (A32, row stride lda32 elements) and
+  // the launch quantizes it first, into codes Aq [M, K/2] (row stride ldq) and
+  // scales SA (the tensor-core layout) in the workspace, meeting at a grid
+  // barrier whose two words are grid_bar.
+  const float* A32 = nullptr; int64_t lda32 = 0;
+  uint8_t* Aq = nullptr; int64_t ldq = 0;
+  uint8_t* SAq = nullptr;
+  unsigned* grid_bar = nullptr;
 };
 
 struct NvQuantArgs {
@@ -151,6 +160,7 @@ cudaError_t launch_wo_skinny(const WoArgs& a, int bits, const SkinnyPlan& pl, cu
 cudaError_t launch_wo_gemm(const WoArgs& a, int bits, cudaStream_t s);
 cudaError_t launch_mx_quantize(const MxQuantArgs& a, cudaStream_t s);
 cudaError_t launch_mx_gemm(const MxGemmArgs& a, cudaStream_t s);
+cudaError_t launch_mx_gemm_qa(const MxGemmArgs& a, cudaStream_t s);  // A from FP32 in the same launch
 // Row-major block scales S [rows, K / block] (row stride lds bytes) -> the
 // tensor-core layout above, tc_sf_bytes(nv, rows, K) bytes at out.
 cudaError_t launch_fp4_scales_tc(bool nv, int rows, int K, const uint8_t* S, int64_t lds, uint8_t* out,

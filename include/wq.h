@@ -65,6 +65,7 @@ typedef struct CUstream_st* wq_stream_t;
 #define WQ_OP_MX_GEMM 3
 #define WQ_OP_FP8_GEMM 4
 #define WQ_OP_NV_GEMM 5
+#define WQ_OP_MX_GEMM_QA 6
 
 /*
  * wq_gemm_w4a16 — Y = X * ((q - 8) * s), INT4 weights dequantized on chip.
@@ -348,6 +349,44 @@ int mx_gemm_fp4_tc(int M, int N, int K, const uint8_t* A, int64_t lda,
                    const uint8_t* SA, size_t sa_bytes, const uint8_t* W,
                    int64_t ldw, const uint8_t* SW, size_t sw_bytes, float* C,
                    int64_t ldc, wq_stream_t stream);
+
+/*
+ * mx_gemm_fp4_qa — C = MXFP4(A) * W^T with A given in FP32, quantized inside
+ * the GEMM's own launch.
+ *
+ * [MXFP4] §三: the simulator quantizes both A and W to MXFP4 (32-element
+ * blocks, E8M0 exponents, nearest E2M1 codes) and then runs the block-scaled
+ * GEMM.  Here W is quantized beforehand (weights) and A, the activations, is
+ * quantized by the GEMM launch itself: every CTA first quantizes its share
+ * of A with exactly mx_quantize_fp4's arithmetic, into the workspace, the
+ * grid meets at one barrier, and the GEMM reads those codes and scales.
+ * No separate quantize launch and no re-layout of A's scales; C equals
+ * mx_quantize_fp4 of A followed by mx_gemm_fp4, bit for bit.
+ *
+ *   A        fp32 [M, K], row stride lda (elements); K % 32 == 0.
+ *   W, SW    W's codes uint8 [N, K/2] (row stride ldw) and its scales in
+ *            the tensor-core layout (fp4_scales_tc with WQ_FP4_MX, N rows),
+ *            sw_bytes the size of that buffer.
+ *   C        fp32 [M, N], row stride ldc.
+ *   workspace, ws_bytes  at least wq_workspace_size(WQ_OP_MX_GEMM_QA, M, N,
+ *            K) bytes, 256-byte aligned.  Its first 8 bytes (the grid
+ *            barrier's counters) must be zero before the first call; every
+ *            call that returns WQ_OK leaves them zero.  After WQ_ERR_DEVICE
+ *            zero them again.  Two calls in flight must not share it.  After
+ *            the call the workspace holds the quantized A, for reuse: its
+ *            codes uint8 [M, ldq] at byte 256 (ldq = K/2 rounded up to a
+ *            multiple of 16, the codes of mx_quantize_fp4 in the first K/2
+ *            bytes of each row), then, at the next 256-byte boundary, its
+ *            scales in the tensor-core layout (fp4_scales_tc of A's scales).
+ * Alignment: A 16-byte aligned with lda a multiple of 4; W, SW 16-byte
+ * aligned with ldw a multiple of 16; C as for mx_gemm_fp4.
+ * The launch is cooperative (all of its CTAs are resident at once); when
+ * its CTAs cannot all be resident the call returns WQ_ERR_LAUNCH.
+ */
+int mx_gemm_fp4_qa(int M, int N, int K, const float* A, int64_t lda,
+                   const uint8_t* W, int64_t ldw, const uint8_t* SW,
+                   size_t sw_bytes, float* C, int64_t ldc, void* workspace,
+                   size_t ws_bytes, wq_stream_t stream);
 
 /*
  * nv_quantize_fp4 — quantize FP32 rows to NVFP4: E2M1 elements in 16-element

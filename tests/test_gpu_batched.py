@@ -154,7 +154,7 @@ def test_repeated_calls_deterministic_and_counters_zero(wq, bits):
         for a, b in zip(first, again):
             assert torch.equal(a, b)
     torch.cuda.synchronize()
-    buf = wq._WS_CACHE[(torch.cuda.current_device(), torch.cuda.current_stream().cuda_stream)]
+    buf = wq._WS_CACHE[("counters", torch.cuda.current_device(), torch.cuda.current_stream().cuda_stream)]
     assert torch.count_nonzero(buf[:65536]).item() == 0
 
 

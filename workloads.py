@@ -178,6 +178,8 @@ WORKLOADS = {
     "w4a16_llama7b": {"op": "w4a16", "shapes": [(m, k, n) for (k, n) in ((4096, 4096), (4096, 11008), (11008, 4096))
                                                 for m in (1, 8, 64, 512, 4096)]},
     "mxfp4": {"op": "mxfp4", "shapes": [(m, 8192, 8192) for m in (128, 2048, 8192)]},
+    # The same, with A quantized inside the GEMM launch (one call per M).
+    "mxfp4_qa": {"op": "mxfp4", "fused_a": True, "shapes": [(m, 8192, 8192) for m in (128, 2048, 8192)]},
     # The same operands in NVFP4 (16-element blocks, E4M3 block scales, FP32
     # tensor scale), quantized on the device, then C = A W^T.
     "nvfp4": {"op": "nvfp4", "shapes": [(m, 8192, 8192) for m in (128, 2048, 8192)]},
