@@ -763,6 +763,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     import bit_quantized_gemm_dequant_gb300 as wq
 
+    wq.set_static_weights(args.static_weights)
     peaks = load_peaks()
     probe = make_workload(torch, wq, args.workload, 1, args.only)
     step_bytes = sum(c["bytes"] for c in probe.calls)
@@ -849,7 +850,8 @@ def run_ours(args):
                        "replicas": replicas,
                        "l2": f"inputs rotate over {replicas} replicas of {step_bytes / 1e6:.0f} MB per step "
                              f"(> 2 x {L2_BYTES / 1e6:.0f} MB L2 between reuses)",
-                       "parallelism": f"replicas x{ws}"},
+                       "parallelism": f"replicas x{ws}",
+                       "static_weights": bool(args.static_weights)},
             "roofline": roof,
             "per_call": [{**c, "achieved": roofline_for(c, peaks)["achieved"]} for c in per_call],
             "e2e": e2e,
@@ -965,6 +967,9 @@ def main():
     ap.add_argument("--only", default=None, help="keep only the calls whose name contains this string")
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--static-weights", action="store_true",
+                    help="wq_set_static_weights(1): the weights are only read during the run, so the decode "
+                         "kernels may load their first weight boxes while the previous call finishes")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture of this build")

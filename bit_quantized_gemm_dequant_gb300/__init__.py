@@ -58,6 +58,7 @@ _SIGS = {
     "wq_get_device_error": [_p, ctypes.POINTER(_i)],
     "wq_version": [],
     "wq_debug_set_wait_limit": [_i64],
+    "wq_set_static_weights": [_i],
 }
 
 
@@ -387,6 +388,14 @@ def mx_gemm_fp4(a, sa, w, sw, c=None, workspace=None, stream=None):
     _check(lib.mx_gemm_fp4(M, N, K, _ptr(a), _ld(a), _ptr(sa), _ld(sa), _ptr(w), _ld(w), _ptr(sw), _ld(sw),
                            _ptr(c), _ld(c), wsp, wsb, _stream(stream)), "mx_gemm_fp4")
     return c
+
+
+def set_static_weights(enable: bool) -> bool:
+    """wq_set_static_weights: promise that weight and scale arrays are not
+    written by any kernel still running when a weight-only call launches, so
+    that the decode kernels may load their first weight boxes early.
+    Returns the previous setting."""
+    return bool(lib.wq_set_static_weights(1 if enable else 0))
 
 
 def mx_gemm_fp4_qa(a, w, sw_tc, c=None, workspace=None, stream=None):

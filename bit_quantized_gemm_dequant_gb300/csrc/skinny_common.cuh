@@ -49,6 +49,9 @@ struct SkinnyArgs {
   const void* zeros;  // weight-only: one zero point per column group, or nullptr
   int group_n;        // weight-only: columns per scale / zero-point group
   uint64_t wait_ns = 2000000000ull;  // limit of a bounded wait before the kernel gives up
+  // The caller promised static weights (wq_set_static_weights): the first
+  // weight boxes may be loaded before the grid dependency wait.
+  int early_w = 0;
 };
 
 // The deepest per-warp ring (2..8 slots) whose slots, one 8-byte barrier

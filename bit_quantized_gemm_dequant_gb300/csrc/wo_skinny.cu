@@ -162,26 +162,59 @@ wo_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       }
     }
   };
+  // With static weights (the caller's promise that no kernel still running
+  // writes W), the first round's weight boxes go straight into the ring
+  // while the previous kernel of the stream may still be running; their
+  // activation boxes, which that kernel may be writing, follow the wait.
+  int early = 0;
+  int early_m[D], early_c[D];
   if (lane == 0) {
     tc::tma_prefetch_desc(&tmW);
     tc::tma_prefetch_desc(&tmX);
-    // Pull the warp's first weight boxes into L2 while the previous kernel of
-    // the stream may still be running (a prefetch cannot read stale data).
-    int pn = cur_n, pc = cur_c;
-    for (int k = 0; k < D && k < n_mine; ++k) {
-      tc::tma_prefetch_l2_2d(&tmW, pn * kTileN, pc * kBoxRows);
-      pc += kWarps;
-      while (pc >= ch) {
-        pc -= ch;
-        if (++pn == pl.n_tiles) pn = 0;
+    if (p.early_w) {
+#pragma unroll
+      for (int k = 0; k < D; ++k) {
+        if (k >= n_mine) break;
+        uint8_t* slot = ring + (warp * D + k) * C::kSlotBytes;
+        tc::mbar_arrive_expect_tx(&full[warp * D + k], kWBytes + C::kXBytes);
+        tc::tma_load_2d(slot, &tmW, cur_n * kTileN, cur_c * kBoxRows, &full[warp * D + k]);
+        early_m[k] = cur_m;
+        early_c[k] = cur_c;
+        early = k + 1;
+        cur_c += kWarps;
+        while (cur_c >= ch) {
+          cur_c -= ch;
+          if (++cur_n == pl.n_tiles) {
+            cur_n = 0;
+            ++cur_m;
+          }
+        }
+      }
+    } else {
+      // Pull the warp's first weight boxes into L2 while the previous kernel
+      // of the stream may still be running (a prefetch cannot read stale data).
+      int pn = cur_n, pc = cur_c;
+      for (int k = 0; k < D && k < n_mine; ++k) {
+        tc::tma_prefetch_l2_2d(&tmW, pn * kTileN, pc * kBoxRows);
+        pc += kWarps;
+        while (pc >= ch) {
+          pc -= ch;
+          if (++pn == pl.n_tiles) pn = 0;
+        }
       }
     }
   }
   // Everything below reads inputs or writes outputs and workspace that
   // earlier work in the stream may still own.
   tc::griddep_wait();
-  if (lane == 0)
-    for (int k = 0; k < D && k < n_mine; ++k) issue(k);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < D; ++k)
+      if (k < early)
+        tc::tma_load_2d(ring + (warp * D + k) * C::kSlotBytes + kWBytes, &tmX, early_c[k] * C::kChunkK,
+                        early_m[k] * C::kRows, &full[warp * D + k]);
+    for (int k = early; k < D && k < n_mine; ++k) issue(k);
+  }
 
   int* ws_count = static_cast<int*>(p.ws);
   float4* ws_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(p.ws) + kCounterBytes);
@@ -572,7 +605,7 @@ SkinnyPlan plan_skinny(int M, int N, int K, int mode) {
 cudaError_t launch_wo_skinny(const WoArgs& a, int bits, const SkinnyPlan& pl, cudaStream_t s) {
   if (a.K == 0) return cudaMemset2DAsync(a.Y, a.ldy * 2, 0, static_cast<size_t>(a.N) * 2, a.M, s);
   const SkinnyArgs sa{a.M, a.N, a.K, a.X, a.ldx, a.W, a.ldw, a.scales, 1.0f, a.Y, a.ldy, a.ws, a.zeros, a.group_n,
-                      skinny_wait_ns()};
+                      skinny_wait_ns(), static_weights() ? 1 : 0};
   return bits == 4 ? launch_mode<kInt4>(sa, pl, s) : launch_mode<kInt8>(sa, pl, s);
 }
 

@@ -29,6 +29,8 @@ std::atomic<uint64_t> g_skinny_wait_ns{2000000000ull};
 }  // namespace
 
 uint64_t skinny_wait_ns() { return g_skinny_wait_ns.load(std::memory_order_relaxed); }
+std::atomic<int> g_static_weights{0};
+bool static_weights() { return g_static_weights.load(std::memory_order_relaxed) != 0; }
 
 int current_device() {
   int d = 0;
@@ -452,6 +454,10 @@ int wq_get_device_error(wq_stream_t stream, int* site) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return WQ_ERR_LAUNCH;
   if (site) *site = host;
   return host ? WQ_ERR_DEVICE : WQ_OK;
+}
+
+int wq_set_static_weights(int enable) {
+  return g_static_weights.exchange(enable ? 1 : 0, std::memory_order_relaxed);
 }
 
 int wq_debug_set_wait_limit(int64_t ns) {

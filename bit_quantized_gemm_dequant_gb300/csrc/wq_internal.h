@@ -50,6 +50,9 @@ class PerDevice {
 // Limit of the skinny kernels' bounded waits (2 s unless a test shortened it
 // with wq_debug_set_wait_limit).
 uint64_t skinny_wait_ns();
+// wq_set_static_weights: whether callers promised that no kernel still
+// running when a weight-only call launches writes its weights or scales.
+bool static_weights();
 
 // Device error word written by kernels whose bounded waits give up.  Lives in
 // wq_api.cu; kernels receive its device address as a parameter.

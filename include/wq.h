@@ -499,6 +499,27 @@ const char* wq_status_string(int status);
 int wq_get_device_error(wq_stream_t stream, int* site);
 
 /*
+ * wq_set_static_weights — the caller's promise that weights are static.
+ *
+ * Off by default.  With enable != 0 the caller promises that, for every
+ * later call of wq_gemm_w4a16, wq_gemm_w8a16 and their _grouped and
+ * _noalloc forms, no kernel that may still be running when the call is
+ * launched writes its weight array (Wq / W) or its scales and zero points:
+ * the weights are loaded once and only read afterwards, as in inference.
+ * The decode (M <= 16) kernels then start loading their first weight boxes
+ * into shared memory while the kernel before them on the stream is still
+ * finishing (they are launched as programmatic dependents), instead of only
+ * prefetching them into L2; activations are still read, and outputs
+ * written, only after that kernel has completed.  Results are identical
+ * either way.  Breaking the promise (writing a weight array in a kernel
+ * that overlaps a later call) can make that call compute with stale
+ * weights.  Process-wide; applies to calls launched afterwards, from any
+ * host thread.  Returns the previous setting (0 or 1).  The pages have no
+ * counterpart: it is a launch-overlap switch, not a new operation.
+ */
+int wq_set_static_weights(int enable);
+
+/*
  * wq_debug_set_wait_limit — testing hook: the limit (in nanoseconds) after
  * which the skinny weight-stream kernels (wq_gemm_w4a16, wq_gemm_w8a16, their
  * _grouped, _noalloc and _batched forms, and fp8_gemm at M <= 16) give up a
