@@ -45,7 +45,8 @@ constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // 54 KB (multiple of
 constexpr int kAccCols = BN;                // FP32 accumulator columns
 constexpr int kTmemCols = 512;              // accumulator + 4 stages of scale columns, rounded up
 constexpr int kThreads = 192;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+constexpr int kBarOffset = kStages * kStageBytes;  // barriers after the ring
+constexpr int kSmemBytes = kBarOffset + 1024 + 1024;
 
 // The two FP4 formats.  MXFP4: 32-element blocks with E8M0 scales, 8 scale
 // bytes per row per K step (two chunks per row group), scales in pairs per
@@ -72,7 +73,10 @@ static_assert(kAccCols + kStages * Fmt<false>::kSfCols <= kTmemCols, "TMEM budge
 // tile's splits are one thread-block cluster and add their partial tiles in
 // distributed shared memory, in rank order: the result is deterministic.
 constexpr int kMaxSplits = 8;
-static_assert(BM * BN * 4 <= kStages * kStageBytes, "a partial tile fits in the idle ring");
+// The receive area recv[S][ceil(BM / S)][BN / 4] float4 fits in the idle ring
+// for every S (S ceil(BM / S) <= BM + S - 1).
+static_assert((BM + kMaxSplits - 1) * BN * 4 <= kStages * kStageBytes, "receive area fits in the idle ring");
+constexpr int kRxBarOffset = 256;  // the receive barrier's byte offset in the barrier area
 
 int mx_splits(int M, int N, int K) {
   const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
@@ -345,12 +349,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint64_t* empty = full + kStages;
   uint64_t* accum = empty + kStages;
   uint64_t* drain = accum + 1;  // MMAs in flight after a give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Split K: counts the peers' parts of this CTA's rows as they arrive.
+  uint64_t* rx_bar = reinterpret_cast<uint64_t*>(smem + kBarOffset + kRxBarOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -367,6 +373,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     tc::mbar_init(accum, 1);
     tc::mbar_init(drain, 1);
+    if (gridDim.z > 1) {
+      // Armed now, long before any peer sends (after the cluster barrier that
+      // follows every CTA's MMAs): (S - 1) parts of this CTA's rows.
+      const int S = gridDim.z, rank = static_cast<int>(blockIdx.z);
+      const int rows = (rank + 1) * BM / S - rank * BM / S;
+      tc::mbar_init(rx_bar, 1);
+      tc::mbar_arrive_expect_tx(rx_bar, static_cast<uint32_t>((S - 1) * rows * BN * 4));
+    }
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -454,78 +468,99 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const float gs = tensor_scale<kNv>(p);
     const bool ok = tc::mbar_wait(accum, 0, abort, err, kSiteGemmEpilogue);
     tc::tc_fence_after();
-    const int q = warp & 3;
-    const int row_l = 32 * q + lane, row = m0 + row_l;
-    // Split K (a cluster of gridDim.z CTAs): park the FP32 partial tile in
-    // the idle ring (every load has landed and every MMA has completed); the
-    // cluster adds the parts below.  Row r is BN / 4 float4s; within each
-    // group of 8 (32 columns) the float4 v sits at slot (v + r) % 8, so the
-    // eight lanes of a 128-bit store phase (eight rows) hit eight different
-    // bank groups.
-    const int S = gridDim.z;
-    float4* part = reinterpret_cast<float4*>(smem);
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
-      tc::tmem_ld_wait();
-      if (S > 1) {
+    // Split K: the accumulator stays in tensor memory until the cluster
+    // exchange below.
+    if (gridDim.z == 1) {
+      const int q = warp & 3;
+      const int row = m0 + 32 * q + lane;
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
+        tc::tmem_ld_wait();
+        if (!ok) continue;
+        if constexpr (kNv) {
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          part[row_l * (BN / 4) + 8 * c + ((v + row_l) & 7)] =
-              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
-                          __uint_as_float(r[4 * v + 3]));
-        continue;
-      }
-      if (!ok) continue;
-      if constexpr (kNv) {
+          for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gs);
+        }
+        if (row >= p.M) continue;
+        const int col0 = n0 + 32 * c;
+        float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+        if (col0 + 32 <= p.N) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gs);
-      }
-      if (row >= p.M) continue;
-      const int col0 = n0 + 32 * c;
-      float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col0;
-      if (col0 + 32 <= p.N) {
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<uint4*>(dst + 4 * v) = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        } else {
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<uint4*>(dst + 4 * v) = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (col0 + t < p.N) dst[t] = __uint_as_float(r[t]);
+          for (int t = 0; t < 32; ++t)
+            if (col0 + t < p.N) dst[t] = __uint_as_float(r[t]);
+        }
       }
     }
   }
   tc::tc_fence_before();
   tc::cta_barrier();
   if (gridDim.z > 1) {
-    // Every CTA of the cluster gets here (all its waits are bounded), so both
-    // cluster barriers end.  First: every partial tile is in place.
-    tc::cluster_sync_all();
+    // Split K over the S CTAs of the cluster: rank k finishes rows
+    // [k BM / S, (k + 1) BM / S) of the tile.  Every CTA gets here (all its
+    // waits are bounded).  After the cluster barrier every CTA's MMAs are
+    // done, so every ring is idle and becomes the receive area
+    // recv[S][rmax][BN / 4]: part j of the owner's rows from rank j, the
+    // float4s of each 32-column group rotated by the row (conflict-free
+    // stores and loads).  Each epilogue warp sends its 32 accumulator rows
+    // straight from tensor memory to their owners with one-way stores that
+    // count toward the owner's receive barrier (its own rows with plain
+    // stores); no CTA reads another's shared memory, so none waits for its
+    // peers before leaving.  The owner adds the S parts in rank order, so the
+    // result does not depend on arrival order.  (Pulling the parts with
+    // loads, or sending row blocks with bulk copies, measured no faster: the
+    // 96 KB each CTA exchanges at S = 4 is bound by the cluster network.)
     const int S = gridDim.z, rank = static_cast<int>(tc::cluster_ctarank());
-    const int r0 = rank * BM / S, r1 = (rank + 1) * BM / S;
-    const float4* part = reinterpret_cast<const float4*>(smem);
-    const float4* peer[kMaxSplits];
+    const int rmax = (BM + S - 1) / S;
+    tc::cluster_sync_all();
+    tc::tc_fence_after();
+    float4* recv = reinterpret_cast<float4*>(smem);
+    if (warp >= 2) {
+      const int q = warp & 3;
+      const int row = 32 * q + lane;                 // tile row = TMEM lane
+      const int k = ((row + 1) * S - 1) / BM;         // its owner
+      const int lr = row - k * BM / S;                // row within the owner's rows
+      const int base = (rank * rmax + lr) * (BN / 4);  // this part's row in the owner's recv
+      const uint32_t peer_recv = tc::dsmem_addr(recv, k);
+      const uint32_t peer_bar = tc::dsmem_addr(rx_bar, k);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
+        tc::tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < kMaxSplits; ++j) peer[j] = tc::peer_ptr(part, j < S ? j : 0);
+        for (int v = 0; v < 8; ++v) {
+          const int slot = base + 8 * c + ((v + lr) & 7);
+          const float4 val = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          if (k == rank) recv[slot] = val;
+          else tc::st_async_f4(peer_recv + 16u * static_cast<uint32_t>(slot), val, peer_bar);
+        }
+      }
+    }
+    tc::cta_barrier();  // this CTA's own part is in place
+    // The peers' parts (bounded wait; the peers always send, so the wait
+    // normally ends; a CTA that gives up leaves without storing).
+    const bool got = tc::mbar_wait_cluster(rx_bar, 0, err, kSiteClusterRecv);
     const float gs = tensor_scale<kNv>(p);
-    const bool live = !*abort;
-    // Rows r0 .. r1 - 1 of the tile, four columns per item: the S parts added
-    // in rank order (deterministic), then the tensor scales (NVFP4).
-    for (int it = threadIdx.x; it < (r1 - r0) * (BN / 4); it += blockDim.x) {
-      const int rr = r0 + it / (BN / 4), c4 = it % (BN / 4);
-      const int slot = rr * (BN / 4) + (c4 & ~7) + (((c4 & 7) + rr) & 7);  // the parking rotation
-      float4 v[kMaxSplits];
-#pragma unroll
-      for (int j = 0; j < kMaxSplits; ++j)
-        if (j < S) v[j] = peer[j][slot];
+    const bool live = got && !*abort;
+    const int r0 = rank * BM / S, rows = (rank + 1) * BM / S - r0;
+    const int n_items = rows * (BN / 4);
+    for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
+      const int lr = it / (BN / 4), c4 = it % (BN / 4);
+      const int slot = lr * (BN / 4) + (c4 & ~7) + (((c4 & 7) + lr) & 7);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < kMaxSplits; ++j)
         if (j < S) {
-          acc.x += v[j].x;
-          acc.y += v[j].y;
-          acc.z += v[j].z;
-          acc.w += v[j].w;
+          const float4 v = recv[j * rmax * (BN / 4) + slot];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
         }
       if constexpr (kNv) {
         acc.x *= gs;
@@ -533,7 +568,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         acc.z *= gs;
         acc.w *= gs;
       }
-      const int row = m0 + rr, col = n0 + 4 * c4;
+      const int row = m0 + r0 + lr, col = n0 + 4 * c4;
       if (!live || row >= p.M || col >= p.N) continue;
       float* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
       if (col + 4 <= p.N) {
@@ -545,9 +580,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (col + t < p.N) dst[t] = a4[t];
       }
     }
-    // Second: no CTA leaves (releasing its shared memory) while a peer may
-    // still read its partial tile.
-    tc::cluster_sync_all();
   }
   if (warp == 1) {
     tc::tc_fence_after();
@@ -600,7 +632,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;     // MMA -> epilogue
   uint64_t* acc_empty = acc_full + 1;       // epilogue warps -> MMA
