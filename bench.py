@@ -547,17 +547,17 @@ FP8_SOURCES = ("bit_quantized_gemm_dequant_gb300/csrc/gemm_fp8.cu",
                "bit_quantized_gemm_dequant_gb300/csrc/wq_internal.h")
 CAPTURED_TRAFFIC = {
     "w8a16_16x4096x14336":
-        {"bytes": 58_928_640 + 70_400, "sources": SKINNY_SOURCES, "sha256": "0012c4e4480b5913ea94e04d9d782aca4a797f80180c6c7af3290f0a3e2b85c8"},
+        {"bytes": 58_932_224 + 81_920, "sources": SKINNY_SOURCES, "sha256": "dd7eac26bf5a279150b6c656275224f6bb697d7a1366c5dff68949f92c906d52"},
     "w8a16_batched_1x4096x4096+4x4096x4096+16x4096x4096+1x4096x14336+4x4096x14336+16x4096x14336":
-        {"bytes": 227_880_704 + 5_643_776, "sources": BATCHED_SOURCES, "sha256": "fb11efdcfa21174e7bb33e576a97be592795b111cc459230fff55d447cdca3bb"},
+        {"bytes": 227_881_216 + 5_397_248, "sources": BATCHED_SOURCES, "sha256": "d2feb37b479c0b3921272d36160bed0a59aaf9ff653ecd9cf3bb821d99568f9e"},
     "w4a16_64x4096x11008":
-        {"bytes": 23_121_408 + 0, "sources": WO_GEMM_SOURCES, "sha256": "45782ffb76b9a8b537c105903b0d991a79009bd3bdc6b13d451be3c6779c16a2"},
+        {"bytes": 23_121_664 + 0, "sources": WO_GEMM_SOURCES, "sha256": "017da18f0fc221b5ab0d5beb4f93f8975fb361416a83d6b69797023eac01d3ef"},
     "mx_gemm_2048x8192x8192":
-        {"bytes": 44_647_936 + 15_960_064, "sources": FP4_GEMM_SOURCES, "sha256": "e2c064d11fb4b89c173db68610bb11c8dad0faccc18a5fe208a77b91ef5a88cb"},
+        {"bytes": 44_646_656 + 15_137_792, "sources": FP4_GEMM_SOURCES, "sha256": "d892f4919e9fa7b16feb14300108738acf536c355b0d4e2548962ae4f2484849"},
     "nv_gemm_2048x8192x8192":
-        {"bytes": 47_286_528 + 17_582_336, "sources": FP4_GEMM_SOURCES, "sha256": "e2c064d11fb4b89c173db68610bb11c8dad0faccc18a5fe208a77b91ef5a88cb"},
+        {"bytes": 47_281_664 + 16_409_088, "sources": FP4_GEMM_SOURCES, "sha256": "d892f4919e9fa7b16feb14300108738acf536c355b0d4e2548962ae4f2484849"},
     "fp8_4096x4096x4096":
-        {"bytes": 33_621_760 + 259_072, "sources": FP8_SOURCES, "sha256": "97433e6524ab3783edb8efbc49fc0dc567493b7763dadc8187e0dfd292484d1a"},
+        {"bytes": 33_626_624 + 254_976, "sources": FP8_SOURCES, "sha256": "101e16716de9de9b413c1c83d254b1cf462789da220821dbfe47f0d7f370f056"},
 }
 
 
