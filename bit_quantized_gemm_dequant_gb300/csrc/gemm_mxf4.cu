@@ -78,11 +78,19 @@ constexpr int kMaxSplits = 8;
 static_assert((BM + kMaxSplits - 1) * BN * 4 <= kStages * kStageBytes, "receive area fits in the idle ring");
 constexpr int kRxBarOffset = 256;  // the receive barrier's byte offset in the barrier area
 
+// Returns 0 when the 128 x 256 tiles fill half the GPU (the persistent
+// kernel); otherwise the number of K splits of the narrow kernel, whose tiles
+// are 128 x kNarrowN: half-width tiles give twice the CTAs for the same split
+// and a third of the partial bytes exchanged in the cluster (which that
+// exchange is bound by).
+constexpr int kNarrowN = 128;
+
 int mx_splits(int M, int N, int K) {
-  const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
-  const int kt = (K / 2 + BKB - 1) / BKB;
+  const int m_tiles = (M + BM - 1) / BM;
   const int sms = sm_count();
-  if (2 * tiles >= sms) return 1;
+  if (2 * ((N + BN - 1) / BN) * m_tiles >= sms) return 0;
+  const int tiles = ((N + kNarrowN - 1) / kNarrowN) * m_tiles;
+  const int kt = (K / 2 + BKB - 1) / BKB;
   int S = sms / tiles;
   if (S > kt / 4) S = kt / 4;
   if (S > kMaxSplits) S = kMaxSplits;
@@ -96,7 +104,9 @@ static_assert(kStageBytes % 1024 == 0, "stage alignment");
 // padded to a multiple of 256, so both exist), the order mma_step copies into
 // TMEM.  The W half and the A half are issued separately, so that a launch
 // that quantizes A first can start W's stream before A exists.
-template <bool kNv>
+// TN: the tile's width (W rows), 256 or 128; a 128-wide tile takes only the
+// first W half of the stage and of the scale area.
+template <bool kNv, int TN = BN>
 __device__ __forceinline__ void load_stage_w(uint8_t* st, const CUtensorMap* tmW, const MxGemmArgs& p, int n0, int kt,
                                              uint64_t* bar) {
   constexpr uint32_t kPiece = Fmt<kNv>::kPiece;
@@ -105,7 +115,7 @@ __device__ __forceinline__ void load_stage_w(uint8_t* st, const CUtensorMap* tmW
   const uint8_t* w = p.SW + ((n0 / 128) * chunks + static_cast<int64_t>(kt) * Fmt<kNv>::kWords) * kSfChunk;
   uint8_t* sf = st + kABytes + kBBytes;
   tc::bulk_load(sf + kPiece, w, kPiece, bar);
-  tc::bulk_load(sf + 2 * kPiece, w + chunks * kSfChunk, kPiece, bar);
+  if (TN == 256) tc::bulk_load(sf + 2 * kPiece, w + chunks * kSfChunk, kPiece, bar);
 }
 
 template <bool kNv>
@@ -118,7 +128,9 @@ __device__ __forceinline__ void load_stage_a(uint8_t* st, const CUtensorMap* tmA
                 Fmt<kNv>::kPiece, bar);
 }
 
-__host__ __device__ constexpr uint32_t stage_tx(bool nv) { return kABytes + kBBytes + 3 * (nv ? Fmt<true>::kPiece : Fmt<false>::kPiece); }
+__host__ __device__ constexpr uint32_t stage_tx(bool nv, int tn = BN) {
+  return kABytes + tn * BKB + (1 + tn / 128) * (nv ? Fmt<true>::kPiece : Fmt<false>::kPiece);
+}
 
 // One K step on the tensor cores: copy the stage's scale chunks into its TMEM
 // columns, then four 128 x 256 x 64 block-scaled MMAs.
@@ -129,12 +141,14 @@ __host__ __device__ constexpr uint32_t stage_tx(bool nv) { return kABytes + kBBy
 //          0-127).
 //   NVFP4: TMEM [A j=0..3][W 0-127 j=0][W 128-255 j=0] .. [W 0-127 j=3][W 128-255 j=3];
 //          MMA j takes the whole word of column 4 j (A) and 16 + 8 j (W).
-template <bool kNv>
+// A 128-wide tile (TN = 128) copies only A's and W rows 0-127's chunks (the
+// first two thirds of the scale area) and issues 128 x 128 x 64 MMAs.
+template <bool kNv, int TN = BN>
 __device__ __forceinline__ void mma_step(uint32_t tmem, uint32_t a, uint32_t b, uint32_t sf, uint32_t sf_col,
                                          bool first) {
   if constexpr (!kNv) {
 #pragma unroll
-    for (int c = 0; c < 6; ++c) {
+    for (int c = 0; c < (TN == 256 ? 6 : 4); ++c) {
       const int pos = (c == 3 || c == 4) ? 7 - c : c;  // chunk order 0, 1, 2, 4, 3, 5
       tc::tmem_cp_32x128b_warpx4(sf_col + 4 * pos, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
     }
@@ -143,12 +157,12 @@ __device__ __forceinline__ void mma_step(uint32_t tmem, uint32_t a, uint32_t b, 
       const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
       const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
       const uint32_t id = 2 * (j & 1);
-      const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, id, id);
+      const uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, TN, id, id);
       tc::mma_mxf4(tmem, adesc, bdesc, idesc, sf_col + 4 * (j >> 1), sf_col + 8 + 8 * (j >> 1), !first || j != 0);
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < 12; ++c) {
+    for (int c = 0; c < (TN == 256 ? 12 : 8); ++c) {
       const int grp = c / 4, j = c % 4;
       const int col = grp == 0 ? 4 * j : 16 + 8 * j + (grp == 2 ? 4 : 0);
       tc::tmem_cp_32x128b_warpx4(sf_col + col, tc::smem_desc(sf + c * kSfChunk, 16, 128, tc::kSwizzleNone));
@@ -157,7 +171,7 @@ __device__ __forceinline__ void mma_step(uint32_t tmem, uint32_t a, uint32_t b, 
     for (int j = 0; j < 4; ++j) {
       const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
       const uint64_t bdesc = tc::smem_desc(b + 32 * j, 1024, 1024, tc::kSwizzle128B);
-      constexpr uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, BN, 0, 0, /*UE4M3*/ 0);
+      constexpr uint32_t idesc = tc::idesc_block_scaled(/*E2M1*/ 1, /*E2M1*/ 1, BM, TN, 0, 0, /*UE4M3*/ 0);
       tc::mma_mxf4nvf4_4x(tmem, adesc, bdesc, idesc, sf_col + 4 * j, sf_col + 16 + 8 * j, !first || j != 0);
     }
   }
@@ -343,7 +357,7 @@ __device__ __forceinline__ void warp_transpose32(uint32_t (&v)[32], int lane) {
   }
 }
 
-template <bool kNv, bool kQA>
+template <bool kNv, bool kQA, int TN>
 __global__ void __launch_bounds__(kThreads, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, MxGemmArgs p,
                int* err) {
@@ -359,7 +373,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* rx_bar = reinterpret_cast<uint64_t*>(smem + kBarOffset + kRxBarOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * TN;
   // K steps [kt0, kt1) of this CTA: all of K, or split z of gridDim.z.
   const int KT_all = (p.K / 2 + BKB - 1) / BKB;
   const int kt0 = static_cast<int>(static_cast<int64_t>(blockIdx.z) * KT_all / gridDim.z);
@@ -379,7 +393,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int S = gridDim.z, rank = static_cast<int>(blockIdx.z);
       const int rows = (rank + 1) * BM / S - rank * BM / S;
       tc::mbar_init(rx_bar, 1);
-      tc::mbar_arrive_expect_tx(rx_bar, static_cast<uint32_t>((S - 1) * rows * BN * 4));
+      tc::mbar_arrive_expect_tx(rx_bar, static_cast<uint32_t>((S - 1) * rows * TN * 4));
     }
     *abort = 0;
     tc::fence_mbar_init();
@@ -402,8 +416,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (warp == 0 && lane == 0) {
       tc::tma_prefetch_desc(&tmW);
       for (int i = 0; i < pre; ++i) {
-        tc::mbar_arrive_expect_tx(&full[i], stage_tx(kNv));
-        load_stage_w<kNv>(smem + i * kStageBytes, &tmW, p, n0, kt0 + i, &full[i]);
+        tc::mbar_arrive_expect_tx(&full[i], stage_tx(kNv, TN));
+        load_stage_w<kNv, TN>(smem + i * kStageBytes, &tmW, p, n0, kt0 + i, &full[i]);
       }
     }
     quantize_a_share(p);
@@ -435,9 +449,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool free_slot = tc::mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer);
       if (!__all_sync(0xffffffffu, free_slot)) break;  // warp-uniform exit
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(&full[s], stage_tx(kNv));
+        tc::mbar_arrive_expect_tx(&full[s], stage_tx(kNv, TN));
         load_stage_a<kNv>(st, &tmA, p, m0, kt, &full[s]);
-        load_stage_w<kNv>(st, &tmW, p, n0, kt, &full[s]);
+        load_stage_w<kNv, TN>(st, &tmW, p, n0, kt, &full[s]);
       }
       issued = i + 1;
     }
@@ -454,7 +468,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t b = a + kABytes;
       const uint32_t sf = b + kBBytes;
       const uint32_t sf_col = tmem + kAccCols + s * Fmt<kNv>::kSfCols;
-      mma_step<kNv>(tmem, a, b, sf, sf_col, i == 0);
+      mma_step<kNv, TN>(tmem, a, b, sf, sf_col, i == 0);
       tc::tc_commit(&empty[s]);
     }
     tc::tc_commit(accum);
@@ -473,7 +487,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (gridDim.z == 1) {
       const int q = warp & 3;
       const int row = m0 + 32 * q + lane;
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < TN / 32; ++c) {
         uint32_t r[32];
         tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
         tc::tmem_ld_wait();
@@ -504,7 +518,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // [k BM / S, (k + 1) BM / S) of the tile.  Every CTA gets here (all its
     // waits are bounded).  After the cluster barrier every CTA's MMAs are
     // done, so every ring is idle and becomes the receive area
-    // recv[S][rmax][BN / 4]: part j of the owner's rows from rank j, the
+    // recv[S][rmax][TN / 4]: part j of the owner's rows from rank j, the
     // float4s of each 32-column group rotated by the row (conflict-free
     // stores and loads).  Each epilogue warp sends its 32 accumulator rows
     // straight from tensor memory to their owners with one-way stores that
@@ -524,10 +538,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int row = 32 * q + lane;                 // tile row = TMEM lane
       const int k = ((row + 1) * S - 1) / BM;         // its owner
       const int lr = row - k * BM / S;                // row within the owner's rows
-      const int base = (rank * rmax + lr) * (BN / 4);  // this part's row in the owner's recv
+      const int base = (rank * rmax + lr) * (TN / 4);  // this part's row in the owner's recv
       const uint32_t peer_recv = tc::dsmem_addr(recv, k);
       const uint32_t peer_bar = tc::dsmem_addr(rx_bar, k);
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < TN / 32; ++c) {
         uint32_t r[32];
         tc::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, r);
         tc::tmem_ld_wait();
@@ -548,15 +562,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const float gs = tensor_scale<kNv>(p);
     const bool live = got && !*abort;
     const int r0 = rank * BM / S, rows = (rank + 1) * BM / S - r0;
-    const int n_items = rows * (BN / 4);
+    const int n_items = rows * (TN / 4);
     for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
-      const int lr = it / (BN / 4), c4 = it % (BN / 4);
-      const int slot = lr * (BN / 4) + (c4 & ~7) + (((c4 & 7) + lr) & 7);
+      const int lr = it / (TN / 4), c4 = it % (TN / 4);
+      const int slot = lr * (TN / 4) + (c4 & ~7) + (((c4 & 7) + lr) & 7);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < kMaxSplits; ++j)
         if (j < S) {
-          const float4 v = recv[j * rmax * (BN / 4) + slot];
+          const float4 v = recv[j * rmax * (TN / 4) + slot];
           acc.x += v.x;
           acc.y += v.y;
           acc.z += v.z;
@@ -816,15 +830,19 @@ template <bool kNv, bool kQA = false>
 cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
   if (a.K == 0)
     return cudaMemset2DAsync(a.C, a.ldc * 4, 0, static_cast<size_t>(a.N) * 4, a.M, s);
+  // splits == 0: the persistent kernel on 128 x 256 tiles; otherwise the
+  // narrow kernel on 128 x 128 tiles, K split over `splits` CTAs.
+  int splits = mx_splits(a.M, a.N, a.K);
+  const int tn = splits == 0 ? BN : kNarrowN;
   CUtensorMap tA, tW;
   cudaError_t e = kQA ? make_tmap_2d(&tA, a.Aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.ldq, BKB, BM,
                                      CU_TENSOR_MAP_SWIZZLE_128B)
                       : make_tmap_2d(&tA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.M, a.lda, BKB, BM,
                                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.N, a.ldw, BKB, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  e = make_tmap_2d(&tW, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.K / 2, a.N, a.ldw, BKB, tn, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  int splits = mx_splits(a.M, a.N, a.K);
+  const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + tn - 1) / tn, tiles = m_tiles * n_tiles;
   // Both kernels start as programmatic dependents of the launch before them
   // (normally the scale re-layout) and wait for it before touching memory.
   cudaLaunchConfig_t cfg = {};
@@ -836,18 +854,34 @@ cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
   else attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kern = mx_gemm_kernel<kNv, kQA>;
+  if (splits == 0) {  // persistent: one CTA per SM
+    auto pk = mx_gemm_persistent<kNv, kQA>;
+    static PerDevice<bool> pconfigured;
+    bool pdone = false;
+    if (!pconfigured.get(pdone, [&](bool& v) {
+          e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+          v = true;
+          return e == cudaSuccess;
+        }))
+      return e;
+    cfg.blockDim = dim3(kPThreads);
+    cfg.gridDim = dim3(tiles < sm_count() ? tiles : sm_count());
+    e = cudaLaunchKernelEx(&cfg, pk, tA, tW, a, device_error_word());
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  auto kern = mx_gemm_kernel<kNv, kQA, kNarrowN>;
   static PerDevice<bool> configured;
   bool done = false;
-  if (splits > 1 &&
-      !configured.get(done, [&](bool& v) {
+  if (!configured.get(done, [&](bool& v) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         v = true;
         return e == cudaSuccess;
       }))
     return e;
-  const int tiles = ((a.N + BN - 1) / BN) * ((a.M + BM - 1) / BM);
   if (kQA) {
+    // The cooperative launch needs every cluster resident at once.  (With
+    // at most 2 x 76 narrow tiles the grid of a split of 1 is one wave.)
     for (; splits > 1; --splits) {
       cudaLaunchConfig_t q = cfg;
       cudaLaunchAttribute ca[1];
@@ -858,35 +892,22 @@ cudaError_t launch_fp4_gemm(const MxGemmArgs& a, cudaStream_t s) {
       q.attrs = ca;
       q.numAttrs = 1;
       q.blockDim = dim3(kThreads);
-      q.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
+      q.gridDim = dim3(n_tiles, m_tiles, splits);
       int clusters = 0;
       if (cudaOccupancyMaxActiveClusters(&clusters, kern, &q) == cudaSuccess && clusters >= tiles) break;
     }
   }
-  cfg.blockDim = dim3(splits == 1 ? kPThreads : kThreads);
-  if (splits == 1) {  // persistent: one CTA per SM
-    auto pk = mx_gemm_persistent<kNv, kQA>;
-    static PerDevice<bool> pconfigured;
-    bool pdone = false;
-    if (!pconfigured.get(pdone, [&](bool& v) {
-          e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-          v = true;
-          return e == cudaSuccess;
-        }))
-      return e;
-    cfg.gridDim = dim3(tiles < sm_count() ? tiles : sm_count());
-    e = cudaLaunchKernelEx(&cfg, pk, tA, tW, a, device_error_word());
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-  }
   // Split K: each tile's splits form a thread-block cluster (along z) that
   // adds its partial tiles in distributed shared memory.
-  cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, splits);
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = splits;
-  cfg.numAttrs = 2;
+  cfg.blockDim = dim3(kThreads);
+  cfg.gridDim = dim3(n_tiles, m_tiles, splits);
+  if (splits > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = splits;
+    cfg.numAttrs = 2;
+  }
   e = cudaLaunchKernelEx(&cfg, kern, tA, tW, a, device_error_word());
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
