@@ -553,9 +553,9 @@ CAPTURED_TRAFFIC = {
     "w4a16_64x4096x11008":
         {"bytes": 23_121_664 + 0, "sources": WO_GEMM_SOURCES, "sha256": "017da18f0fc221b5ab0d5beb4f93f8975fb361416a83d6b69797023eac01d3ef"},
     "mx_gemm_2048x8192x8192":
-        {"bytes": 44_646_656 + 15_137_792, "sources": FP4_GEMM_SOURCES, "sha256": "d892f4919e9fa7b16feb14300108738acf536c355b0d4e2548962ae4f2484849"},
+        {"bytes": 44_648_448 + 15_944_960, "sources": FP4_GEMM_SOURCES, "sha256": "96193f1a0a2166ceb44388742798903c0bcb9b4f19486fb1b40d3900c01c95bb"},
     "nv_gemm_2048x8192x8192":
-        {"bytes": 47_281_664 + 16_409_088, "sources": FP4_GEMM_SOURCES, "sha256": "d892f4919e9fa7b16feb14300108738acf536c355b0d4e2548962ae4f2484849"},
+        {"bytes": 47_278_336 + 17_590_272, "sources": FP4_GEMM_SOURCES, "sha256": "96193f1a0a2166ceb44388742798903c0bcb9b4f19486fb1b40d3900c01c95bb"},
     "fp8_4096x4096x4096":
         {"bytes": 33_626_624 + 254_976, "sources": FP8_SOURCES, "sha256": "101e16716de9de9b413c1c83d254b1cf462789da220821dbfe47f0d7f370f056"},
 }
