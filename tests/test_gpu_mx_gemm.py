@@ -154,10 +154,12 @@ def test_split_k_cluster_is_deterministic(wq):
     assert_gemm_close(c, ref, "fp32")
 
 
-@pytest.mark.parametrize("M,N,K,ldc", [(1, 2560, 8192, 2564), (100, 300, 2048, 304), (8, 256, 4096, None)])
+@pytest.mark.parametrize("M,N,K,ldc", [(1, 2560, 8192, 2564), (1, 2048, 8192, None), (100, 300, 2048, 304),
+                                     (8, 256, 4096, None)])
 def test_split_k_cluster_ragged(wq, M, N, K, ldc):
-    """Split-K clusters with ragged M and N (the rows and columns past the
-    matrix are neither read nor written), clusters of 8 and a padded ldc."""
+    """Split-K clusters on 128-column tiles with ragged M and N (the rows and
+    columns past the matrix are neither read nor written) and a padded ldc:
+    clusters of 7 (20 tiles), 8 (16 tiles), 2 and 4."""
     a = workloads.mx_source(M, K, seed=M, stream=0)
     w = workloads.mx_source(N, K, seed=N, stream=1)
     ad, asc = O.mx_quantize_fp4(a)
