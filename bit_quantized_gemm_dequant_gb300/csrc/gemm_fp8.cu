@@ -10,8 +10,8 @@
 //   warp 0      TMA producer: A box 128(k) x 128(m) and BN/128 B boxes
 //               128(n) x 128(k), 128-byte swizzle, into a 4-stage ring that
 //               runs continuously across the CTA's tiles.
-//   warp 1      TMEM allocator and MMA issuer: per stage, 4 K-steps x BN/128
-//               tcgen05.mma.kind::f8f6f4 of 128 x 128 x 32 (A K-major, B
+//   warp 1      TMEM allocator and MMA issuer: per stage, 4 K-steps of one
+//               tcgen05.mma.kind::f8f6f4 of 128 x BN x 32 (A K-major, B
 //               MN-major straight from the [K, N] layout, no transpose pass)
 //               into one of two TMEM accumulators; tcgen05.commit frees the
 //               stage and, after the last K step, hands the accumulator over.
@@ -112,7 +112,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
         tc::mbar_wait_drain(&full[i % kStages], (i / kStages) & 1);
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = tc::idesc_dense(/*E4M3*/ 0, /*E4M3*/ 0, /*A K-major*/ 0, /*B MN-major*/ 1, 128, 128);
+    // One 128 x BN x 32 MMA per K slice: A is read once per slice.  B is
+    // MN-major: its BN / 128 swizzle atoms along N are the B boxes, kBHalfBytes
+    // apart (the descriptor's leading byte offset); 8-row K groups are 1 KB
+    // apart (stride byte offset).
+    constexpr uint32_t idesc = tc::idesc_dense(/*E4M3*/ 0, /*E4M3*/ 0, /*A K-major*/ 0, /*B MN-major*/ 1, 128, BN);
     int it = 0, local = 0;
     for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x, ++local) {
       const int buf = local & 1;
@@ -129,11 +133,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
         for (int j = 0; j < BK / 32; ++j) {
           const uint64_t adesc = tc::smem_desc(a + 32 * j, 1024, 1024, tc::kSwizzle128B);
-#pragma unroll
-          for (int h = 0; h < HALVES; ++h) {
-            const uint64_t bdesc = tc::smem_desc(b + h * kBHalfBytes + 32 * 128 * j, 1024, 1024, tc::kSwizzle128B);
-            tc::mma_f8f6f4(acc + 128 * h, adesc, bdesc, idesc, (kt | j) != 0);
-          }
+          const uint64_t bdesc = tc::smem_desc(b + 32 * 128 * j, kBHalfBytes, 1024, tc::kSwizzle128B);
+          tc::mma_f8f6f4(acc, adesc, bdesc, idesc, (kt | j) != 0);
         }
         tc::tc_commit(&empty[s]);
       }
