@@ -152,6 +152,15 @@ __host__ __device__ constexpr uint32_t stage_tx(bool nv, int tn = BN) { return s
 //          MMA j takes the whole word of column 4 j (A) and 16 + 8 j (W).
 // A 128-wide tile (TN = 128) copies only A's and W rows 0-127's chunks (the
 // first two thirds of the scale area) and issues 128 x 128 x 64 MMAs.
+// Four consecutive 32-bit TMEM columns of this warp's 32 lanes (one row per
+// thread), from registers; complete once tmem_st_wait returns.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // First TMEM column (relative to the stage's scale columns) of the stage's
 // scale chunk c, in the scale area's order (A, W rows 0-127, W rows 128-255).
 template <bool kNv>
@@ -865,7 +874,7 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int s = it % kStages;
-          ok = tc::mbar_wait_sleep(&sfull[s], (it / kStages) & 1, abort, err, kSiteGemmScales);
+          ok = tc::mbar_wait_sleep(&sfull[s], (it / kStages) & 1, abort, err, kSiteGemmEpilogue);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -875,10 +884,10 @@ mx_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
           for (int i = 0; i < kHalf; ++i) {
             const int c = h * kHalf + i;
-            tc::tmem_st_32x32b_x4(col + sf_column<kNv>(c),
+            tmem_st_32x32b_x4(col + sf_column<kNv>(c),
                                   *reinterpret_cast<const uint4*>(sf + c * kSfChunk + 16 * lane));
           }
-          tc::tmem_st_wait();
+          tmem_st_wait();
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sf_ready[s]);

@@ -384,15 +384,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Four consecutive 32-bit TMEM columns of this warp's 32 lanes (one row per
-// thread), from registers; complete once tmem_st_wait returns.
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading

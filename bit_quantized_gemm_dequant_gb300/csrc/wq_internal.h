@@ -68,7 +68,6 @@ enum ErrorSite : int {
   kSiteClusterRecv = 5,    // a CTA waited too long for its cluster peers' partial sums
   kSiteBatchRecv = 6,      // a batched-call CTA waited too long for its neighbours' published parts
   kSiteGridBarrier = 7,    // a CTA of the quantize-then-GEMM launch waited too long for the others
-  kSiteGemmScales = 8,     // a GEMM's scale-staging warps waited too long for a stage's scales
 };
 
 struct WoArgs {           // weight-only GEMM (W4A16 / W8A16)
