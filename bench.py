@@ -553,11 +553,11 @@ CAPTURED_TRAFFIC = {
     "w4a16_64x4096x11008":
         {"bytes": 23_121_664 + 0, "sources": WO_GEMM_SOURCES, "sha256": "017da18f0fc221b5ab0d5beb4f93f8975fb361416a83d6b69797023eac01d3ef"},
     "mx_gemm_2048x8192x8192":
-        {"bytes": 44_648_448 + 15_944_960, "sources": FP4_GEMM_SOURCES, "sha256": "96193f1a0a2166ceb44388742798903c0bcb9b4f19486fb1b40d3900c01c95bb"},
+        {"bytes": 44_658_176 + 16_946_944, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
     "nv_gemm_2048x8192x8192":
-        {"bytes": 47_278_336 + 17_590_272, "sources": FP4_GEMM_SOURCES, "sha256": "96193f1a0a2166ceb44388742798903c0bcb9b4f19486fb1b40d3900c01c95bb"},
+        {"bytes": 47_368_192 + 19_126_272, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
     "fp8_4096x4096x4096":
-        {"bytes": 33_626_624 + 254_976, "sources": FP8_SOURCES, "sha256": "101e16716de9de9b413c1c83d254b1cf462789da220821dbfe47f0d7f370f056"},
+        {"bytes": 33_617_664 + 270_336, "sources": FP8_SOURCES, "sha256": "8f643419b8d45943d2d2bfaf2aeaaf830154c17ffe52631ed550bc20dae1b12a"},
 }
 
 
