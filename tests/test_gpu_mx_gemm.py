@@ -69,6 +69,11 @@ def test_per_row_and_per_block_scales(wq):
     (130, 256, 8192, None, None, None, None, None),
     (384, 128, 4096, 2064, 130, 2048, 128, 132),
     (300, 520, 1024, None, None, None, None, None),  # odd number of 128-row tiles, ragged N
+    # The persistent kernel (at least half as many 128 x 256 tiles as SMs),
+    # with more tiles than CTAs, fewer K steps than ring slots, ragged edges:
+    (1300, 4100, 256, None, None, None, None, 4104),  # 187 tiles, one K step
+    (2048, 2560, 800, None, None, None, None, None),  # 160 tiles, partial fourth K step
+    (1030, 5000, 1312, 1312, 48, None, None, None),   # 180 tiles, six K steps, the last partial
 ])
 def test_random_quantized(wq, M, N, K, lda, ldsa, ldw, ldsw, ldc):
     a = workloads.mx_source(M, K, seed=M + K, stream=0)

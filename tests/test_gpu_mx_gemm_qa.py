@@ -44,6 +44,10 @@ def _quantized_a(ws, M, K):
     (128, 8192, 4096, None, None),  # the K-split cluster path
     (300, 520, 1024, None, None),   # three 128-row tiles, ragged N (persistent path)
     (2048, 512, 2048, None, None),
+    # The persistent instance (at least half as many 128 x 256 tiles as SMs):
+    (1300, 4100, 256, None, 4104),  # 187 tiles, one K step
+    (2048, 2560, 800, 804, None),   # 160 tiles, partial fourth K step, padded rows of A
+    (1030, 5000, 1312, None, None), # 180 tiles, six K steps
 ])
 def test_fused_quantize_gemm(wq, M, N, K, lda, ldc):
     a = workloads.mx_source(M, K, seed=M + K, stream=0)

@@ -143,6 +143,12 @@ def test_gemm_per_row_and_per_block_scales(wq):
     (384, 128, 4096, 2064, 272, 2048, 256, 132),
     (300, 520, 1040, 528, None, 528, None, None),     # K not a multiple of 256: partial last step
     (64, 256, 1040, 528, 80, 528, 80, None),          # partial last step, 16-byte scale rows
+    # The persistent kernel (at least half as many 128 x 256 tiles as SMs),
+    # whose epilogue warps stage the scales: more tiles than CTAs, fewer K
+    # steps than ring slots, ragged edges:
+    (1300, 4100, 256, None, None, None, None, 4104),  # 187 tiles, one K step
+    (2048, 2560, 800, None, None, None, None, None),  # 160 tiles, partial fourth K step
+    (1030, 5000, 1312, 1312, 96, None, None, None),   # 180 tiles, six K steps, the last partial
 ])
 def test_gemm_random_quantized(wq, M, N, K, lda, ldsa, ldw, ldsw, ldc):
     a = workloads.mx_source(M, K, seed=M + K, stream=0)
