@@ -37,6 +37,9 @@ def _run(wq, case, lda=None, ldb=None, ldc=None):
     (200, 96, 300, None, 304, 304),      # ragged M, N, K (K below one 128-byte step)
     (257, 640, 520, 656, 528, 528),      # padded leading dimensions
     (384, 1000, 1024, 1008, None, None),
+    # The persistent kernel with more 128 x 256 tiles than CTAs (187), so
+    # both TMEM accumulators take several tiles, with ragged M, N and K:
+    (1300, 1000, 4100, 1008, 4112, 4104),
     (16, 8192, 8192, None, None, None),  # the M = 16 FP8 workload (skinny e4m3 path)
     (3, 99, 300, 112, 304, 304),         # K not a multiple of 4: zero-masked tail bytes of A
     (12, 1000, 520, 1008, 528, 528),     # second MMA column block, ragged N
