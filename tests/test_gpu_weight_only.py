@@ -168,6 +168,7 @@ LARGE_M = [  # (M, K, N, ldx, ldw, ldy): the tensor-memory path (M > 64)
     (257, 1000, 200, 1008, 208, 200),   # ragged M, N, K (K not a multiple of 64)
     (300, 4096, 640, None, None, None),
     (512, 2048, 1024, None, None, None),
+    (2100, 1000, 4100, 1008, 4112, 4104),  # two rounds of CTAs (297 tiles), ragged M, N and K
 ]
 
 
