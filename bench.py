@@ -552,6 +552,8 @@ CAPTURED_TRAFFIC = {
         {"bytes": 227_881_216 + 5_397_248, "sources": BATCHED_SOURCES, "sha256": "d2feb37b479c0b3921272d36160bed0a59aaf9ff653ecd9cf3bb821d99568f9e"},
     "w4a16_64x4096x11008":
         {"bytes": 23_121_664 + 0, "sources": WO_GEMM_SOURCES, "sha256": "017da18f0fc221b5ab0d5beb4f93f8975fb361416a83d6b69797023eac01d3ef"},
+    "mx_gemm_128x8192x8192":
+        {"bytes": 36_239_872 + 2_304, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
     "mx_gemm_2048x8192x8192":
         {"bytes": 44_658_176 + 16_946_944, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
     "nv_gemm_2048x8192x8192":
