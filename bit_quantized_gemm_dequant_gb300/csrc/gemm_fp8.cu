@@ -65,6 +65,20 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const int n_tiles = (p.N + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
   const int KT = (p.K + BK - 1) / BK;
+  // Tile order: bands of kBand row tiles, M fastest within a band.  A round
+  // of tiles then reads kBand row panels of A and a few column panels of B
+  // (about 40 MB at 8192^3) instead of every row panel of A (64 MB), which
+  // L2 could not keep while C streams out.
+  constexpr int kBand = 32;
+  auto band_rows = [&](int t) {
+    const int m_base = t / (kBand * n_tiles) * kBand;
+    return m_tiles - m_base < kBand ? m_tiles - m_base : kBand;
+  };
+  auto tile_m = [&](int t) {
+    const int b = t / (kBand * n_tiles);
+    return b * kBand + (t - b * kBand * n_tiles) % band_rows(t);
+  };
+  auto tile_n = [&](int t) { return (t - t / (kBand * n_tiles) * kBand * n_tiles) / band_rows(t); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -88,14 +102,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Tile t -> (m tile, n tile): consecutive tiles walk down M, so the CTAs
-  // running at the same time share B columns.
+  // Tile t -> (tile_m(t), tile_n(t)): consecutive tiles walk down M within a
+  // band, so the CTAs running at the same time share B columns.
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_desc(&tmA);
     tc::tma_prefetch_desc(&tmB);
     int it = 0, issued = 0;
     for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x) {
-      const int m0 = (t % m_tiles) * BM, n0 = (t / m_tiles) * BN;
+      const int m0 = tile_m(t) * BM, n0 = tile_n(t) * BN;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int s = it % kStages;
         if (!tc::mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, abort, err, kSiteGemmProducer)) break;
@@ -157,7 +171,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const bool ok = tc::mbar_wait(&acc_full[buf], (local >> 1) & 1, abort, err, kSiteGemmEpilogue);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::tc_fence_after();
-      const int m0 = (t % m_tiles) * BM, n0 = (t / m_tiles) * BN;
+      const int m0 = tile_m(t) * BM, n0 = tile_n(t) * BN;
       const int row = m0 + 32 * q + lane;
       const uint32_t acc = tmem + buf * Cfg::kAccCols + (static_cast<uint32_t>(32 * q) << 16);
       for (int c = 0; c < BN / 32; ++c) {
