@@ -558,8 +558,14 @@ CAPTURED_TRAFFIC = {
         {"bytes": 44_658_176 + 16_946_944, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
     "nv_gemm_2048x8192x8192":
         {"bytes": 47_368_192 + 19_126_272, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
+    "mx_gemm_8192x8192x8192":
+        {"bytes": 123_218_432 + 229_491_456, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
+    "nv_gemm_8192x8192x8192":
+        {"bytes": 151_796_992 + 231_795_200, "sources": FP4_GEMM_SOURCES, "sha256": "7e31aaba2391f37b7b6b2c8d9220cc160d19db187ac3d68f7a87b7dd6c5d45be"},
+    "fp8_8192x8192x8192":
+        {"bytes": 214_076_672 + 110_690_816, "sources": FP8_SOURCES, "sha256": "cc4cfe24612f25dd3ab2a6bae7fbdc0ed6040fa71727478b9752671a18d37d5d"},
     "fp8_4096x4096x4096":
-        {"bytes": 33_617_664 + 270_336, "sources": FP8_SOURCES, "sha256": "8f643419b8d45943d2d2bfaf2aeaaf830154c17ffe52631ed550bc20dae1b12a"},
+        {"bytes": 33_620_992 + 288_000, "sources": FP8_SOURCES, "sha256": "cc4cfe24612f25dd3ab2a6bae7fbdc0ed6040fa71727478b9752671a18d37d5d"},
 }
 
 
